@@ -1,0 +1,220 @@
+"""Pure-Python model of the paged, refcounted fork allocator (test infrastructure only).
+
+Restates, as plain list manipulation:
+* ForkKV L2, section 3 (Figure 6, fork analogy): a new agent maps its parent's
+  base-cache pages read-only and pays only for its own residual pages;
+* ForkServe README, "Design vs APC" and "Methods" (CoW tree): fork aliases the
+  parent's page frames at once; live memory is b(L + sum l_i), not b(kL + sum l_i);
+  freeing the parent does not drop the trunk (the child's reference pins it);
+* ForkServe README, adaptive unaligned tail and "Status": the pack path clones
+  the r = L mod P valid rows of the parent's partial last page into a private
+  page of the child (a row copy of n_valid rows, not P).
+
+Policies the pages leave open (fixed here so page ids are deterministic, and
+mirrored bit for bit by the C++ allocator):
+* each pool has a LIFO free stack, initialised so that pops yield 0, 1, 2, ...;
+* freeing walks base pages then residual pages in logical order, pushing a page
+  when its refcount reaches zero;
+* fork without FORK_SHARE_RES allocates fresh residual pages for the whole
+  inherited prefix (the child's adapter gives it different xA rows); with it,
+  full residual pages are aliased and a partial one is copied like the base tail;
+* append copies a partial last page first if it is shared (refcount > 1);
+* sequence ids count up from 0 and are never reused;
+* on any error nothing changes.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence, Tuple
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_OUT_OF_PAGES = -2
+ERR_BAD_PAGE = -3
+ERR_REFCOUNT = -4
+ERR_UNSUPPORTED = -5
+
+JOB_BASE = 0
+JOB_RES = 1
+
+
+class AllocatorError(Exception):
+    def __init__(self, code: int, msg: str = ""):
+        super().__init__(f"{code}: {msg}")
+        self.code = code
+
+
+def _ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+class _Seq:
+    __slots__ = ("length", "base", "res")
+
+    def __init__(self, length: int, base: List[int], res: List[int]):
+        self.length = length
+        self.base = base
+        self.res = res
+
+
+class AllocatorModel:
+    def __init__(self, num_base_pages: int, num_res_pages: int, page_size: int):
+        if num_base_pages < 0 or num_res_pages < 0 or page_size < 1:
+            raise AllocatorError(ERR_INVALID_ARG, "bad pool sizes")
+        self.P = page_size
+        self.base_free = list(range(num_base_pages - 1, -1, -1))
+        self.res_free = list(range(num_res_pages - 1, -1, -1))
+        self.base_ref = [0] * num_base_pages
+        self.res_ref = [0] * num_res_pages
+        self.seqs: Dict[int, _Seq] = {}
+        self.next_id = 0
+
+    # -- helpers -----------------------------------------------------------
+    def _seq(self, sid: int) -> _Seq:
+        if sid not in self.seqs:
+            raise AllocatorError(ERR_INVALID_ARG, f"unknown sequence {sid}")
+        return self.seqs[sid]
+
+    def _pop(self, kind: int) -> int:
+        stack, ref = (self.base_free, self.base_ref) if kind == JOB_BASE else (self.res_free, self.res_ref)
+        p = stack.pop()
+        ref[p] = 1
+        return p
+
+    def _new_id(self) -> int:
+        sid = self.next_id
+        self.next_id += 1
+        return sid
+
+    # -- operations --------------------------------------------------------
+    def seq_create(self, n_tokens: int) -> int:
+        if n_tokens < 0:
+            raise AllocatorError(ERR_INVALID_ARG, "negative length")
+        npg = _ceil_div(n_tokens, self.P)
+        if npg > len(self.base_free) or npg > len(self.res_free):
+            raise AllocatorError(ERR_OUT_OF_PAGES)
+        base = [self._pop(JOB_BASE) for _ in range(npg)]
+        res = [self._pop(JOB_RES) for _ in range(npg)]
+        sid = self._new_id()
+        self.seqs[sid] = _Seq(n_tokens, base, res)
+        return sid
+
+    def fork(self, parent: int, prefix_len: int, share_res: bool = False,
+             jobs_cap: Optional[int] = None) -> Tuple[int, List[Tuple[int, int, int, int]]]:
+        par = self._seq(parent)
+        if prefix_len < 0 or prefix_len > par.length:
+            raise AllocatorError(ERR_INVALID_ARG, "prefix_len out of range")
+        P = self.P
+        nf, t = divmod(prefix_len, P)
+        npg = nf + (1 if t else 0)
+        need_base = 1 if t else 0
+        need_res = (1 if t else 0) if share_res else npg
+        n_jobs = (1 if t else 0) * (2 if share_res else 1)
+        if jobs_cap is not None and n_jobs > jobs_cap:
+            raise AllocatorError(ERR_INVALID_ARG, "job buffer too small")
+        if need_base > len(self.base_free) or need_res > len(self.res_free):
+            raise AllocatorError(ERR_OUT_OF_PAGES)
+        jobs = []
+        base = list(par.base[:nf])
+        for p in base:
+            self.base_ref[p] += 1
+        if t:
+            dst = self._pop(JOB_BASE)
+            jobs.append((par.base[nf], dst, t, JOB_BASE))
+            base.append(dst)
+        if share_res:
+            res = list(par.res[:nf])
+            for p in res:
+                self.res_ref[p] += 1
+            if t:
+                dst = self._pop(JOB_RES)
+                jobs.append((par.res[nf], dst, t, JOB_RES))
+                res.append(dst)
+        else:
+            res = [self._pop(JOB_RES) for _ in range(npg)]
+        sid = self._new_id()
+        self.seqs[sid] = _Seq(prefix_len, base, res)
+        return sid, jobs
+
+    def append(self, sid: int, n_tokens: int, jobs_cap: Optional[int] = None) -> List[Tuple[int, int, int, int]]:
+        s = self._seq(sid)
+        if n_tokens < 0:
+            raise AllocatorError(ERR_INVALID_ARG, "negative length")
+        P = self.P
+        L = s.length
+        grow = _ceil_div(L + n_tokens, P) - _ceil_div(L, P)
+        tail = L % P
+        cow_base = bool(n_tokens > 0 and tail and self.base_ref[s.base[-1]] > 1)
+        cow_res = bool(n_tokens > 0 and tail and self.res_ref[s.res[-1]] > 1)
+        n_jobs = int(cow_base) + int(cow_res)
+        if jobs_cap is not None and n_jobs > jobs_cap:
+            raise AllocatorError(ERR_INVALID_ARG, "job buffer too small")
+        if grow + cow_base > len(self.base_free) or grow + cow_res > len(self.res_free):
+            raise AllocatorError(ERR_OUT_OF_PAGES)
+        jobs = []
+        if cow_base:
+            old = s.base[-1]
+            dst = self._pop(JOB_BASE)
+            self.base_ref[old] -= 1
+            s.base[-1] = dst
+            jobs.append((old, dst, tail, JOB_BASE))
+        s.base.extend(self._pop(JOB_BASE) for _ in range(grow))
+        if cow_res:
+            old = s.res[-1]
+            dst = self._pop(JOB_RES)
+            self.res_ref[old] -= 1
+            s.res[-1] = dst
+            jobs.append((old, dst, tail, JOB_RES))
+        s.res.extend(self._pop(JOB_RES) for _ in range(grow))
+        s.length = L + n_tokens
+        return jobs
+
+    def free(self, sid: int) -> None:
+        s = self._seq(sid)
+        for p in s.base:
+            self.base_ref[p] -= 1
+            if self.base_ref[p] == 0:
+                self.base_free.append(p)
+        for p in s.res:
+            self.res_ref[p] -= 1
+            if self.res_ref[p] == 0:
+                self.res_free.append(p)
+        del self.seqs[sid]
+
+    def page_tables(self, sids: Sequence[int], stride: int):
+        """Rows of base / residual page ids (padded with -1) and lengths."""
+        bpt, rpt, lens = [], [], []
+        for sid in sids:
+            s = self._seq(sid)
+            if len(s.base) > stride:
+                raise AllocatorError(ERR_INVALID_ARG, "stride too small")
+            bpt.append(s.base + [-1] * (stride - len(s.base)))
+            rpt.append(s.res + [-1] * (stride - len(s.res)))
+            lens.append(s.length)
+        return bpt, rpt, lens
+
+    def refcount(self, kind: int, page: int) -> int:
+        ref = self.base_ref if kind == JOB_BASE else self.res_ref
+        if page < 0 or page >= len(ref):
+            raise AllocatorError(ERR_BAD_PAGE)
+        return ref[page]
+
+    def stats(self) -> dict:
+        return {
+            "n_seqs": len(self.seqs),
+            "base_live": sum(1 for c in self.base_ref if c > 0),
+            "res_live": sum(1 for c in self.res_ref if c > 0),
+            "base_free": len(self.base_free),
+            "res_free": len(self.res_free),
+            "base_shared": sum(1 for c in self.base_ref if c > 1),
+            "res_shared": sum(1 for c in self.res_ref if c > 1),
+            "base_refsum": sum(self.base_ref),
+            "res_refsum": sum(self.res_ref),
+        }
+
+
+def cow_copy_rows_model(src_page_rows, dst_page_rows, n_valid: int):
+    """Row copy of the pack path: rows [0, n_valid) of src into dst, the rest untouched."""
+    out = [list(r) for r in dst_page_rows]
+    for i in range(n_valid):
+        out[i] = list(src_page_rows[i])
+    return out
