@@ -1,0 +1,378 @@
+#!/usr/bin/env python3
+"""ResidualAttention decode throughput on GB300 (tokens/s and achieved HBM GB/s).
+
+Workload: the Llama-3-8B-shaped decode fan-out (32 q / 8 kv heads, head_dim
+128, rank 16; 8 agents forked from an 8192-token prefix whose base pages are
+aliased with refcount 8, each with U[256,1024] private tokens; 1 query per
+agent), seeded and synthetic, with one set of paged pools per model layer (32
+layers, 1.9 GB) so that consecutive calls never find their inputs in L2.
+
+One step = one decode step of all 32 layers: per layer, the new token's rows
+are scattered into the pools (forkkv_write_rows) and ResidualAttention decode
+runs (forkkv_residual_attn_decode: split-KV kernel + combine kernel).  The
+writes of a step and the decodes of a step are each captured in a CUDA graph;
+the timed region replays them K times.  tokens/s counts one (agent, layer)
+attention as one token, i.e. A * layers / step time.
+
+--impl reference times the fp64 CPU oracle instead (the only reference this
+method has), on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ResidualAttention decode tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def _traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)[kernel]
+        src = os.path.join(ROOT, d["source"])
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        return d["dram_bytes_per_launch"] if sha == d["source_sha256"] else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.idx = device_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_figures(w, layers: int):
+    """Algorithmic bytes and flops of one decode call (one layer), from the drawn lengths."""
+    cfg = w.cfg
+    A, Hq, Hkv, D, r, G = cfg.n_agents, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.rank, cfg.group
+    unique_rows = sum(w.node_tokens)            # every base row once, shared prefix included once
+    lens = [int(x) for x in w.seq_lens]
+    base = unique_rows * Hkv * D * 2 * 2         # K and V, bf16
+    res = sum(lens) * 2 * r * 2                  # k_res and v_res, bf16
+    qo = 2 * A * Hq * D * 2                      # q in, out
+    adapters = A * 2 * r * Hkv * D * 2           # B_k, B_v
+    tables = sum(2 * math.ceil(L / 16) * 4 for L in lens) + A * 8
+    flops = sum(lens) * Hkv * (2 * D * (r + 2 * G) + 2 * G * r)
+    return {"bytes": base + res + qo + adapters + tables, "base_bytes": base, "res_bytes": res, "flops": flops}
+
+
+def run_oracle_sample(w, agent: int, kv_head: int):
+    from oracle import residual_attention as ra
+    import torch
+    kb, vb = w.agent_base(agent)
+    f = lambda t: t.to(torch.float64).numpy()
+    G = w.cfg.group
+    heads = list(range(kv_head * G, (kv_head + 1) * G))
+    ra.residual_attention(f(w.q[agent]), w.positions[agent].numpy(), f(kb), f(vb), f(w.k_res[agent]),
+                          f(w.v_res[agent]), f(w.B_k[agent]), f(w.B_v[agent]), w.cfg.rope_theta, q_heads=heads)
+    return len(heads) / w.cfg.n_q_heads  # fraction of one (agent, layer) token
+
+
+def cpu_baseline(w, seconds: float = 12.0) -> dict:
+    """The oracle, as it stands, on a bounded sample: (agent, KV head) units of one layer call."""
+    t0 = time.perf_counter()
+    tokens, units = 0.0, 0
+    while time.perf_counter() - t0 < seconds:
+        a = units % w.cfg.n_agents
+        h = (units // w.cfg.n_agents) % w.cfg.n_kv_heads
+        tokens += run_oracle_sample(w, a, h)
+        units += 1
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{units} (agent, KV head) units of one layer call ({w.cfg.group} query heads each, "
+                      f"fp64 NumPy, default BLAS threading) in {dt:.1f} s; one unit = "
+                      f"{1 / w.cfg.n_kv_heads:.3f} of an (agent, layer) token",
+            "machine": platform.machine()}
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="forkkv", choices=["forkkv", "reference"])
+    ap.add_argument("--config", default="llama3_8b_decode")
+    ap.add_argument("--layers", type=int, default=0, help="pool sets (0 = the model's layer count)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from disaggregated_kv_attention_gb300 import workload as wl
+    cfg = wl.CONFIGS[args.config]
+    if cfg.q_len != 1:
+        raise SystemExit("bench.py times decode workloads (q_len = 1)")
+    layers = args.layers or cfg.model_layers
+    w = wl.generate(cfg)
+    fig = workload_figures(w, layers)
+    config = {"workload": f"{cfg.name}: {cfg.description}", "layers": layers, "agents": cfg.n_agents,
+              "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "rank": cfg.rank,
+              "page": cfg.page_size, "seq_lens": [int(x) for x in w.seq_lens], "seed": cfg.seed,
+              "l2": "inputs larger than L2: one pool set per layer, %.2f GB in total" % (
+                  layers * fig["bytes"] / 1e9)}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        samples = []
+        for k in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            frac = run_oracle_sample(w, k % cfg.n_agents, (k // cfg.n_agents) % cfg.n_kv_heads)
+            dt = time.perf_counter() - t0
+            if k >= args.warmup:
+                samples.append((frac, dt))
+        tok = sum(f for f, _ in samples)
+        sec = sum(d for _, d in samples)
+        value = tok / sec
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sec / len(samples),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                                 "kind": "oracle",
+                                 "sample": f"each step: one (agent, KV head) unit of one layer call "
+                                           f"({cfg.group} query heads, fp64 NumPy), rotating over agents and heads"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from disaggregated_kv_attention_gb300 import build as _build
+    _build.build()
+    from disaggregated_kv_attention_gb300 import forkkv as fk
+    from disaggregated_kv_attention_gb300 import paged
+
+    dev = torch.device("cuda", local)
+    P = paged.place(w, device=dev, n_layers=layers)
+    A, Hq, Hkv = cfg.n_agents, cfg.n_q_heads, cfg.n_kv_heads
+    lens = [int(x) for x in w.seq_lens]
+    rope = fk.rope_table(cfg.rope_theta, P.max_seq_len, device=dev)
+    plan, info = fk.forkkv_plan_build(P.bpt_np, w.seq_lens.numpy(), Hkv)
+    plan_d = torch.from_numpy(plan).to(dev)
+
+    # per-layer step inputs: q, and the new token's rows (the workload's own last rows)
+    q_all = P.q.unsqueeze(0).repeat(layers, 1, 1, 1, 1).contiguous()
+    out_all = torch.empty_like(q_all)
+    kb_last = torch.stack([w.agent_base(a)[0][lens[a] - 1] for a in range(A)])
+    vb_last = torch.stack([w.agent_base(a)[1][lens[a] - 1] for a in range(A)])
+    kr_last = torch.stack([w.k_res[a][lens[a] - 1] for a in range(A)])
+    vr_last = torch.stack([w.v_res[a][lens[a] - 1] for a in range(A)])
+    kb_new = kb_last.unsqueeze(0).repeat(layers, 1, 1, 1).to(dev).contiguous()
+    vb_new = vb_last.unsqueeze(0).repeat(layers, 1, 1, 1).to(dev).contiguous()
+    kr_new = kr_last.unsqueeze(0).repeat(layers, 1, 1).to(dev).contiguous()
+    vr_new = vr_last.unsqueeze(0).repeat(layers, 1, 1).to(dev).contiguous()
+    slot_b = torch.tensor([int(P.bpt_np[a, (lens[a] - 1) // 16]) * 16 + (lens[a] - 1) % 16 for a in range(A)],
+                          dtype=torch.int32, device=dev)
+    slot_r = torch.tensor([int(P.rpt_np[a, (lens[a] - 1) // 16]) * 16 + (lens[a] - 1) % 16 for a in range(A)],
+                          dtype=torch.int32, device=dev)
+
+    params = []
+    for l in range(layers):
+        p = fk.attn_params(P.pools, l, q_all[l], out_all[l], P.bpt, P.rpt, P.seq_lens, P.positions, P.max_seq_len,
+                           P.B_k, P.B_v, rope=rope, plan=plan_d, plan_info=info)
+        params.append(p)
+    ws = fk.workspace_for(params[0], device=dev)
+    for p in params:
+        fk.set_workspace(p, ws)
+
+    def writes():
+        for l in range(layers):
+            fk.forkkv_write_rows(P.pools, l, slot_b, slot_r, kb_new[l], vb_new[l], kr_new[l], vr_new[l])
+
+    def decodes():
+        for p in params:
+            fk.forkkv_residual_attn_decode(p)
+
+    # eager once (sets kernel attributes), check status, then capture
+    writes()
+    decodes()
+    torch.cuda.synchronize()
+    st = fk.forkkv_get_device_status()
+    if st:
+        raise RuntimeError(f"device status {st} after the first step")
+    g_w, g_d = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g_w, stream=s):
+            writes()
+        with torch.cuda.graph(g_d, stream=s):
+            decodes()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        g_w.replay()
+        g_d.replay()
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    e_start.record(stream)
+    for k in range(args.steps):
+        g_w.replay()
+        ev0[k].record(stream)
+        g_d.replay()
+        ev1[k].record(stream)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = e_start.elapsed_time(e_end)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    dec_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    call_us = 1000 * statistics.mean(dec_ms) / layers
+    ms_step = total_ms / args.steps
+    value = world * A * layers / (ms_step / 1000)
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    q_h = q_all.cpu().pin_memory()
+    kbh, vbh = kb_new.cpu().pin_memory(), vb_new.cpu().pin_memory()
+    krh, vrh = kr_new.cpu().pin_memory(), vr_new.cpu().pin_memory()
+    bpt_h, rpt_h = P.bpt.cpu().pin_memory(), P.rpt.cpu().pin_memory()
+    lens_h, pos_h = P.seq_lens.cpu().pin_memory(), P.positions.cpu().pin_memory()
+    out_h = torch.empty_like(out_all, device="cpu").pin_memory()
+    h2d = [(q_all, q_h), (kb_new, kbh), (vb_new, vbh), (kr_new, krh), (vr_new, vrh), (P.bpt, bpt_h),
+           (P.rpt, rpt_h), (P.seq_lens, lens_h), (P.positions, pos_h)]
+    h2d_bytes = sum(h.numel() * h.element_size() for _, h in h2d)
+    d2h_bytes = out_h.numel() * out_h.element_size()
+    e2e_steps = max(10, args.steps // 4)
+
+    def e2e_step():
+        for d, h in h2d:
+            d.copy_(h, non_blocking=True)
+        g_w.replay()
+        g_d.replay()
+        out_h.copy_(out_all, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * A * layers / e2e_s
+
+    torch.cuda.synchronize()
+    st = fk.forkkv_get_device_status()
+    if st:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    hbm, tf, tf_sus, src = _peaks()
+    achieved = fig["bytes"] / (call_us * 1e-6) / 1e9
+    traffic = _traffic("decode_split_kernel")
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic, "peak_source": f"{src} hbm_gbs (of {src})",
+                     "kernel": "forkkv_residual_attn_decode (split-KV kernel + combine kernel), per layer call",
+                     "alg_bytes_per_launch": fig["bytes"], "launch_us": call_us},
+        "decode_call_us": call_us,
+        "model_step_tokens_per_s": world * A / (ms_step / 1000),
+        "achieved_tflops": fig["flops"] / (call_us * 1e-6) / 1e12,
+        "alg_flops_per_call": fig["flops"],
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps},
+        "gpu_launches": args.steps * layers * 3,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

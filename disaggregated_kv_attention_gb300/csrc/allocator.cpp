@@ -1,0 +1,284 @@
+// Host allocator: paged, refcounted base and residual pools with fork / append /
+// free and copy-on-write jobs.
+//
+// Semantics: ForkKV L2 section 3 (Figure 6: a new agent maps the parent's base
+// pages read-only and allocates only its residual pages) and the ForkServe
+// README ("Design vs APC" and "Methods": fork aliases the parent's frames in
+// O(pages) with refcounts, so freeing the parent keeps the trunk alive;
+// unaligned tail, pack path: the L mod P valid rows are copied into a private
+// page of the child).  Free-list order, id assignment and the error policy are
+// fixed choices documented in include/forkkv.h.
+#include <cstdint>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/forkkv.h"
+
+namespace {
+
+struct Seq {
+  int32_t length = 0;
+  std::vector<int32_t> base;
+  std::vector<int32_t> res;
+};
+
+inline int32_t ceil_div(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1) / b); }
+
+}  // namespace
+
+struct forkkv_alloc {
+  int32_t page = FORKKV_PAGE_SIZE;
+  std::vector<int32_t> base_free, res_free;  // LIFO stacks
+  std::vector<int32_t> base_ref, res_ref;
+  std::unordered_map<int32_t, Seq> seqs;
+  int32_t next_id = 0;
+
+  int32_t pop(bool base) {
+    auto& st = base ? base_free : res_free;
+    auto& rf = base ? base_ref : res_ref;
+    int32_t p = st.back();
+    st.pop_back();
+    rf[p] = 1;
+    return p;
+  }
+  Seq* find(int32_t id) {
+    auto it = seqs.find(id);
+    return it == seqs.end() ? nullptr : &it->second;
+  }
+  const Seq* find(int32_t id) const {
+    auto it = seqs.find(id);
+    return it == seqs.end() ? nullptr : &it->second;
+  }
+};
+
+extern "C" {
+
+int32_t forkkv_alloc_create(int32_t num_base_pages, int32_t num_res_pages, int32_t page_size,
+                            forkkv_alloc** out) {
+  if (!out || num_base_pages < 0 || num_res_pages < 0) return FORKKV_ERR_INVALID_ARG;
+  if (page_size != FORKKV_PAGE_SIZE) return FORKKV_ERR_UNSUPPORTED;
+  forkkv_alloc* a = new (std::nothrow) forkkv_alloc();
+  if (!a) return FORKKV_ERR_INVALID_ARG;
+  try {
+    a->base_free.resize(num_base_pages);
+    a->res_free.resize(num_res_pages);
+    for (int32_t i = 0; i < num_base_pages; ++i) a->base_free[i] = num_base_pages - 1 - i;
+    for (int32_t i = 0; i < num_res_pages; ++i) a->res_free[i] = num_res_pages - 1 - i;
+    a->base_ref.assign(num_base_pages, 0);
+    a->res_ref.assign(num_res_pages, 0);
+  } catch (...) {
+    delete a;
+    return FORKKV_ERR_INVALID_ARG;
+  }
+  *out = a;
+  return FORKKV_OK;
+}
+
+int32_t forkkv_alloc_destroy(forkkv_alloc* alloc) {
+  delete alloc;
+  return FORKKV_OK;
+}
+
+int32_t forkkv_seq_create(forkkv_alloc* a, int32_t n_tokens, int32_t* seq_out) {
+  if (!a || !seq_out || n_tokens < 0) return FORKKV_ERR_INVALID_ARG;
+  const int32_t npg = ceil_div(n_tokens, a->page);
+  if (npg > static_cast<int32_t>(a->base_free.size()) || npg > static_cast<int32_t>(a->res_free.size()))
+    return FORKKV_ERR_OUT_OF_PAGES;
+  try {
+    Seq s;
+    s.length = n_tokens;
+    s.base.reserve(npg);
+    s.res.reserve(npg);
+    const int32_t id = a->next_id;
+    a->seqs.emplace(id, Seq());  // may throw before any page moves
+    for (int32_t i = 0; i < npg; ++i) s.base.push_back(a->pop(true));
+    for (int32_t i = 0; i < npg; ++i) s.res.push_back(a->pop(false));
+    a->seqs[id] = std::move(s);
+    a->next_id++;
+    *seq_out = id;
+  } catch (...) {
+    return FORKKV_ERR_INVALID_ARG;
+  }
+  return FORKKV_OK;
+}
+
+int32_t forkkv_fork(forkkv_alloc* a, int32_t parent, int32_t prefix_len, uint32_t flags,
+                    int32_t* child_out, forkkv_cow_job* jobs, int32_t jobs_cap, int32_t* n_jobs) {
+  if (!a || !child_out || !n_jobs || jobs_cap < 0 || (jobs_cap > 0 && !jobs)) return FORKKV_ERR_INVALID_ARG;
+  if (flags & ~FORKKV_FORK_SHARE_RES) return FORKKV_ERR_INVALID_ARG;
+  const Seq* par = a->find(parent);
+  if (!par || prefix_len < 0 || prefix_len > par->length) return FORKKV_ERR_INVALID_ARG;
+  const bool share_res = (flags & FORKKV_FORK_SHARE_RES) != 0;
+  const int32_t P = a->page;
+  const int32_t nf = prefix_len / P, t = prefix_len % P;
+  const int32_t npg = nf + (t ? 1 : 0);
+  const int32_t need_base = t ? 1 : 0;
+  const int32_t need_res = share_res ? (t ? 1 : 0) : npg;
+  const int32_t nj = (t ? 1 : 0) * (share_res ? 2 : 1);
+  if (nj > jobs_cap) return FORKKV_ERR_INVALID_ARG;
+  if (need_base > static_cast<int32_t>(a->base_free.size()) || need_res > static_cast<int32_t>(a->res_free.size()))
+    return FORKKV_ERR_OUT_OF_PAGES;
+  try {
+    Seq c;
+    c.length = prefix_len;
+    c.base.reserve(npg);
+    c.res.reserve(npg);
+    const int32_t id = a->next_id;
+    a->seqs.emplace(id, Seq());  // may throw (and invalidate nothing else) before any change
+    par = a->find(parent);       // re-find: emplace may rehash
+    int32_t k = 0;
+    for (int32_t i = 0; i < nf; ++i) {
+      c.base.push_back(par->base[i]);
+      a->base_ref[par->base[i]]++;
+    }
+    if (t) {
+      const int32_t dst = a->pop(true);
+      jobs[k++] = forkkv_cow_job{par->base[nf], dst, t, FORKKV_JOB_BASE};
+      c.base.push_back(dst);
+    }
+    if (share_res) {
+      for (int32_t i = 0; i < nf; ++i) {
+        c.res.push_back(par->res[i]);
+        a->res_ref[par->res[i]]++;
+      }
+      if (t) {
+        const int32_t dst = a->pop(false);
+        jobs[k++] = forkkv_cow_job{par->res[nf], dst, t, FORKKV_JOB_RES};
+        c.res.push_back(dst);
+      }
+    } else {
+      for (int32_t i = 0; i < npg; ++i) c.res.push_back(a->pop(false));
+    }
+    a->seqs[id] = std::move(c);
+    a->next_id++;
+    *child_out = id;
+    *n_jobs = k;
+  } catch (...) {
+    return FORKKV_ERR_INVALID_ARG;
+  }
+  return FORKKV_OK;
+}
+
+int32_t forkkv_append(forkkv_alloc* a, int32_t seq, int32_t n_tokens, forkkv_cow_job* jobs, int32_t jobs_cap,
+                      int32_t* n_jobs) {
+  if (!a || !n_jobs || n_tokens < 0 || jobs_cap < 0 || (jobs_cap > 0 && !jobs)) return FORKKV_ERR_INVALID_ARG;
+  Seq* s = a->find(seq);
+  if (!s) return FORKKV_ERR_INVALID_ARG;
+  const int32_t P = a->page;
+  const int64_t L = s->length;
+  if (L + n_tokens > INT32_MAX) return FORKKV_ERR_INVALID_ARG;
+  const int32_t grow = ceil_div(L + n_tokens, P) - ceil_div(L, P);
+  const int32_t tail = static_cast<int32_t>(L % P);
+  const bool cow_base = n_tokens > 0 && tail && a->base_ref[s->base.back()] > 1;
+  const bool cow_res = n_tokens > 0 && tail && a->res_ref[s->res.back()] > 1;
+  const int32_t nj = (cow_base ? 1 : 0) + (cow_res ? 1 : 0);
+  if (nj > jobs_cap) return FORKKV_ERR_INVALID_ARG;
+  if (grow + (cow_base ? 1 : 0) > static_cast<int32_t>(a->base_free.size()) ||
+      grow + (cow_res ? 1 : 0) > static_cast<int32_t>(a->res_free.size()))
+    return FORKKV_ERR_OUT_OF_PAGES;
+  try {
+    s->base.reserve(s->base.size() + grow);  // may throw before any change
+    s->res.reserve(s->res.size() + grow);
+  } catch (...) {
+    return FORKKV_ERR_INVALID_ARG;
+  }
+  int32_t k = 0;
+  if (cow_base) {
+    const int32_t old = s->base.back();
+    const int32_t dst = a->pop(true);
+    a->base_ref[old]--;
+    s->base.back() = dst;
+    jobs[k++] = forkkv_cow_job{old, dst, tail, FORKKV_JOB_BASE};
+  }
+  for (int32_t i = 0; i < grow; ++i) s->base.push_back(a->pop(true));
+  if (cow_res) {
+    const int32_t old = s->res.back();
+    const int32_t dst = a->pop(false);
+    a->res_ref[old]--;
+    s->res.back() = dst;
+    jobs[k++] = forkkv_cow_job{old, dst, tail, FORKKV_JOB_RES};
+  }
+  for (int32_t i = 0; i < grow; ++i) s->res.push_back(a->pop(false));
+  s->length = static_cast<int32_t>(L + n_tokens);
+  *n_jobs = k;
+  return FORKKV_OK;
+}
+
+int32_t forkkv_free(forkkv_alloc* a, int32_t seq) {
+  if (!a) return FORKKV_ERR_INVALID_ARG;
+  Seq* s = a->find(seq);
+  if (!s) return FORKKV_ERR_INVALID_ARG;
+  for (int32_t p : s->base)
+    if (a->base_ref[p] <= 0) return FORKKV_ERR_REFCOUNT;
+  for (int32_t p : s->res)
+    if (a->res_ref[p] <= 0) return FORKKV_ERR_REFCOUNT;
+  // pushes never exceed the pool size, so reserve once to keep push_back from throwing
+  a->base_free.reserve(a->base_ref.size());
+  a->res_free.reserve(a->res_ref.size());
+  for (int32_t p : s->base)
+    if (--a->base_ref[p] == 0) a->base_free.push_back(p);
+  for (int32_t p : s->res)
+    if (--a->res_ref[p] == 0) a->res_free.push_back(p);
+  a->seqs.erase(seq);
+  return FORKKV_OK;
+}
+
+int32_t forkkv_seq_len(const forkkv_alloc* a, int32_t seq, int32_t* len_out) {
+  if (!a || !len_out) return FORKKV_ERR_INVALID_ARG;
+  const Seq* s = a->find(seq);
+  if (!s) return FORKKV_ERR_INVALID_ARG;
+  *len_out = s->length;
+  return FORKKV_OK;
+}
+
+int32_t forkkv_page_tables(const forkkv_alloc* a, const int32_t* seqs, int32_t n, int32_t stride, int32_t* bpt,
+                           int32_t* rpt, int32_t* seq_lens) {
+  if (!a || n < 0 || stride < 0 || (n > 0 && (!seqs || !bpt || !rpt || !seq_lens))) return FORKKV_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    const Seq* s = a->find(seqs[i]);
+    if (!s || static_cast<int64_t>(s->base.size()) > stride) return FORKKV_ERR_INVALID_ARG;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const Seq* s = a->find(seqs[i]);
+    int32_t* b = bpt + static_cast<int64_t>(i) * stride;
+    int32_t* r = rpt + static_cast<int64_t>(i) * stride;
+    const int32_t np = static_cast<int32_t>(s->base.size());
+    for (int32_t j = 0; j < stride; ++j) {
+      b[j] = j < np ? s->base[j] : -1;
+      r[j] = j < np ? s->res[j] : -1;
+    }
+    seq_lens[i] = s->length;
+  }
+  return FORKKV_OK;
+}
+
+int32_t forkkv_refcount(const forkkv_alloc* a, int32_t kind, int32_t page, int32_t* out) {
+  if (!a || !out || (kind != FORKKV_JOB_BASE && kind != FORKKV_JOB_RES)) return FORKKV_ERR_INVALID_ARG;
+  const auto& rf = kind == FORKKV_JOB_BASE ? a->base_ref : a->res_ref;
+  if (page < 0 || page >= static_cast<int32_t>(rf.size())) return FORKKV_ERR_BAD_PAGE;
+  *out = rf[page];
+  return FORKKV_OK;
+}
+
+int32_t forkkv_stats_get(const forkkv_alloc* a, forkkv_stats* out) {
+  if (!a || !out) return FORKKV_ERR_INVALID_ARG;
+  forkkv_stats s{};
+  s.n_seqs = static_cast<int32_t>(a->seqs.size());
+  for (int32_t c : a->base_ref) {
+    s.base_live += c > 0;
+    s.base_shared += c > 1;
+    s.base_refsum += c;
+  }
+  for (int32_t c : a->res_ref) {
+    s.res_live += c > 0;
+    s.res_shared += c > 1;
+    s.res_refsum += c;
+  }
+  s.base_free = static_cast<int32_t>(a->base_free.size());
+  s.res_free = static_cast<int32_t>(a->res_free.size());
+  *out = s;
+  return FORKKV_OK;
+}
+
+}  // extern "C"

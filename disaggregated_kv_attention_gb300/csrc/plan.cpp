@@ -1,0 +1,177 @@
+// Decode work planning: fork-tree segments -> work items.
+//
+// Agents forked from one trunk alias the same base pages (ForkKV L2 section 3,
+// Figure 6; ForkServe "Methods", CoW tree).  Reading such a page once for
+// every agent that maps it is what makes sharing pay in HBM bytes, so the plan
+// groups, per run of logical pages, the agents whose page tables hold the same
+// physical base page there.  The groups fall out of the page tables alone: walk
+// the logical page index, and split a group of agents whenever their physical
+// pages differ (or some of them end).  Each segment (agent group, page range)
+// is then cut into items of at most 8 agents and a bounded number of stages.
+#include <algorithm>
+#include <cstdint>
+#include <map>
+#include <vector>
+
+#include "../../include/forkkv.h"
+
+namespace {
+
+struct Segment {
+  std::vector<int32_t> agents;
+  int32_t p0, p1;
+};
+
+// Work pages per stage for a group of na agents: 8 consumer warps = na * wpp.
+int32_t pages_per_stage(int32_t na) { return 8 / na; }
+
+int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents, int32_t pt_stride,
+                   int32_t num_kv_heads, int32_t target_ctas, int32_t* plan, int32_t plan_cap_ints,
+                   forkkv_plan_info* info) {
+  if (!bpt || !seq_lens || !info || n_agents < 1 || pt_stride < 1 || num_kv_heads < 1 || target_ctas < 0)
+    return FORKKV_ERR_INVALID_ARG;
+  if (target_ctas == 0) target_ctas = 2 * 152;
+  std::vector<int32_t> npages(n_agents);
+  for (int32_t a = 0; a < n_agents; ++a) {
+    if (seq_lens[a] < 1) return FORKKV_ERR_INVALID_ARG;
+    npages[a] = (seq_lens[a] + FORKKV_PAGE_SIZE - 1) / FORKKV_PAGE_SIZE;
+    if (npages[a] > pt_stride) return FORKKV_ERR_INVALID_ARG;
+    for (int32_t j = 0; j < npages[a]; ++j)
+      if (bpt[(int64_t)a * pt_stride + j] < 0) return FORKKV_ERR_BAD_PAGE;
+  }
+
+  // 1. segments of the fork tree, by an explicit-stack walk over logical pages
+  std::vector<Segment> segs;
+  struct Frame {
+    std::vector<int32_t> group;
+    int32_t i0;
+  };
+  std::vector<Frame> stack;
+  {
+    std::vector<int32_t> all(n_agents);
+    for (int32_t a = 0; a < n_agents; ++a) all[a] = a;
+    stack.push_back({all, 0});
+  }
+  while (!stack.empty()) {
+    Frame f = std::move(stack.back());
+    stack.pop_back();
+    int32_t i = f.i0;
+    for (;;) {
+      bool same = true;
+      const int32_t a0 = f.group[0];
+      for (int32_t a : f.group) {
+        if (i >= npages[a] || bpt[(int64_t)a * pt_stride + i] != bpt[(int64_t)a0 * pt_stride + i]) {
+          same = false;
+          break;
+        }
+      }
+      if (!same) break;
+      ++i;
+    }
+    if (i > f.i0) segs.push_back({f.group, f.i0, i});
+    // agents still active at page i, grouped by their physical page (first-seen order)
+    std::vector<int32_t> order;
+    std::map<int32_t, std::vector<int32_t>> cls;
+    for (int32_t a : f.group) {
+      if (i >= npages[a]) continue;
+      const int32_t pg = bpt[(int64_t)a * pt_stride + i];
+      if (!cls.count(pg)) order.push_back(pg);
+      cls[pg].push_back(a);
+    }
+    for (auto it = order.rbegin(); it != order.rend(); ++it) stack.push_back({cls[*it], i});
+  }
+
+  // 2. groups of at most 8 agents (8, then 4, 2, 1 for the remainder)
+  struct Chunk {
+    int32_t agents[8];
+    int32_t na, p0, p1, stages;
+  };
+  std::vector<Chunk> chunks;
+  for (const Segment& s : segs) {
+    size_t k = 0;
+    while (k < s.agents.size()) {
+      const size_t left = s.agents.size() - k;
+      const int32_t na = left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
+      Chunk c{};
+      for (int32_t x = 0; x < 8; ++x) c.agents[x] = x < na ? s.agents[k + x] : -1;
+      c.na = na;
+      c.p0 = s.p0;
+      c.p1 = s.p1;
+      const int32_t wpp = pages_per_stage(na);
+      c.stages = (s.p1 - s.p0 + wpp - 1) / wpp;
+      chunks.push_back(c);
+      k += na;
+    }
+  }
+
+  // 3. the largest stage cap T whose item count still reaches target_ctas / Hkv
+  const int64_t want = std::max<int64_t>(1, (target_ctas + num_kv_heads - 1) / num_kv_heads);
+  int32_t max_stages = 1;
+  for (const Chunk& c : chunks) max_stages = std::max(max_stages, c.stages);
+  auto count = [&](int32_t T) {
+    int64_t n = 0;
+    for (const Chunk& c : chunks) n += (c.stages + T - 1) / T;
+    return n;
+  };
+  int32_t lo = 1, hi = max_stages;
+  while (lo < hi) {  // largest T with count(T) >= want
+    const int32_t mid = lo + (hi - lo + 1) / 2;
+    if (count(mid) >= want)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int32_t T = lo;
+
+  // 4. items (near-equal stage counts per chunk), slots and the per-agent slot lists
+  std::vector<int32_t> items;
+  std::vector<std::vector<int32_t>> agent_slots(n_agents);
+  int32_t n_items = 0, n_slots = 0;
+  for (const Chunk& c : chunks) {
+    const int32_t wpp = pages_per_stage(c.na);
+    const int32_t parts = (c.stages + T - 1) / T;
+    for (int32_t k = 0; k < parts; ++k) {
+      const int32_t s0 = (int32_t)((int64_t)c.stages * k / parts), s1 = (int32_t)((int64_t)c.stages * (k + 1) / parts);
+      const int32_t p0 = c.p0 + s0 * wpp, p1 = std::min(c.p1, c.p0 + s1 * wpp);
+      int32_t rec[FORKKV_PLAN_ITEM_INTS] = {0};
+      rec[0] = p0;
+      rec[1] = p1;
+      rec[2] = c.na;
+      rec[3] = wpp;
+      for (int32_t x = 0; x < 8; ++x) rec[4 + x] = x < c.na ? c.agents[x] : c.agents[0];
+      rec[12] = n_slots;
+      items.insert(items.end(), rec, rec + FORKKV_PLAN_ITEM_INTS);
+      for (int32_t x = 0; x < c.na; ++x) agent_slots[c.agents[x]].push_back(n_slots + x);
+      n_slots += c.na;
+      ++n_items;
+    }
+  }
+  const int64_t need = (int64_t)items.size() + n_agents + 1 + n_slots;
+  info->n_items = n_items;
+  info->n_slots = n_slots;
+  info->plan_ints = (int32_t)need;
+  if (!plan) return FORKKV_OK;  // size query
+  if (need > plan_cap_ints) return FORKKV_ERR_INVALID_ARG;
+  std::copy(items.begin(), items.end(), plan);
+  int32_t* off = plan + items.size();
+  int32_t* sl = off + n_agents + 1;
+  int32_t k = 0;
+  for (int32_t a = 0; a < n_agents; ++a) {
+    off[a] = k;
+    for (int32_t s : agent_slots[a]) sl[k++] = s;
+  }
+  off[n_agents] = k;
+  return FORKKV_OK;
+}
+
+}  // namespace
+
+extern "C" int32_t forkkv_plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents, int32_t pt_stride,
+                                     int32_t num_kv_heads, int32_t target_ctas, int32_t* plan, int32_t plan_cap_ints,
+                                     forkkv_plan_info* info) {
+  try {
+    return plan_build(bpt, seq_lens, n_agents, pt_stride, num_kv_heads, target_ctas, plan, plan_cap_ints, info);
+  } catch (...) {
+    return FORKKV_ERR_INVALID_ARG;
+  }
+}

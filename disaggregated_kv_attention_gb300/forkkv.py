@@ -1,0 +1,335 @@
+"""Thin ctypes binding of libforkkv (include/forkkv.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does no
+computation of its own: tensors are passed as device pointers, host arrays as
+host pointers, and a non-zero status raises ``ForkKVError``.  PyTorch only
+provides device memory and streams.  Importing this module does not load the
+library; the first call does, and raises if ``libforkkv.so`` has not been
+built (``__graft_entry__.build()``).  There is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libforkkv.so")
+_lib = None
+
+PAGE_SIZE = 16
+HEAD_DIM = 128
+RANK = 16
+BASE_TILE_BYTES = 4096
+RES_TILE_BYTES = 512
+ROPE_ROW_BYTES = 256
+PLAN_ITEM_INTS = 16
+JOB_BASE = 0
+JOB_RES = 1
+FORK_SHARE_RES = 1
+DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_ARG = 1, 2, 4
+
+
+class ForkKVError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {code} ({strerror(code)})")
+        self.code = code
+
+
+class forkkv_cow_job(ctypes.Structure):
+    _fields_ = [("src_page", ctypes.c_int32), ("dst_page", ctypes.c_int32), ("n_valid", ctypes.c_int32),
+                ("kind", ctypes.c_int32)]
+
+
+class forkkv_stats(ctypes.Structure):
+    _fields_ = [("n_seqs", ctypes.c_int32), ("base_live", ctypes.c_int32), ("res_live", ctypes.c_int32),
+                ("base_free", ctypes.c_int32), ("res_free", ctypes.c_int32), ("base_shared", ctypes.c_int32),
+                ("res_shared", ctypes.c_int32), ("base_refsum", ctypes.c_int64), ("res_refsum", ctypes.c_int64)]
+
+
+class forkkv_pool_desc(ctypes.Structure):
+    _fields_ = [("k_base", ctypes.c_void_p), ("v_base", ctypes.c_void_p), ("k_res", ctypes.c_void_p),
+                ("v_res", ctypes.c_void_p), ("num_base_pages", ctypes.c_int32), ("num_res_pages", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("n_layers", ctypes.c_int32)]
+
+
+class forkkv_plan_info(ctypes.Structure):
+    _fields_ = [("n_items", ctypes.c_int32), ("n_slots", ctypes.c_int32), ("plan_ints", ctypes.c_int32)]
+
+
+class forkkv_attn_params(ctypes.Structure):
+    _fields_ = [
+        ("n_agents", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("rank", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("layer", ctypes.c_int32), ("pools", forkkv_pool_desc),
+        ("q", ctypes.c_void_p), ("out", ctypes.c_void_p), ("bpt", ctypes.c_void_p), ("rpt", ctypes.c_void_p),
+        ("pt_stride", ctypes.c_int32), ("seq_lens", ctypes.c_void_p), ("positions", ctypes.c_void_p),
+        ("max_seq_len", ctypes.c_int32), ("B_k", ctypes.c_void_p), ("B_v", ctypes.c_void_p),
+        ("adapter_ids", ctypes.c_void_p), ("n_adapters", ctypes.c_int32), ("rope_table", ctypes.c_void_p),
+        ("rope_table_positions", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("sm_scale", ctypes.c_float),
+        ("plan", ctypes.c_void_p), ("plan_items", ctypes.c_int32), ("plan_slots", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_P = ctypes.POINTER
+_i32, _u32, _vp = ctypes.c_int32, ctypes.c_uint32, ctypes.c_void_p
+_SIGNATURES = {
+    "forkkv_strerror": ([_i32], ctypes.c_char_p),
+    "forkkv_version": ([], _i32),
+    "forkkv_alloc_create": ([_i32, _i32, _i32, _P(_vp)], _i32),
+    "forkkv_alloc_destroy": ([_vp], _i32),
+    "forkkv_seq_create": ([_vp, _i32, _P(_i32)], _i32),
+    "forkkv_fork": ([_vp, _i32, _i32, _u32, _P(_i32), _P(forkkv_cow_job), _i32, _P(_i32)], _i32),
+    "forkkv_append": ([_vp, _i32, _i32, _P(forkkv_cow_job), _i32, _P(_i32)], _i32),
+    "forkkv_free": ([_vp, _i32], _i32),
+    "forkkv_seq_len": ([_vp, _i32, _P(_i32)], _i32),
+    "forkkv_page_tables": ([_vp, _vp, _i32, _i32, _vp, _vp, _vp], _i32),
+    "forkkv_refcount": ([_vp, _i32, _i32, _P(_i32)], _i32),
+    "forkkv_stats_get": ([_vp, _P(forkkv_stats)], _i32),
+    "forkkv_write_rows": ([_P(forkkv_pool_desc), _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "forkkv_cow_copy_rows": ([_P(forkkv_pool_desc), _P(forkkv_cow_job), _i32, _vp], _i32),
+    "forkkv_rope_table_bytes": ([_i32, _P(ctypes.c_size_t)], _i32),
+    "forkkv_rope_table_build": ([ctypes.c_double, _i32, _vp, _vp], _i32),
+    "forkkv_plan_build": ([_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _P(forkkv_plan_info)], _i32),
+    "forkkv_decode_workspace_size": ([_P(forkkv_attn_params), _P(ctypes.c_size_t)], _i32),
+    "forkkv_residual_attn_decode": ([_P(forkkv_attn_params), _vp], _i32),
+    "forkkv_prefill_workspace_size": ([_P(forkkv_attn_params), _P(ctypes.c_size_t)], _i32),
+    "forkkv_residual_attn_prefill_chunk": ([_P(forkkv_attn_params), _vp], _i32),
+    "forkkv_get_device_status": ([_P(_u32), _vp], _i32),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build(); "
+                               "there is no CPU or PyTorch fallback for this library")
+        l = ctypes.CDLL(_LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = l
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().forkkv_strerror(code).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise ForkKVError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# ---- allocator -------------------------------------------------------------
+
+def forkkv_alloc_create(num_base_pages: int, num_res_pages: int, page_size: int = PAGE_SIZE) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().forkkv_alloc_create(num_base_pages, num_res_pages, page_size, ctypes.byref(h)), "alloc_create")
+    return h.value
+
+
+def forkkv_alloc_destroy(alloc: int) -> None:
+    _check(lib().forkkv_alloc_destroy(alloc), "alloc_destroy")
+
+
+def forkkv_seq_create(alloc: int, n_tokens: int) -> int:
+    sid = ctypes.c_int32()
+    _check(lib().forkkv_seq_create(alloc, n_tokens, ctypes.byref(sid)), "seq_create")
+    return sid.value
+
+
+def _jobs_out(buf, n) -> List[Tuple[int, int, int, int]]:
+    return [(buf[i].src_page, buf[i].dst_page, buf[i].n_valid, buf[i].kind) for i in range(n)]
+
+
+def forkkv_fork(alloc: int, parent: int, prefix_len: int, flags: int = 0) -> Tuple[int, list]:
+    child, n = ctypes.c_int32(), ctypes.c_int32()
+    buf = (forkkv_cow_job * 2)()
+    _check(lib().forkkv_fork(alloc, parent, prefix_len, flags, ctypes.byref(child), buf, 2, ctypes.byref(n)), "fork")
+    return child.value, _jobs_out(buf, n.value)
+
+
+def forkkv_append(alloc: int, seq: int, n_tokens: int) -> list:
+    n = ctypes.c_int32()
+    buf = (forkkv_cow_job * 2)()
+    _check(lib().forkkv_append(alloc, seq, n_tokens, buf, 2, ctypes.byref(n)), "append")
+    return _jobs_out(buf, n.value)
+
+
+def forkkv_free(alloc: int, seq: int) -> None:
+    _check(lib().forkkv_free(alloc, seq), "free")
+
+
+def forkkv_seq_len(alloc: int, seq: int) -> int:
+    n = ctypes.c_int32()
+    _check(lib().forkkv_seq_len(alloc, seq, ctypes.byref(n)), "seq_len")
+    return n.value
+
+
+def forkkv_page_tables(alloc: int, seqs: Sequence[int], stride: int):
+    """(bpt, rpt, seq_lens) as int32 numpy arrays [n, stride], [n, stride], [n]."""
+    n = len(seqs)
+    s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+    bpt = np.empty((n, stride), np.int32)
+    rpt = np.empty((n, stride), np.int32)
+    lens = np.empty((n,), np.int32)
+    _check(lib().forkkv_page_tables(alloc, s.ctypes.data, n, stride, bpt.ctypes.data, rpt.ctypes.data,
+                                    lens.ctypes.data), "page_tables")
+    return bpt, rpt, lens
+
+
+def forkkv_refcount(alloc: int, kind: int, page: int) -> int:
+    out = ctypes.c_int32()
+    _check(lib().forkkv_refcount(alloc, kind, page, ctypes.byref(out)), "refcount")
+    return out.value
+
+
+def forkkv_stats_get(alloc: int) -> dict:
+    st = forkkv_stats()
+    _check(lib().forkkv_stats_get(alloc, ctypes.byref(st)), "stats")
+    return {f: getattr(st, f) for f, _ in forkkv_stats._fields_}
+
+
+# ---- pools -----------------------------------------------------------------
+
+class Pools:
+    """Device pools owned by PyTorch, described to the library by a forkkv_pool_desc."""
+
+    def __init__(self, num_base_pages: int, num_res_pages: int, num_kv_heads: int, n_layers: int = 1,
+                 device="cuda", fill: Optional[int] = None):
+        mk = (lambda shape: torch.full(shape, fill, dtype=torch.uint8, device=device)) if fill is not None else \
+            (lambda shape: torch.empty(shape, dtype=torch.uint8, device=device))
+        self.k_base = mk((n_layers, num_base_pages, num_kv_heads, BASE_TILE_BYTES))
+        self.v_base = mk((n_layers, num_base_pages, num_kv_heads, BASE_TILE_BYTES))
+        self.k_res = mk((n_layers, num_res_pages, RES_TILE_BYTES))
+        self.v_res = mk((n_layers, num_res_pages, RES_TILE_BYTES))
+        self.desc = forkkv_pool_desc(self.k_base.data_ptr(), self.v_base.data_ptr(), self.k_res.data_ptr(),
+                                     self.v_res.data_ptr(), num_base_pages, num_res_pages, num_kv_heads, n_layers)
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() for t in (self.k_base, self.v_base, self.k_res, self.v_res))
+
+
+def forkkv_write_rows(pools: Pools, layer: int, slot_base: Optional[torch.Tensor], slot_res: Optional[torch.Tensor],
+                      k_base_rows=None, v_base_rows=None, k_res_rows=None, v_res_rows=None, stream=None) -> None:
+    n = int((slot_base if slot_base is not None else slot_res).numel())
+    _check(lib().forkkv_write_rows(ctypes.byref(pools.desc), layer, n, _ptr(slot_base), _ptr(slot_res),
+                                   _ptr(k_base_rows), _ptr(v_base_rows), _ptr(k_res_rows), _ptr(v_res_rows),
+                                   _stream(stream)), "write_rows")
+
+
+def forkkv_cow_copy_rows(pools: Pools, jobs: Sequence[Tuple[int, int, int, int]], stream=None) -> None:
+    buf = (forkkv_cow_job * max(1, len(jobs)))(*[forkkv_cow_job(*j) for j in jobs])
+    _check(lib().forkkv_cow_copy_rows(ctypes.byref(pools.desc), buf, len(jobs), _stream(stream)), "cow_copy_rows")
+
+
+def forkkv_rope_table_build(rope_theta: float, n_positions: int, table: torch.Tensor, stream=None) -> None:
+    assert table.numel() * table.element_size() >= n_positions * ROPE_ROW_BYTES
+    _check(lib().forkkv_rope_table_build(float(rope_theta), n_positions, table.data_ptr(), _stream(stream)),
+           "rope_table_build")
+
+
+def rope_table(rope_theta: float, n_positions: int, device="cuda", stream=None) -> torch.Tensor:
+    n = (n_positions + PAGE_SIZE - 1) // PAGE_SIZE * PAGE_SIZE
+    t = torch.empty((n, ROPE_ROW_BYTES), dtype=torch.uint8, device=device)
+    forkkv_rope_table_build(rope_theta, n, t, stream)
+    return t
+
+
+def forkkv_plan_build(bpt: np.ndarray, seq_lens: np.ndarray, num_kv_heads: int, target_ctas: int = 0):
+    """Host plan: (int32 numpy array, forkkv_plan_info)."""
+    bpt = np.ascontiguousarray(bpt, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    A, stride = bpt.shape
+    info = forkkv_plan_info()
+    _check(lib().forkkv_plan_build(bpt.ctypes.data, lens.ctypes.data, A, stride, num_kv_heads, target_ctas, None, 0,
+                                   ctypes.byref(info)), "plan_build(size)")
+    plan = np.empty((info.plan_ints,), np.int32)
+    _check(lib().forkkv_plan_build(bpt.ctypes.data, lens.ctypes.data, A, stride, num_kv_heads, target_ctas,
+                                   plan.ctypes.data, info.plan_ints, ctypes.byref(info)), "plan_build")
+    return plan, info
+
+
+# ---- attention -------------------------------------------------------------
+
+def attn_params(pools: Pools, layer: int, q: torch.Tensor, out: torch.Tensor, bpt: torch.Tensor, rpt: torch.Tensor,
+                seq_lens: torch.Tensor, positions: torch.Tensor, max_seq_len: int, B_k: torch.Tensor,
+                B_v: torch.Tensor, adapter_ids: Optional[torch.Tensor] = None, rope: Optional[torch.Tensor] = None,
+                rope_theta: float = 0.0, sm_scale: float = 0.0, plan: Optional[torch.Tensor] = None,
+                plan_info: Optional[forkkv_plan_info] = None) -> forkkv_attn_params:
+    """Fill a forkkv_attn_params from tensors (q/out [A, q_len, Hq, 128], tables [A, stride])."""
+    A, q_len, Hq, D = q.shape
+    p = forkkv_attn_params()
+    p.n_agents, p.q_len, p.num_q_heads = A, q_len, Hq
+    p.num_kv_heads = pools.desc.num_kv_heads
+    p.head_dim, p.rank, p.page_size, p.layer = D, RANK, PAGE_SIZE, layer
+    p.pools = pools.desc
+    p.q, p.out = q.data_ptr(), out.data_ptr()
+    p.bpt, p.rpt, p.pt_stride = bpt.data_ptr(), rpt.data_ptr(), bpt.shape[1]
+    p.seq_lens, p.positions, p.max_seq_len = seq_lens.data_ptr(), positions.data_ptr(), max_seq_len
+    p.B_k, p.B_v = B_k.data_ptr(), B_v.data_ptr()
+    p.adapter_ids = _ptr(adapter_ids)
+    p.n_adapters = B_k.shape[0]
+    p.rope_table = _ptr(rope)
+    p.rope_table_positions = 0 if rope is None else rope.shape[0]
+    p.rope_theta = rope_theta
+    p.sm_scale = sm_scale
+    if plan is not None:
+        p.plan, p.plan_items, p.plan_slots = plan.data_ptr(), plan_info.n_items, plan_info.n_slots
+    return p
+
+
+def forkkv_decode_workspace_size(p: forkkv_attn_params) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().forkkv_decode_workspace_size(ctypes.byref(p), ctypes.byref(n)), "decode_workspace_size")
+    return n.value
+
+
+def forkkv_prefill_workspace_size(p: forkkv_attn_params) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().forkkv_prefill_workspace_size(ctypes.byref(p), ctypes.byref(n)), "prefill_workspace_size")
+    return n.value
+
+
+def set_workspace(p: forkkv_attn_params, ws: Optional[torch.Tensor]) -> None:
+    p.workspace = _ptr(ws)
+    p.workspace_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+
+
+def workspace_for(p: forkkv_attn_params, prefill: bool = False, device="cuda") -> Optional[torch.Tensor]:
+    n = forkkv_prefill_workspace_size(p) if prefill else forkkv_decode_workspace_size(p)
+    ws = torch.empty((max(n, 256) + 255) // 256 * 256, dtype=torch.uint8, device=device) if n else None
+    set_workspace(p, ws)
+    return ws
+
+
+def forkkv_residual_attn_decode(p: forkkv_attn_params, stream=None) -> None:
+    _check(lib().forkkv_residual_attn_decode(ctypes.byref(p), _stream(stream)), "residual_attn_decode")
+
+
+def forkkv_residual_attn_prefill_chunk(p: forkkv_attn_params, stream=None) -> None:
+    _check(lib().forkkv_residual_attn_prefill_chunk(ctypes.byref(p), _stream(stream)), "residual_attn_prefill_chunk")
+
+
+def forkkv_get_device_status(stream=None) -> int:
+    v = ctypes.c_uint32()
+    _check(lib().forkkv_get_device_status(ctypes.byref(v), _stream(stream)), "get_device_status")
+    return v.value

@@ -1,0 +1,282 @@
+/*
+ * forkkv.h — C ABI of libforkkv: ResidualAttention over a disaggregated,
+ * copy-on-write KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (ForkKV: Scaling Multi-LoRA Agent Serving via Copy-on-Write
+ * Disaggregated KV Cache — L2, sections 2, 3, 4 and 7):
+ *   a LoRA-adapted key/value projection is xW + xA_i B_i, so the cache is kept
+ *   in two parts: a base cache ("bCache": xW_k with RoPE already applied, and
+ *   xW_v), shared by every agent that forked from the same prefix, and a rank-r
+ *   residual cache ("rCache": xA_k and xA_v, stored without RoPE) private to
+ *   each agent.  Attention rebuilds, on chip and never in HBM,
+ *       K_j = Kb_j + RoPE_{p_j}(Kr_j B_k[:, hD:(h+1)D])     (deferred RoPE)
+ *       V_j = Vb_j + Vr_j B_v[:, hD:(h+1)D]
+ *   and returns softmax(q K^T / sqrt(D)) V, evaluating the value path as
+ *   sum_j p_j Vb_j + (sum_j p_j Vr_j) B_v so that B_v is applied once per
+ *   query after the key loop (associativity of the value path).
+ * Fork and copy-on-write follow ForkKV L2 section 3 (Figure 6: a new agent maps
+ * the parent's bCache pages and allocates only its own rCache pages) and the
+ * ForkServe README ("Design vs APC", "Methods", "Status": fork aliases the
+ * parent's page frames with refcounts; the unaligned tail is packed by copying
+ * its n_valid rows, not a whole page).
+ *
+ * Conventions
+ *   - Every function returns int32_t: FORKKV_OK (0) or a negative FORKKV_ERR_*.
+ *     On error nothing has changed (no allocator state, no launch).
+ *   - No C++ exception crosses this boundary.
+ *   - Device buffers (pools, page tables, q, out, adapters, tables, workspace)
+ *     are allocated and owned by the caller; no entry point allocates device
+ *     memory.  The library owns only the host allocator objects it creates.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Kernels run asynchronously: a successful return means the launch was
+ *     accepted.  Out-of-range indices met on the device are skipped and
+ *     recorded in a device status word read by forkkv_get_device_status().
+ *   - Data is bf16 (IEEE binary16 with 8 exponent bits), indices int32.
+ *   - Fixed geometry: head_dim D = 128, residual rank r = 16, page size P = 16.
+ *
+ * Pool layouts (device memory, 16-byte aligned)
+ *   Base pools k_base, v_base: [n_layers][num_base_pages][num_kv_heads] tiles of
+ *   FORKKV_BASE_TILE_BYTES.  A tile holds the 16 rows x 128 bf16 of one page and
+ *   one KV head in the tensor core's 128-byte-swizzled K-major layout: element
+ *   (row t, column d) lives at byte
+ *       (d / 64) * 2048 + t * 128 + ((((d % 64) / 8) ^ (t % 8)) * 16) + (d % 8) * 2.
+ *   Residual pools k_res, v_res: [n_layers][num_res_pages] tiles of
+ *   FORKKV_RES_TILE_BYTES, 16 rows x 16 bf16 in the 32-byte-swizzled layout:
+ *       t * 32 + (((k / 8) ^ ((t / 4) % 2)) * 16) + (k % 8) * 2.
+ *   A token at logical position j of a sequence lives in row j % 16 of page
+ *   table entry j / 16.  forkkv_write_rows() is the portable way to fill pools.
+ */
+#ifndef FORKKV_H_
+#define FORKKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define FORKKV_OK 0
+#define FORKKV_ERR_INVALID_ARG (-1)  /* bad size, pointer, alignment or id     */
+#define FORKKV_ERR_OUT_OF_PAGES (-2) /* a pool has too few free pages          */
+#define FORKKV_ERR_BAD_PAGE (-3)     /* a page id outside its pool             */
+#define FORKKV_ERR_REFCOUNT (-4)     /* refcount would underflow               */
+#define FORKKV_ERR_UNSUPPORTED (-5)  /* geometry other than D=128, r=16, P=16  */
+#define FORKKV_ERR_CUDA (-6)         /* a CUDA runtime call failed             */
+
+/* device status bits (forkkv_get_device_status) */
+#define FORKKV_DEV_BAD_PAGE 1u  /* a page id read from a device table was out of range */
+#define FORKKV_DEV_TIMEOUT 2u   /* a bounded wait on an mbarrier gave up               */
+#define FORKKV_DEV_BAD_ARG 4u   /* a device-side argument (length, position) invalid   */
+
+/* ---- fixed geometry ---------------------------------------------------- */
+#define FORKKV_PAGE_SIZE 16
+#define FORKKV_HEAD_DIM 128
+#define FORKKV_RANK 16
+#define FORKKV_MAX_GROUP 8             /* query heads per KV head, at most   */
+#define FORKKV_BASE_TILE_BYTES 4096    /* 16 rows x 128 bf16                 */
+#define FORKKV_RES_TILE_BYTES 512      /* 16 rows x 16 bf16                  */
+#define FORKKV_ROPE_ROW_BYTES 256      /* one position of the rotation table */
+#define FORKKV_PLAN_ITEM_INTS 16       /* int32 per decode work item         */
+
+/* Message for a status code (static string). */
+const char* forkkv_strerror(int32_t code);
+/* Library ABI version (major * 100 + minor). */
+int32_t forkkv_version(void);
+
+/* ==== host allocator ======================================================
+ * Two page pools: base pages (shared, refcounted) and residual pages
+ * (private unless FORKKV_FORK_SHARE_RES).  Each pool has a LIFO free stack
+ * that initially pops 0, 1, 2, ...; freeing pushes pages, in logical order,
+ * whose refcount reaches 0.  Sequence ids count up from 0 and are not reused.
+ * An allocator object is not thread-safe: serialise calls on one object.   */
+typedef struct forkkv_alloc forkkv_alloc;
+
+#define FORKKV_JOB_BASE 0  /* copy rows of a base page (all layers, all KV heads, K and V) */
+#define FORKKV_JOB_RES 1   /* copy rows of a residual page (all layers, k_res and v_res)  */
+
+/* One copy-on-write job: rows [0, n_valid) of page src_page are copied into
+ * page dst_page; rows n_valid..15 of dst_page are left untouched. */
+typedef struct {
+  int32_t src_page;
+  int32_t dst_page;
+  int32_t n_valid;
+  int32_t kind; /* FORKKV_JOB_BASE or FORKKV_JOB_RES */
+} forkkv_cow_job;
+
+#define FORKKV_FORK_SHARE_RES 1u /* child aliases the parent's residual pages too */
+
+typedef struct {
+  int32_t n_seqs;
+  int32_t base_live, res_live;     /* pages with refcount > 0 */
+  int32_t base_free, res_free;     /* pages on the free stacks */
+  int32_t base_shared, res_shared; /* pages with refcount > 1 */
+  int64_t base_refsum, res_refsum; /* sum of refcounts */
+} forkkv_stats;
+
+/* Create an allocator over num_base_pages base and num_res_pages residual
+ * pages of page_size tokens (page_size must be 16).  *out owns host memory
+ * only; release it with forkkv_alloc_destroy. */
+int32_t forkkv_alloc_create(int32_t num_base_pages, int32_t num_res_pages, int32_t page_size,
+                            forkkv_alloc** out);
+int32_t forkkv_alloc_destroy(forkkv_alloc* alloc);
+
+/* A root sequence of n_tokens >= 0 tokens with ceil(n/16) private base and
+ * residual pages (base pages popped in logical order, then residual ones). */
+int32_t forkkv_seq_create(forkkv_alloc* alloc, int32_t n_tokens, int32_t* seq_out);
+
+/* Fork (ForkKV L2 section 3, Figure 6; ForkServe "Methods", CoW tree):
+ * the child's first prefix_len tokens (0 <= prefix_len <= parent length) are
+ * the parent's.  Full base pages are aliased (refcount + 1).  If prefix_len
+ * is not a multiple of 16, the child gets a new private base page and a job
+ * {parent tail page, new page, prefix_len % 16, FORKKV_JOB_BASE} (the pack
+ * path of the ForkServe unaligned tail).  Residual pages covering the prefix
+ * are newly allocated (the child's adapter gives it its own xA rows, which the
+ * caller writes); with FORKKV_FORK_SHARE_RES full residual pages are aliased
+ * and a partial one is copied by a FORKKV_JOB_RES job.  Jobs go to
+ * jobs[0 .. *n_jobs) (host memory, jobs_cap entries; at most 2 are made). */
+int32_t forkkv_fork(forkkv_alloc* alloc, int32_t parent, int32_t prefix_len, uint32_t flags,
+                    int32_t* child_out, forkkv_cow_job* jobs, int32_t jobs_cap, int32_t* n_jobs);
+
+/* Grow a sequence by n_tokens >= 0.  A partial last page that is shared
+ * (refcount > 1) is first replaced by a private copy (one job per pool, at
+ * most 2), then ceil-new-length pages are added in logical order. */
+int32_t forkkv_append(forkkv_alloc* alloc, int32_t seq, int32_t n_tokens, forkkv_cow_job* jobs,
+                      int32_t jobs_cap, int32_t* n_jobs);
+
+/* Drop a sequence: every page's refcount - 1; pages reaching 0 are freed.
+ * A child's references keep an aliased trunk alive after its parent is freed. */
+int32_t forkkv_free(forkkv_alloc* alloc, int32_t seq);
+
+int32_t forkkv_seq_len(const forkkv_alloc* alloc, int32_t seq, int32_t* len_out);
+
+/* Page tables of n sequences, row-major [n][stride] (host memory), unused
+ * entries set to -1, and their lengths.  INVALID_ARG if a sequence has more
+ * than stride pages. */
+int32_t forkkv_page_tables(const forkkv_alloc* alloc, const int32_t* seqs, int32_t n, int32_t stride,
+                           int32_t* bpt, int32_t* rpt, int32_t* seq_lens);
+
+int32_t forkkv_refcount(const forkkv_alloc* alloc, int32_t kind, int32_t page, int32_t* out);
+int32_t forkkv_stats_get(const forkkv_alloc* alloc, forkkv_stats* out);
+
+/* ==== pools ================================================================ */
+typedef struct {
+  void* k_base;            /* [n_layers][num_base_pages][num_kv_heads][4096 B] */
+  void* v_base;            /* same shape                                       */
+  void* k_res;             /* [n_layers][num_res_pages][512 B]                 */
+  void* v_res;             /* same shape                                       */
+  int32_t num_base_pages;
+  int32_t num_res_pages;
+  int32_t num_kv_heads;    /* 1..16 */
+  int32_t n_layers;        /* >= 1; layers are stored back to back */
+} forkkv_pool_desc;
+
+/* Scatter n_rows new cache rows into layer `layer` of the pools
+ * (ForkKV L2 section 7, disaggregation: base activations and residual
+ * activations go to separate pools).  Device inputs:
+ *   slot_base[n_rows], slot_res[n_rows]: page * 16 + row, or -1 to skip;
+ *   k_base_rows, v_base_rows: bf16 [n_rows][num_kv_heads][128] (keys already rotated);
+ *   k_res_rows, v_res_rows:   bf16 [n_rows][16] (unrotated).
+ * Pass NULL slot_base (or NULL slot_res) to write only the other part. */
+int32_t forkkv_write_rows(const forkkv_pool_desc* pools, int32_t layer, int32_t n_rows,
+                          const int32_t* slot_base, const int32_t* slot_res,
+                          const void* k_base_rows, const void* v_base_rows,
+                          const void* k_res_rows, const void* v_res_rows, void* stream);
+
+/* Execute copy-on-write jobs on every layer (ForkServe "Status": the pack path
+ * copies n_valid rows of a page, not the page).  `jobs` is HOST memory; the
+ * jobs travel in the kernel's parameters, so no device buffer is needed.
+ * Base jobs copy K and V of every KV head; residual jobs copy k_res and v_res.
+ * Rows >= n_valid of the destination are not written.  Ids and n_valid are
+ * checked on the host (BAD_PAGE / INVALID_ARG) before anything is launched. */
+int32_t forkkv_cow_copy_rows(const forkkv_pool_desc* pools, const forkkv_cow_job* jobs, int32_t n_jobs,
+                             void* stream);
+
+/* ==== rotation table ======================================================
+ * cos/sin of p * theta^(-2i/128) for positions p < n_positions and the 64
+ * rotate-half frequencies i (fp16), FORKKV_ROPE_ROW_BYTES per position:
+ * frequencies (2m, 2m+1) form 8-byte group m = [cos 2m, cos 2m+1, sin 2m, sin 2m+1],
+ * stored at 32-byte unit (m / 4) ^ (p % 8), slot m % 4, of the position's row.
+ * Angles are reduced exactly in 64-bit fixed point before sin/cos. */
+int32_t forkkv_rope_table_bytes(int32_t n_positions, size_t* bytes);
+int32_t forkkv_rope_table_build(double rope_theta, int32_t n_positions, void* table, void* stream);
+
+/* ==== decode work plan =====================================================
+ * Splits the key ranges of a decode batch into work items so that pages
+ * shared by several agents (a fork tree's trunks) are read once per group of
+ * up to 8 agents.  Built on the host from host copies of the page tables.
+ * Item i is FORKKV_PLAN_ITEM_INTS int32:
+ *   [0] first logical page  [1] end logical page   [2] n_agents (1..8)
+ *   [3] pages per stage      [4..11] agent indices  [12] first partial slot
+ * followed by the per-agent slot lists (CSR: n_agents+1 offsets, then slots). */
+typedef struct {
+  int32_t n_items;     /* CTAs per KV head */
+  int32_t n_slots;     /* partial-result slots */
+  int32_t plan_ints;   /* int32 words written to plan */
+} forkkv_plan_info;
+
+/* target_ctas: desired CTAs over all KV heads (0 = 2 per SM of a GB300). */
+int32_t forkkv_plan_build(const int32_t* bpt_host, const int32_t* seq_lens_host, int32_t n_agents,
+                          int32_t pt_stride, int32_t num_kv_heads, int32_t target_ctas,
+                          int32_t* plan, int32_t plan_cap_ints, forkkv_plan_info* info);
+
+/* ==== attention ============================================================ */
+typedef struct {
+  int32_t n_agents;        /* A >= 1 */
+  int32_t q_len;           /* 1 for decode; chunk length C for prefill */
+  int32_t num_q_heads;     /* Hq = G * num_kv_heads with 1 <= G <= 8 */
+  int32_t num_kv_heads;    /* must equal pools.num_kv_heads */
+  int32_t head_dim;        /* must be 128 */
+  int32_t rank;            /* must be 16  */
+  int32_t page_size;       /* must be 16  */
+  int32_t layer;           /* layer of the pools to read */
+  forkkv_pool_desc pools;
+  const void* q;           /* bf16 [A][q_len][Hq][128], already rotated at `positions` */
+  void* out;               /* bf16 [A][q_len][Hq][128] */
+  const int32_t* bpt;      /* [A][pt_stride] base page ids (device) */
+  const int32_t* rpt;      /* [A][pt_stride] residual page ids (device) */
+  int32_t pt_stride;
+  const int32_t* seq_lens; /* [A] keys of each agent, including the query tokens' own rows */
+  const int32_t* positions;/* [A][q_len] absolute query positions; key j visible iff j <= position */
+  int32_t max_seq_len;     /* host-known bound on every seq_len */
+  const void* B_k;         /* bf16 [n_adapters][16][num_kv_heads * 128] */
+  const void* B_v;         /* bf16 [n_adapters][16][num_kv_heads * 128] */
+  const int32_t* adapter_ids; /* [A] adapter of each agent, or NULL for agent a -> adapter a */
+  int32_t n_adapters;
+  const void* rope_table;  /* table for >= max_seq_len positions, or NULL: built in workspace */
+  int32_t rope_table_positions;
+  double rope_theta;       /* used when rope_table is NULL */
+  float sm_scale;          /* 0 -> 1/sqrt(128) */
+  const int32_t* plan;     /* device copy of a forkkv_plan_build plan, or NULL (decode only) */
+  int32_t plan_items;
+  int32_t plan_slots;
+  void* workspace;         /* device scratch, >= the *_workspace_size bytes, 256-byte aligned */
+  size_t workspace_bytes;
+} forkkv_attn_params;
+
+/* Scratch bytes forkkv_residual_attn_decode needs for these params. */
+int32_t forkkv_decode_workspace_size(const forkkv_attn_params* p, size_t* bytes);
+
+/* ResidualAttention decode (q_len = 1): split-KV over pages (or over a plan's
+ * items), dual-accumulator online softmax, then one merge per (agent, query
+ * head) that applies B_v once and writes bf16 out.  Launches 2 kernels (3 if
+ * the rotation table is built in the workspace). */
+int32_t forkkv_residual_attn_decode(const forkkv_attn_params* p, void* stream);
+
+int32_t forkkv_prefill_workspace_size(const forkkv_attn_params* p, size_t* bytes);
+
+/* ResidualAttention over a prefill chunk: q_len query tokens per agent at
+ * `positions`, causal (key j visible iff j <= position and j < seq_len).  The
+ * chunk's own rows must already be in the pools (forkkv_write_rows). */
+int32_t forkkv_residual_attn_prefill_chunk(const forkkv_attn_params* p, void* stream);
+
+/* Read and clear the device status word of the current device (OR of
+ * FORKKV_DEV_* bits set by kernels since the last read).  Synchronises
+ * `stream`. */
+int32_t forkkv_get_device_status(uint32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FORKKV_H_ */

@@ -1,0 +1,224 @@
+"""Host-side checks of libforkkv (no GPU needed).
+
+* the shared library loads and exports every function include/forkkv.h declares;
+* the C++ allocator matches the pure-Python allocator model bit for bit (page
+  ids, jobs, refcounts, stats) on the ForkServe scenarios and on random
+  operation sequences, including the no-change-on-error rule;
+* the decode work plan covers every (agent, logical page) exactly once, only
+  groups agents that map the same physical page, and lists each agent's slots.
+"""
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+from disaggregated_kv_attention_gb300 import forkkv as fk
+from oracle.allocator import AllocatorError, AllocatorModel
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    from disaggregated_kv_attention_gb300 import build
+    build.build()
+    return fk.lib()
+
+
+def test_exports_every_declared_function():
+    with open(os.path.join(ROOT, "include", "forkkv.h")) as f:
+        text = f.read()
+    names = set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(forkkv_\w+)\s*\(", text, flags=re.M))
+    assert len(names) >= 20, names
+    lib = fk.lib()
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(fk._SIGNATURES) == names  # the binding declares exactly the header's functions
+
+
+def test_strerror_and_version():
+    assert fk.strerror(0) == "ok"
+    assert "pages" in fk.strerror(-2)
+    assert fk.lib().forkkv_version() >= 100
+
+
+class _Pair:
+    """C++ allocator and Python model driven side by side."""
+
+    def __init__(self, nb, nr):
+        self.c = fk.forkkv_alloc_create(nb, nr)
+        self.m = AllocatorModel(nb, nr, 16)
+        self.ids = {}  # model id -> C id (they must be equal)
+
+    def close(self):
+        fk.forkkv_alloc_destroy(self.c)
+
+    def op(self, name, *args):
+        err_c = err_m = None
+        rc = rm = None
+        try:
+            rc = getattr(self, "_c_" + name)(*args)
+        except fk.ForkKVError as e:
+            err_c = e.code
+        try:
+            rm = getattr(self, "_m_" + name)(*args)
+        except AllocatorError as e:
+            err_m = e.code
+        assert err_c == err_m, (name, args, err_c, err_m)
+        assert rc == rm, (name, args, rc, rm)
+        return rm
+
+    def _c_create(self, n):
+        return fk.forkkv_seq_create(self.c, n)
+
+    def _m_create(self, n):
+        return self.m.seq_create(n)
+
+    def _c_fork(self, p, n, share):
+        return fk.forkkv_fork(self.c, p, n, fk.FORK_SHARE_RES if share else 0)
+
+    def _m_fork(self, p, n, share):
+        return self.m.fork(p, n, share_res=share)
+
+    def _c_append(self, s, n):
+        return fk.forkkv_append(self.c, s, n)
+
+    def _m_append(self, s, n):
+        return self.m.append(s, n)
+
+    def _c_free(self, s):
+        return fk.forkkv_free(self.c, s)
+
+    def _m_free(self, s):
+        return self.m.free(s)
+
+    def check_state(self):
+        st = fk.forkkv_stats_get(self.c)
+        ms = self.m.stats()
+        for k in ms:
+            assert st[k] == ms[k], (k, st[k], ms[k])
+        sids = sorted(self.m.seqs)
+        if sids:
+            stride = max(1, max(len(self.m.seqs[s].base) for s in sids))
+            b, r, l = fk.forkkv_page_tables(self.c, sids, stride)
+            mb, mr, ml = self.m.page_tables(sids, stride)
+            assert np.array_equal(b, np.array(mb, np.int32))
+            assert np.array_equal(r, np.array(mr, np.int32))
+            assert np.array_equal(l, np.array(ml, np.int32))
+        for p in range(0, len(self.m.base_ref), 7):
+            assert fk.forkkv_refcount(self.c, fk.JOB_BASE, p) == self.m.base_ref[p]
+
+
+def test_cpp_allocator_matches_model_on_forkserve_scenarios():
+    for L, k, ell in [(2048, 4, 64), (4096, 8, 128), (2050, 4, 48), (8192, 8, 32), (1024, 6, 4), (16384, 4, 256)]:
+        pr = _Pair(20000, 40000)
+        root = pr.op("create", L)
+        kids = []
+        for _ in range(k):
+            c, jobs = pr.op("fork", root, L, False)
+            kids.append(c)
+            pr.op("append", c, ell)
+        pr.check_state()
+        pr.op("free", root)
+        pr.check_state()
+        pr.close()
+
+
+def test_cpp_allocator_matches_model_on_random_operations():
+    rnd = random.Random(11)
+    pr = _Pair(200, 260)
+    live = []
+    for step in range(2500):
+        x = rnd.random()
+        if x < 0.2 or not live:
+            sid = pr.op("create", rnd.randint(0, 60))
+            if sid is not None:
+                live.append(sid)
+        elif x < 0.5:
+            par = rnd.choice(live)
+            res = pr.op("fork", par, rnd.randint(0, pr.m.seqs[par].length + 2), rnd.random() < 0.3)
+            if res is not None:
+                live.append(res[0])
+        elif x < 0.8:
+            pr.op("append", rnd.choice(live), rnd.randint(-1, 40))
+        else:
+            pr.op("free", live.pop(rnd.randrange(len(live))))
+        if step % 50 == 0:
+            pr.check_state()
+    pr.check_state()
+    for s in live:
+        pr.op("free", s)
+    st = fk.forkkv_stats_get(pr.c)
+    assert st["base_free"] == 200 and st["res_free"] == 260 and st["n_seqs"] == 0
+    pr.close()
+
+
+def test_invalid_arguments_rejected():
+    a = fk.forkkv_alloc_create(8, 8)
+    with pytest.raises(fk.ForkKVError) as e:
+        fk.forkkv_free(a, 123)
+    assert e.value.code == -1
+    with pytest.raises(fk.ForkKVError) as e:
+        fk.forkkv_refcount(a, fk.JOB_BASE, 8)
+    assert e.value.code == -3
+    with pytest.raises(fk.ForkKVError) as e:
+        fk.forkkv_alloc_create(8, 8, 32)
+    assert e.value.code == -5
+    fk.forkkv_alloc_destroy(a)
+
+
+def _tree_tables(rnd, n_agents_per, depth_tokens):
+    """Page tables of a random two-level fork tree built with the C++ allocator."""
+    a = fk.forkkv_alloc_create(100000, 200000)
+    root = fk.forkkv_seq_create(a, depth_tokens[0])
+    agents = []
+    for t in range(len(n_agents_per)):
+        trunk, _ = fk.forkkv_fork(a, root, depth_tokens[0])
+        fk.forkkv_append(a, trunk, depth_tokens[1])
+        L = depth_tokens[0] + depth_tokens[1]
+        for _ in range(n_agents_per[t]):
+            c, _ = fk.forkkv_fork(a, trunk, L)
+            fk.forkkv_append(a, c, rnd.randint(1, 300))
+            agents.append(c)
+    stride = max(fk.forkkv_seq_len(a, s) for s in agents) // 16 + 1
+    bpt, rpt, lens = fk.forkkv_page_tables(a, agents, stride)
+    fk.forkkv_alloc_destroy(a)
+    return bpt, lens
+
+
+@pytest.mark.parametrize("shape", [([3], (512, 0)), ([16, 16, 16, 16], (4096, 256)), ([1, 9, 5], (200, 37)),
+                                   ([2], (0, 0))])
+@pytest.mark.parametrize("target", [0, 7, 1000])
+def test_plan_covers_every_page_once(shape, target):
+    rnd = random.Random(5)
+    per, toks = shape
+    bpt, lens = _tree_tables(rnd, per, toks)
+    A = len(lens)
+    hkv = 8
+    plan, info = fk.forkkv_plan_build(bpt, lens, hkv, target)
+    items = plan[:info.n_items * fk.PLAN_ITEM_INTS].reshape(info.n_items, fk.PLAN_ITEM_INTS)
+    off = plan[info.n_items * fk.PLAN_ITEM_INTS:][:A + 1]
+    slots = plan[info.n_items * fk.PLAN_ITEM_INTS + A + 1:]
+    assert info.plan_ints == plan.size and len(slots) == info.n_slots
+    cover = {}
+    slot_owner = {}
+    for i, it in enumerate(items):
+        p0, p1, na, wpp = it[:4]
+        assert na in (1, 2, 4, 8) and wpp == 8 // na and 0 <= p0 < p1
+        ags = list(it[4:4 + na])
+        for x, ag in enumerate(ags):
+            slot_owner[it[12] + x] = ag
+        for pg in range(p0, p1):
+            phys = {bpt[ag, pg] for ag in ags}
+            assert len(phys) == 1  # one base page read for all agents of the item
+            for ag in ags:
+                assert pg < (lens[ag] + 15) // 16
+                assert (ag, pg) not in cover
+                cover[(ag, pg)] = i
+    for ag in range(A):
+        for pg in range((lens[ag] + 15) // 16):
+            assert (ag, pg) in cover
+        assert sorted(slots[off[ag]:off[ag + 1]]) == sorted(s for s, o in slot_owner.items() if o == ag)
+    assert off[A] == info.n_slots
