@@ -106,6 +106,7 @@ const char* forkkv_strerror(int32_t code) {
     case FORKKV_ERR_REFCOUNT: return "refcount underflow";
     case FORKKV_ERR_UNSUPPORTED: return "unsupported geometry (needs head_dim 128, rank 16, page 16, group <= 8)";
     case FORKKV_ERR_CUDA: return "CUDA runtime error";
+    case FORKKV_ERR_SCRATCH: return "workload needs more scratch than the static decode buffer holds";
     default: return "unknown status";
   }
 }

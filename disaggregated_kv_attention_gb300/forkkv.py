@@ -99,6 +99,7 @@ _SIGNATURES = {
     "forkkv_prefill_workspace_size": ([_P(forkkv_attn_params), _P(ctypes.c_size_t)], _i32),
     "forkkv_residual_attn_prefill_chunk": ([_P(forkkv_attn_params), _vp], _i32),
     "forkkv_get_device_status": ([_P(_u32), _vp], _i32),
+    "forkkv_residual_attn_decode_static": ([_P(forkkv_attn_params), _vp], _i32),
 }
 
 
@@ -327,6 +328,17 @@ def forkkv_residual_attn_decode(p: forkkv_attn_params, stream=None) -> None:
 
 def forkkv_residual_attn_prefill_chunk(p: forkkv_attn_params, stream=None) -> None:
     _check(lib().forkkv_residual_attn_prefill_chunk(ctypes.byref(p), _stream(stream)), "residual_attn_prefill_chunk")
+
+
+STATIC_SCRATCH_BYTES = 8 << 20
+ERR_SCRATCH = -7
+
+
+def forkkv_residual_attn_decode_static(p: forkkv_attn_params, stream=None) -> None:
+    """Decode with the library's own static scratch, for callers that cannot allocate device
+    memory (the workspace fields of ``p`` are ignored; see include/forkkv.h)."""
+    _check(lib().forkkv_residual_attn_decode_static(ctypes.byref(p), _stream(stream)),
+           "residual_attn_decode_static")
 
 
 def forkkv_get_device_status(stream=None) -> int:

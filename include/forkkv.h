@@ -64,6 +64,7 @@ extern "C" {
 #define FORKKV_ERR_REFCOUNT (-4)     /* refcount would underflow               */
 #define FORKKV_ERR_UNSUPPORTED (-5)  /* geometry other than D=128, r=16, P=16  */
 #define FORKKV_ERR_CUDA (-6)         /* a CUDA runtime call failed             */
+#define FORKKV_ERR_SCRATCH (-7)      /* needs more than the static decode scratch */
 
 /* device status bits (forkkv_get_device_status) */
 #define FORKKV_DEV_BAD_PAGE 1u  /* a page id read from a device table was out of range */
@@ -270,6 +271,31 @@ int32_t forkkv_prefill_workspace_size(const forkkv_attn_params* p, size_t* bytes
  * `positions`, causal (key j visible iff j <= position and j < seq_len).  The
  * chunk's own rows must already be in the pools (forkkv_write_rows). */
 int32_t forkkv_residual_attn_prefill_chunk(const forkkv_attn_params* p, void* stream);
+
+/* ==== decode without caller scratch =======================================
+ * No counterpart in the paper: an addition for callers that cannot allocate.
+ * Some callers own no spare device memory to lend as scratch (a serving engine
+ * that gives nearly all free HBM to its own KV-cache pool at start-up, or a
+ * plugin host that calls an attention op without offering a workspace and
+ * forbids cudaMalloc on its hot path, since an allocation can synchronise the
+ * device and can fail under memory pressure).  This entry point computes
+ * exactly what forkkv_residual_attn_decode computes, with the same arguments,
+ * but keeps its scratch in a fixed array of FORKKV_STATIC_SCRATCH_BYTES inside
+ * the library's device image, which every GPU that loads the library holds
+ * until the process exits.  The workspace fields of `p` are ignored; nothing
+ * is allocated (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - Workloads whose scratch (forkkv_decode_workspace_size, which includes the
+ *     rotation table when `p->rope_table` is NULL) exceeds the array are
+ *     rejected with FORKKV_ERR_SCRATCH before anything is launched.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array and leaves its contents behind; nothing
+ *     in it needs to start at zero (every partial is written before it is read).
+ *     Calls whose kernels overlap on the GPU (different streams without
+ *     ordering, or concurrent host threads) race on the array: serialise them. */
+#define FORKKV_STATIC_SCRATCH_BYTES (8u << 20)
+int32_t forkkv_residual_attn_decode_static(const forkkv_attn_params* p, void* stream);
 
 /* Read and clear the device status word of the current device (OR of
  * FORKKV_DEV_* bits set by kernels since the last read).  Synchronises
