@@ -14,7 +14,7 @@ constexpr int kHeadDim = 128;
 constexpr int kRank = 16;
 constexpr int kBaseTile = 4096;  // 16 rows x 128 bf16
 constexpr int kResTile = 512;    // 16 rows x 16 bf16
-constexpr int kRopeRow = 256;    // 64 frequencies x (cos, sin) fp16
+constexpr int kRopeRow = 256;    // 64 frequencies x (cos, sin) bf16
 
 constexpr uint32_t kDevBadPage = 1u;
 constexpr uint32_t kDevTimeout = 2u;

@@ -37,7 +37,7 @@ constexpr int kWarps = 8;                    // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
 constexpr int kMaxStages = 8;
 constexpr int kSmemBytes = 227 * 1024;  // the sm_100 family's per-block maximum
-constexpr int kHeaderBytes = 1024;           // mbarriers
+constexpr int kHeaderBytes = 4096;           // mbarriers, agent ids, page-id cache
 constexpr int kPartCols = kHeadDim + kRank;  // 144 floats per (slot, head, query head)
 
 struct DecodeArgs {
@@ -71,7 +71,12 @@ struct Item {
   int32_t agents[8];
 };
 
-__device__ __forceinline__ int32_t stage_bytes(int32_t wpp) { return wpp * (2 * kBaseTile + 16 * kRopeRow) + 8 * 2 * kResTile; }
+// Pages per pipeline stage for a group of na agents (8 consumer warps = na x warps-per-agent).
+__device__ __forceinline__ int32_t stage_pages(int32_t na) { return na == 8 ? 2 : na == 1 ? 8 : 4; }
+// Stage layout: [SP][K tile] [SP][V tile] [SP][16 rotation rows] [na][SP][k_res] [na][SP][v_res]
+__device__ __forceinline__ int32_t stage_bytes(int32_t sp, int32_t na) {
+  return sp * (2 * kBaseTile + 16 * kRopeRow) + 2 * na * sp * kResTile;
+}
 
 __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
   Item it;
@@ -88,7 +93,7 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
       flag_status(a.status, kDevBadArg);
       it.na = 1;
     }
-    it.wpp = 8 / it.na;
+    it.wpp = 8 / it.na;  // warps per agent
     if (it.slot_base < 0 || it.slot_base + it.na > a.n_slots) {
       flag_status(a.status, kDevBadArg);
       it.p1 = it.p0;  // empty: writes nothing useful, reads nothing
@@ -121,23 +126,40 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
   return it;
 }
 
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hadd2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Rotate the pair (lo, hi) = (U_d, U_{d+64}) of two adjacent columns by (cos, sin), bf16x2.
+__device__ __forceinline__ void rotate_bf16x2(uint32_t& lo, uint32_t& hi, uint32_t c, uint32_t s) {
+  const __nv_bfloat162 L = *reinterpret_cast<__nv_bfloat162*>(&lo), H = *reinterpret_cast<__nv_bfloat162*>(&hi);
+  const __nv_bfloat162 C = *reinterpret_cast<__nv_bfloat162*>(&c), S = *reinterpret_cast<__nv_bfloat162*>(&s);
+  const __nv_bfloat162 l2 = __hfma2(L, C, __hneg2(__hmul2(H, S)));
+  const __nv_bfloat162 h2 = __hfma2(L, S, __hmul2(H, C));
+  lo = *reinterpret_cast<const uint32_t*>(&l2);
+  hi = *reinterpret_cast<const uint32_t*>(&h2);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
+  int32_t* s_agents = reinterpret_cast<int32_t*>(smem + 256);  // [8]
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + 512);     // [16 stages][32] page ids (producer only)
   uint8_t* stages = smem + kHeaderBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   const Item it = load_item(a);
   const int na = it.na, wpp = it.wpp;
-  const int32_t sbytes = stage_bytes(wpp);
+  const int SP = stage_pages(na);
+  const int32_t sbytes = stage_bytes(SP, na);
   const int NS = min(kMaxStages, (kSmemBytes - kHeaderBytes) / sbytes);
   const int n_pages = it.p1 - it.p0;
-  const int n_stages = (n_pages + wpp - 1) / wpp;
-  // stage layout: [wpp][K tile | V tile] [wpp][rotation rows of 16 positions] [8 warps][k_res | v_res]
-  const int32_t rope_at = wpp * 2 * kBaseTile;
-  const int32_t res_at = rope_at + wpp * 16 * kRopeRow;
+  const int n_stages = (n_pages + SP - 1) / SP;
+  const int32_t v_at = SP * kBaseTile, rope_at = 2 * SP * kBaseTile, kr_at = rope_at + SP * 16 * kRopeRow;
+  const int32_t vr_at = kr_at + na * SP * kResTile;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
@@ -146,9 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
     mbar_fence_init();
   }
+  if (threadIdx.x < 8) s_agents[threadIdx.x] = it.agents[threadIdx.x];
   __syncthreads();
 
-  const int64_t base_tile_stride = (int64_t)a.hkv * kBaseTile;
+  const int64_t head_base = (int64_t)h * a.num_base_pages;  // first tile of this head (page-major)
   const int g = lane >> 2, q4 = lane & 3;
 
   // per-warp partial (consumers): acc^T [d][query head], acc_r^T [k][query head], m, l
@@ -163,48 +186,82 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 
   if (warp == kWarps) {
     // ------------------------------ producer ------------------------------
-    const int32_t lead = it.agents[0];
+    // s_ids[stage % 16][32]: [0, SP) base page ids, [8 + ai*SP + pg] residual page id of agent ai, page pg
+    const int32_t lead = s_agents[0];
     int issued = 0;
     bool ok = true;
     for (int s = 0; s < n_stages && ok; ++s) {
+      if ((s & 15) == 0) {
+        int32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {  // 16 independent loads per lane, all in flight together
+          v[i] = -1;
+          const int ss = s + i;
+          if (ss < n_stages) {
+            if (lane < 8) {
+              const int pi = it.p0 + ss * SP + lane;
+              if (lane < SP && pi < it.p1) v[i] = a.bpt[(int64_t)lead * a.pt_stride + pi];
+            } else if (lane < 8 + na * SP) {
+              const int ai = (lane - 8) / SP, pg = (lane - 8) % SP;
+              const int pi = it.p0 + ss * SP + pg;
+              if (pi < it.p1) v[i] = a.rpt[(int64_t)s_agents[ai] * a.pt_stride + pi];
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          int32_t x = v[i];
+          const int32_t lim = lane < 8 ? a.num_base_pages : a.num_res_pages;
+          if (x != -1 && (uint32_t)x >= (uint32_t)lim) {
+            flag_status(a.status, kDevBadPage);
+            x = 0;
+          }
+          s_ids[i * 32 + lane] = x;
+        }
+        __syncwarp();
+      }
       const int slot = s % NS;
       const uint32_t round = s / NS;
       if (s >= NS) ok = mbar_wait(&empty[slot], (round - 1) & 1, a.status);
       if (!ok) break;
-      const int pbase = it.p0 + s * wpp;
-      const int nvp = min(wpp, it.p1 - pbase);
+      const int pbase = it.p0 + s * SP;
+      const int nvp = min(SP, it.p1 - pbase);
       uint8_t* st = stages + (int64_t)slot * sbytes;
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], nvp * (2 * kBaseTile + 16 * kRopeRow) + nvp * na * 2 * kResTile);
+      const int32_t* ids = s_ids + (s & 15) * 32;
+      if (lane == 0) mbar_arrive_expect_tx(&full[slot], nvp * (2 * kBaseTile + 16 * kRopeRow) + na * nvp * 2 * kResTile);
       __syncwarp();
-      if (lane < nvp) {
-        const int pi = pbase + lane;
-        int32_t page = a.bpt[(int64_t)lead * a.pt_stride + pi];
-        if ((uint32_t)page >= (uint32_t)a.num_base_pages) {
-          flag_status(a.status, kDevBadPage);
-          page = 0;
+      if (lane < 2) {
+        // K (lane 0) or V (lane 1) tiles: one bulk copy per run of consecutive page ids
+        const uint8_t* pool = lane == 0 ? a.k_base : a.v_base;
+        uint8_t* dst = st + (lane == 0 ? 0 : v_at);
+        int r0 = 0;
+        for (int pg = 1; pg <= nvp; ++pg) {
+          if (pg == nvp || ids[pg] != ids[pg - 1] + 1) {
+            bulk_g2s(dst + r0 * kBaseTile, pool + (head_base + ids[r0]) * kBaseTile, (pg - r0) * kBaseTile,
+                     &full[slot]);
+            r0 = pg;
+          }
         }
-        int64_t rrow = (int64_t)pi * 16;
-        if (rrow + 16 > a.rope_positions) {
+      } else if (lane == 2) {
+        int64_t rrow = (int64_t)pbase * 16;
+        if (rrow + 16 * nvp > a.rope_positions) {
           flag_status(a.status, kDevBadArg);
           rrow = 0;
         }
-        const int64_t off = (int64_t)page * base_tile_stride + (int64_t)h * kBaseTile;
-        bulk_g2s(st + lane * 2 * kBaseTile, a.k_base + off, kBaseTile, &full[slot]);
-        bulk_g2s(st + lane * 2 * kBaseTile + kBaseTile, a.v_base + off, kBaseTile, &full[slot]);
-        bulk_g2s(st + rope_at + lane * 16 * kRopeRow, a.rope + rrow * kRopeRow, 16 * kRopeRow, &full[slot]);
-      } else if (lane >= 8 && lane < 16) {
-        const int w = lane - 8;
-        const int ai = w % na, pl = w / na;
-        if (pl < nvp) {
-          const int pi = pbase + pl;
-          int32_t page = a.rpt[(int64_t)it.agents[ai] * a.pt_stride + pi];
-          if ((uint32_t)page >= (uint32_t)a.num_res_pages) {
-            flag_status(a.status, kDevBadPage);
-            page = 0;
+        bulk_g2s(st + rope_at, a.rope + rrow * kRopeRow, nvp * 16 * kRopeRow, &full[slot]);
+      } else if (lane >= 8 && lane < 8 + na) {
+        // residual k and v tiles of one agent, one copy per run of consecutive page ids
+        const int ai = lane - 8;
+        const int32_t* rid = ids + 8 + ai * SP;
+        int r0 = 0;
+        for (int pg = 1; pg <= nvp; ++pg) {
+          if (pg == nvp || rid[pg] != rid[pg - 1] + 1) {
+            const int64_t src = (int64_t)rid[r0] * kResTile;
+            const uint32_t n = (pg - r0) * kResTile;
+            bulk_g2s(st + kr_at + (ai * SP + r0) * kResTile, a.k_res + src, n, &full[slot]);
+            bulk_g2s(st + vr_at + (ai * SP + r0) * kResTile, a.v_res + src, n, &full[slot]);
+            r0 = pg;
           }
-          bulk_g2s(st + res_at + w * 2 * kResTile, a.k_res + (int64_t)page * kResTile, kResTile, &full[slot]);
-          bulk_g2s(st + res_at + w * 2 * kResTile + kResTile, a.v_res + (int64_t)page * kResTile, kResTile,
-                   &full[slot]);
         }
       }
       issued = s + 1;
@@ -214,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   } else {
     // ------------------------------ consumers ------------------------------
     const int ai = warp % na, pl = warp / na;
-    const int32_t agent = it.agents[ai];
+    const int32_t agent = s_agents[ai];
     const int32_t L = a.seq_lens[agent];
     const int32_t pos = a.positions[agent];
     const int G = a.G;
@@ -226,22 +283,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       adapter = 0;
     }
 
-    // q^T operand fragments (B of m16n8k16: n = query head g, k = d), bf16 and fp16
-    uint32_t qb[8][2], qh[8][2];
+    // q^T operand fragments (B of m16n8k16: n = query head g, k = d), bf16
+    uint32_t qb[8][2];
     {
       const __nv_bfloat16* qrow = a.q + ((int64_t)agent * a.hkv * G + (int64_t)h * G + g) * kHeadDim;
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
+      for (int s = 0; s < 8; ++s)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int d = 16 * s + 8 * e + 2 * q4;
-          uint32_t raw = 0;
-          if (g < G) raw = *reinterpret_cast<const uint32_t*>(qrow + d);
-          qb[s][e] = raw;
-          const float2 f = bf2_to_f2(raw);
-          qh[s][e] = pack_f16(f.x, f.y);
-        }
-      }
+        for (int e = 0; e < 2; ++e)
+          qb[s][e] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s + 8 * e + 2 * q4) : 0u;
     }
     // B_k operand fragments (B of m16n8k16: k = rank, n = d within the head)
     uint32_t bk[16][2];
@@ -262,34 +312,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       }
     }
 
+    // per-lane shared-memory offsets (loop invariant)
     const int mi = lane >> 3;
-    const int lrow = (lane & 7) + (mi & 1) * 8;   // ldmatrix row for the non-transposed A loads
-    const int tkey = (lane & 7) + (mi >> 1) * 8;  // ldmatrix row for the transposed loads
+    const int lrow = (lane & 7) + (mi & 1) * 8, bsel = mi >> 1;  // A fragments of K (keys x d), Kr
+    const int tkey = (lane & 7) + (mi >> 1) * 8, vsel = mi & 1;  // transposed A fragments of V, Vr
+    uint32_t kofs[4], vofs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      kofs[i] = lrow * 128 + (((2 * i + bsel) ^ (lrow & 7)) << 4);
+      vofs[i] = tkey * 128 + (((2 * i + vsel) ^ (tkey & 7)) << 4);
+    }
+    const uint32_t krofs = res_off(lrow, bsel * 8), vrofs = res_off(tkey, vsel * 8);
+    const uint32_t rrow0 = g * kRopeRow + q4 * 8, rrow1 = (g + 8) * kRopeRow + q4 * 8;
 
     for (int s = 0; s < n_stages; ++s) {
       const int slot = s % NS;
       if (!mbar_wait(&full[slot], (s / NS) & 1, a.status)) break;
-      const int pi = it.p0 + s * wpp + pl;
-      if (pi < it.p1) {
-        const uint8_t* st = stages + (int64_t)slot * sbytes;
-        const uint32_t sK = smem_u32(st + pl * 2 * kBaseTile);
-        const uint32_t sV = sK + kBaseTile;
-        const uint32_t sR = smem_u32(st + rope_at + pl * 16 * kRopeRow);
-        const uint32_t sKr = smem_u32(st + res_at + warp * 2 * kResTile);
-        const uint32_t sVr = sKr + kResTile;
-        const int j0 = pi * kPage;
+      const int pbase = it.p0 + s * SP;
+      const int nvp = min(SP, it.p1 - pbase);
+      const uint32_t st = smem_u32(stages + (int64_t)slot * sbytes);
+      for (int pg = pl; pg < nvp; pg += wpp) {
+        const uint32_t sK = st + pg * kBaseTile;
+        const uint32_t sV = st + v_at + pg * kBaseTile;
+        const uint32_t sR = st + rope_at + pg * 16 * kRopeRow;
+        const uint32_t sKr = st + kr_at + (ai * SP + pg) * kResTile;
+        const uint32_t sVr = st + vr_at + (ai * SP + pg) * kResTile;
+        const int j0 = (pbase + pg) * kPage;
 
-        float S[4] = {0.f, 0.f, 0.f, 0.f};
-        // base scores: S^T += Kb . q^T
-#pragma unroll
-        for (int s8 = 0; s8 < 8; ++s8) {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4(sK + base_off(lrow, 16 * s8 + (mi >> 1) * 8), r0, r1, r2, r3);
-          mma_bf16(S, r0, r1, r2, r3, qb[s8][0], qb[s8][1]);
-        }
-        // residual keys: up-project, rotate (deferred RoPE), score
+        // full keys K = Kb + RoPE_j(Kr B_k) as A fragments, and S^T = K q^T
+        float S0[4] = {0.f, 0.f, 0.f, 0.f}, S1[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t ka0, ka1, ka2, ka3;
-        ldsm_x4(sKr + res_off(lrow, (mi >> 1) * 8), ka0, ka1, ka2, ka3);
+        ldsm_x4(sKr + krofs, ka0, ka1, ka2, ka3);
 #pragma unroll
         for (int s4 = 0; s4 < 4; ++s4) {
           float U[4][4];
@@ -299,71 +352,79 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             U[x][0] = U[x][1] = U[x][2] = U[x][3] = 0.f;
             mma_bf16(U[x], ka0, ka1, ka2, ka3, bk[t][0], bk[t][1]);
           }
-          uint32_t lo_[2][2], hi_[2][2];  // [tile 2s4 | 2s4+1][row g | g+8]
+          uint32_t klo[4], khi[4];  // Kb fragments of k-steps s4 (d < 64) and s4 + 4 (d >= 64)
+          ldsm_x4(sK + kofs[s4], klo[0], klo[1], klo[2], klo[3]);
+          ldsm_x4(sK + 2048 + kofs[s4], khi[0], khi[1], khi[2], khi[3]);
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
-            const int m = 4 * (2 * s4 + x) + q4;  // frequency group of d = 8t + 2q4
+            const uint32_t cofs = ((2 * s4 + x) ^ g) << 5;  // frequency group 4(2s4+x)+q4, swizzled by row
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-              const int kr = g + 8 * rr;
-              const uint2 cs = ld_shared_u64(sR + kr * kRopeRow + rope_off(kr, m));
-              const __half2 c = as_h2(cs.x), sn = as_h2(cs.y);
-              const __half2 lo = __floats2half2_rn(U[x][2 * rr], U[x][2 * rr + 1]);
-              const __half2 hi = __floats2half2_rn(U[x + 2][2 * rr], U[x + 2][2 * rr + 1]);
-              lo_[x][rr] = as_u32(__hfma2(lo, c, __hneg2(__hmul2(hi, sn))));
-              hi_[x][rr] = as_u32(__hfma2(lo, sn, __hmul2(hi, c)));
+              const uint2 cs = ld_shared_u64(sR + (rr ? rrow1 : rrow0) + cofs);
+              uint32_t lo = pack_bf16(U[x][2 * rr], U[x][2 * rr + 1]);
+              uint32_t hi = pack_bf16(U[x + 2][2 * rr], U[x + 2][2 * rr + 1]);
+              rotate_bf16x2(lo, hi, cs.x, cs.y);
+              klo[2 * x + rr] = bf2_add(klo[2 * x + rr], lo);
+              khi[2 * x + rr] = bf2_add(khi[2 * x + rr], hi);
             }
           }
-          mma_f16(S, lo_[0][0], lo_[0][1], lo_[1][0], lo_[1][1], qh[s4][0], qh[s4][1]);
-          mma_f16(S, hi_[0][0], hi_[0][1], hi_[1][0], hi_[1][1], qh[s4 + 4][0], qh[s4 + 4][1]);
+          mma_bf16(S0, klo[0], klo[1], klo[2], klo[3], qb[s4][0], qb[s4][1]);
+          mma_bf16(S1, khi[0], khi[1], khi[2], khi[3], qb[s4 + 4][0], qb[s4 + 4][1]);
         }
-        // mask + online softmax (base-2 exponent, scale folded in)
-        const int ja = j0 + g, jb = j0 + g + 8;
-        const bool va = ja < L && ja <= pos, vb = jb < L && jb <= pos;
-        const float s0 = va ? S[0] * a.scale_log2 : -INFINITY;
-        const float s1 = va ? S[1] * a.scale_log2 : -INFINITY;
-        const float s2 = vb ? S[2] * a.scale_log2 : -INFINITY;
-        const float s3 = vb ? S[3] * a.scale_log2 : -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+        // mask (only the last pages of an agent need it) + online softmax in base 2
+        float sc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = (S0[e] + S1[e]) * a.scale_log2;
+        if (!(j0 + kPage - 1 < L && j0 + kPage - 1 <= pos)) {
+          const int ja = j0 + g, jb = j0 + g + 8;
+          if (!(ja < L && ja <= pos)) sc[0] = sc[1] = -INFINITY;
+          if (!(jb < L && jb <= pos)) sc[2] = sc[3] = -INFINITY;
+        }
+        float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-        const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
-        const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
-        l0 = l0 * al0 + p0 + p2;
-        l1 = l1 * al1 + p1 + p3;
-        m0 = mn0;
-        m1 = mn1;
+        // lazy rescale: move the reference maximum only when a score exceeds it by 2^8
+        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+          const float al0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
+          const float al1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+          l0 *= al0;
+          l1 *= al1;
 #pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-          acc[mb][0] *= al0;
-          acc[mb][1] *= al1;
-          acc[mb][2] *= al0;
-          acc[mb][3] *= al1;
+          for (int mb = 0; mb < 8; ++mb) {
+            acc[mb][0] *= al0;
+            acc[mb][1] *= al1;
+            acc[mb][2] *= al0;
+            acc[mb][3] *= al1;
+          }
+          accr[0] *= al0;
+          accr[1] *= al1;
+          accr[2] *= al0;
+          accr[3] *= al1;
+          m0 = mn0;
+          m1 = mn1;
         }
-        accr[0] *= al0;
-        accr[1] *= al1;
-        accr[2] *= al0;
-        accr[3] *= al1;
+        const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+        const float p0 = exp2f(sc[0] - mu0), p2 = exp2f(sc[2] - mu0);
+        const float p1 = exp2f(sc[1] - mu1), p3 = exp2f(sc[3] - mu1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
         // probabilities as the B operand (k = key, n = query head)
         const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
         const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
-        // acc^T += Vb^T . P^T
+        // acc^T += Vb^T . P^T ; acc_r^T += Vr^T . P^T
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb) {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(sV + base_off(tkey, 16 * mb + (mi & 1) * 8), r0, r1, r2, r3);
+          ldsm_x4_t(sV + (mb >> 2) * 2048 + vofs[mb & 3], r0, r1, r2, r3);
           mma_bf16(acc[mb], r0, r1, r2, r3, pb0, pb1);
         }
-        // acc_r^T += Vr^T . P^T
         {
           uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(sVr + res_off(tkey, (mi & 1) * 8), r0, r1, r2, r3);
+          ldsm_x4_t(sVr + vrofs, r0, r1, r2, r3);
           mma_bf16(accr, r0, r1, r2, r3, pb0, pb1);
         }
       }
@@ -448,9 +509,18 @@ struct CombineArgs {
   __nv_bfloat16* out;        // [A][Hq][128]
 };
 
+constexpr int kCombineSlots = 1024;  // slots handled per pass
+
+// One CTA per (agent, KV head, query head): log-sum-exp merge of the agent's
+// partials, then out = (acc + acc_r B_v[:, hD:(h+1)D]) / l.  All partial loads
+// of a pass are independent, so their latencies overlap.
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ CombineArgs a) {
-  const int agent = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+  const int agent = blockIdx.x, h = blockIdx.y, gq = blockIdx.z, d = threadIdx.x;
   const int G = a.G;
+  __shared__ float s_w[kCombineSlots];
+  __shared__ int32_t s_slot[kCombineSlots];
+  __shared__ float s_red[4];
+  __shared__ float s_accr[kRank];
   int32_t s_begin, s_end;
   if (a.csr_off) {
     s_begin = a.csr_off[agent];
@@ -459,47 +529,65 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     s_begin = agent * a.chunks;
     s_end = s_begin + a.chunks;
   }
-  int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
-  if ((uint32_t)adapter >= (uint32_t)a.n_adapters) adapter = 0;
-  float bv[kRank];
-  {
-    const __nv_bfloat16* B = a.B_v + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim + d;
-#pragma unroll
-    for (int k = 0; k < kRank; ++k) bv[k] = __bfloat162float(B[(int64_t)k * a.hkv * kHeadDim]);
-  }
-  __shared__ float accr_s[kRank];
   if (s_begin < 0 || s_end < s_begin || s_end > a.n_slots) {
     if (d == 0) flag_status(a.status, kDevBadArg);
     s_end = s_begin = 0;
   }
-  for (int gq = 0; gq < G; ++gq) {
-    float M = -INFINITY;
-    for (int i = s_begin; i < s_end; ++i) {
-      const int32_t slot = a.csr_off ? a.csr_slots[i] : i;
-      if ((uint32_t)slot >= (uint32_t)a.n_slots) continue;
-      M = fmaxf(M, a.ml[(((int64_t)slot * a.hkv + h) * G + gq) * 2]);
-    }
-    float acc = 0.f, accr = 0.f, lsum = 0.f;
-    for (int i = s_begin; i < s_end; ++i) {
-      const int32_t slot = a.csr_off ? a.csr_slots[i] : i;
-      if ((uint32_t)slot >= (uint32_t)a.n_slots) continue;
-      const int64_t rec = ((int64_t)slot * a.hkv + h) * G + gq;
-      const float m = a.ml[rec * 2];
-      if (m == -INFINITY) continue;
-      const float wt = exp2f(m - M);
-      lsum += wt * a.ml[rec * 2 + 1];
-      acc += wt * a.part[rec * kPartCols + d];
-      if (d < kRank) accr += wt * a.part[rec * kPartCols + kHeadDim + d];
-    }
-    __syncthreads();
-    if (d < kRank) accr_s[d] = accr;
-    __syncthreads();
-    float o = acc;
+  int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
+  if ((uint32_t)adapter >= (uint32_t)a.n_adapters) adapter = 0;
+  const __nv_bfloat16* Bv = a.B_v + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim + d;
+  float bv[kRank];
 #pragma unroll
-    for (int k = 0; k < kRank; ++k) o += accr_s[k] * bv[k];
-    o = lsum > 0.f ? o / lsum : 0.f;
-    a.out[((int64_t)agent * a.hkv * G + (int64_t)h * G + gq) * kHeadDim + d] = __float2bfloat16_rn(o);
+  for (int k = 0; k < kRank; ++k) bv[k] = __bfloat162float(Bv[(int64_t)k * a.hkv * kHeadDim]);
+
+  // pass 1: global maximum of the reference maxima
+  float M = -INFINITY;
+  for (int i = s_begin + d; i < s_end; i += 128) {
+    int32_t slot = a.csr_off ? a.csr_slots[i] : i;
+    if ((uint32_t)slot >= (uint32_t)a.n_slots) slot = -1;
+    if (slot >= 0) M = fmaxf(M, a.ml[(((int64_t)slot * a.hkv + h) * G + gq) * 2]);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if ((d & 31) == 0) s_red[d >> 5] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+
+  float acc = 0.f, accr = 0.f, lsum = 0.f;
+  for (int b0 = s_begin; b0 < s_end; b0 += kCombineSlots) {
+    const int nb = min(kCombineSlots, s_end - b0);
+    __syncthreads();
+    for (int i = d; i < nb; i += 128) {
+      int32_t slot = a.csr_off ? a.csr_slots[b0 + i] : b0 + i;
+      float w = 0.f;
+      if ((uint32_t)slot < (uint32_t)a.n_slots) {
+        const float m = a.ml[(((int64_t)slot * a.hkv + h) * G + gq) * 2];
+        w = (m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(m - M);
+      } else {
+        slot = 0;
+      }
+      s_w[i] = w;
+      s_slot[i] = slot;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int i = 0; i < nb; ++i) {
+      const float w = s_w[i];
+      const int64_t rec = ((int64_t)s_slot[i] * a.hkv + h) * G + gq;
+      acc += w * a.part[rec * kPartCols + d];
+      if (d < kRank) accr += w * a.part[rec * kPartCols + kHeadDim + d];
+      if (d == 0) lsum += w * a.ml[rec * 2 + 1];
+    }
+  }
+  if (d < kRank) s_accr[d] = accr;
+  if (d == 0) s_red[0] = lsum;
+  __syncthreads();
+  float o = acc;
+#pragma unroll
+  for (int k = 0; k < kRank; ++k) o += s_accr[k] * bv[k];
+  lsum = s_red[0];
+  o = lsum > 0.f ? o / lsum : 0.f;
+  a.out[((int64_t)agent * a.hkv * G + (int64_t)h * G + gq) * kHeadDim + d] = __float2bfloat16_rn(o);
 }
 
 }  // namespace
@@ -599,7 +687,7 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   c.adapter_ids = p.adapter_ids;
   c.n_adapters = p.n_adapters;
   c.out = static_cast<__nv_bfloat16*>(p.out);
-  decode_combine_kernel<<<dim3(p.n_agents, p.num_kv_heads), 128, 0, stream>>>(c);
+  decode_combine_kernel<<<dim3(p.n_agents, p.num_kv_heads, G), 128, 0, stream>>>(c);
   return cudaGetLastError();
 }
 

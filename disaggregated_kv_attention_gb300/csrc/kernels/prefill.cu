@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int32_t key_limit = s_meta[0];
   const int n_pages = max(0, (key_limit + kPage - 1) / kPage);
   const int n_stages = (n_pages + kPagesPerStage - 1) / kPagesPerStage;
-  const int64_t base_tile_stride = (int64_t)a.hkv * kBaseTile;
+  const int64_t head_base = (int64_t)h * a.num_base_pages * kBaseTile;  // this head's tiles, page-major
 
   int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
   if ((uint32_t)adapter >= (uint32_t)a.n_adapters) {
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           flag_status(a.status, kDevBadArg);
           rrow = 0;
         }
-        const int64_t off = (int64_t)bpage * base_tile_stride + (int64_t)h * kBaseTile;
+        const int64_t off = head_base + (int64_t)bpage * kBaseTile;
         bulk_g2s(st + lane * 2 * kBaseTile, a.k_base + off, kBaseTile, &full[slot]);
         bulk_g2s(st + lane * 2 * kBaseTile + kBaseTile, a.v_base + off, kBaseTile, &full[slot]);
         bulk_g2s(st + kRopeAt + lane * 16 * kRopeRow, a.rope + rrow * kRopeRow, 16 * kRopeRow, &full[slot]);
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int rr = 0; rr < 2; ++rr) {
           const int kr = g + 8 * rr;
           const uint2 cs = ld_shared_u64(sR + kr * kRopeRow + rope_off(kr, m));
-          const float2 c = __half22float2(as_h2(cs.x)), sn = __half22float2(as_h2(cs.y));
+          const float2 c = bf2_to_f2(cs.x), sn = bf2_to_f2(cs.y);
           const float l0 = ulo[2 * rr], l1 = ulo[2 * rr + 1], h0 = uhi[2 * rr], h1 = uhi[2 * rr + 1];
           const float2 kbl = bf2_to_f2(ld_shared_u32(sKb + base_off(kr, d)));
           const float2 kbh = bf2_to_f2(ld_shared_u32(sKb + base_off(kr, d + 64)));

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) write_rows_kernel(const WriteArgs a) {
     }
     const uint4* src = kv ? a.vb : a.kb;
     const uint4 v = src[((int64_t)row * a.hkv + h) * 16 + c];
-    uint8_t* dst = (kv ? a.v_base : a.k_base) + (page * a.hkv + h) * kBaseTile + base_off(t, c * 8);
+    uint8_t* dst = (kv ? a.v_base : a.k_base) + ((int64_t)h * a.num_base_pages + page) * kBaseTile + base_off(t, c * 8);
     *reinterpret_cast<uint4*>(dst) = v;
   } else {
     if (!a.slot_res) return;
@@ -76,11 +76,12 @@ struct CowArgs {
   uint8_t* k_res;
   uint8_t* v_res;
   int64_t base_layer_bytes, res_layer_bytes;
+  int64_t num_base_pages;
   int32_t hkv;
 };
 
 // blockIdx.x = job, blockIdx.y = layer.  A base row t occupies the two 128-byte
-// segments at t*128 and 2048 + t*128 of each (page, head) tile (the swizzle only
+// segments at t*128 and 2048 + t*128 of each (head, page) tile (the swizzle only
 // permutes chunks inside a segment), a residual row the 32 bytes at t*32.
 __global__ void __launch_bounds__(256) cow_copy_kernel(const CowArgs a, const __grid_constant__ CowJobBatch b) {
   const forkkv_cow_job job = b.jobs[blockIdx.x];
@@ -94,8 +95,9 @@ __global__ void __launch_bounds__(256) cow_copy_kernel(const CowArgs a, const __
       const int32_t t = c >> 4, part = (c >> 3) & 1, w = c & 7;
       const uint32_t off = part * 2048 + t * 128 + w * 16;
       uint8_t* pool = (kv ? a.v_base : a.k_base) + layer * a.base_layer_bytes;
-      const uint4 v = *reinterpret_cast<const uint4*>(pool + ((int64_t)job.src_page * a.hkv + h) * kBaseTile + off);
-      *reinterpret_cast<uint4*>(pool + ((int64_t)job.dst_page * a.hkv + h) * kBaseTile + off) = v;
+      const int64_t head0 = (int64_t)h * a.num_base_pages;
+      const uint4 v = *reinterpret_cast<const uint4*>(pool + (head0 + job.src_page) * kBaseTile + off);
+      *reinterpret_cast<uint4*>(pool + (head0 + job.dst_page) * kBaseTile + off) = v;
     }
   } else {
     const int32_t total = 2 * job.n_valid * 2;
@@ -131,11 +133,9 @@ __global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__
     const float y = (float)(int64_t)frac * 0x1p-63f;            // 2 * turns in [-1, 1)
     sincospif(y, &sn[e], &cs[e]);
   }
-  __half2 c2 = __floats2half2_rn(cs[0], cs[1]);
-  __half2 s2 = __floats2half2_rn(sn[0], sn[1]);
   uint2 v;
-  v.x = *reinterpret_cast<uint32_t*>(&c2);
-  v.y = *reinterpret_cast<uint32_t*>(&s2);
+  v.x = pack_bf16(cs[0], cs[1]);
+  v.y = pack_bf16(sn[0], sn[1]);
   *reinterpret_cast<uint2*>(a.table + (int64_t)p * kRopeRow + rope_off(p, m)) = v;
 }
 
@@ -178,6 +178,7 @@ cudaError_t launch_cow_copy(const forkkv_pool_desc& pools, const CowJobBatch& ba
   a.v_res = static_cast<uint8_t*>(pools.v_res);
   a.base_layer_bytes = (int64_t)pools.num_base_pages * pools.num_kv_heads * kBaseTile;
   a.res_layer_bytes = (int64_t)pools.num_res_pages * kResTile;
+  a.num_base_pages = pools.num_base_pages;
   a.hkv = pools.num_kv_heads;
   cow_copy_kernel<<<dim3(batch.n, pools.n_layers), 256, 0, stream>>>(a, batch);
   return cudaGetLastError();

@@ -22,8 +22,9 @@ struct Segment {
   int32_t p0, p1;
 };
 
-// Work pages per stage for a group of na agents: 8 consumer warps = na * wpp.
-int32_t pages_per_stage(int32_t na) { return 8 / na; }
+// Pages per pipeline stage of the decode kernel for a group of na agents (it
+// has 8 consumer warps: 8 / na warps per agent, each taking stage pages in turn).
+int32_t pages_per_stage(int32_t na) { return na == 8 ? 2 : na == 1 ? 8 : 4; }
 
 int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents, int32_t pt_stride,
                    int32_t num_kv_heads, int32_t target_ctas, int32_t* plan, int32_t plan_cap_ints,

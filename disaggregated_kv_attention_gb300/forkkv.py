@@ -217,8 +217,8 @@ class Pools:
                  device="cuda", fill: Optional[int] = None):
         mk = (lambda shape: torch.full(shape, fill, dtype=torch.uint8, device=device)) if fill is not None else \
             (lambda shape: torch.empty(shape, dtype=torch.uint8, device=device))
-        self.k_base = mk((n_layers, num_base_pages, num_kv_heads, BASE_TILE_BYTES))
-        self.v_base = mk((n_layers, num_base_pages, num_kv_heads, BASE_TILE_BYTES))
+        self.k_base = mk((n_layers, num_kv_heads, num_base_pages, BASE_TILE_BYTES))
+        self.v_base = mk((n_layers, num_kv_heads, num_base_pages, BASE_TILE_BYTES))
         self.k_res = mk((n_layers, num_res_pages, RES_TILE_BYTES))
         self.v_res = mk((n_layers, num_res_pages, RES_TILE_BYTES))
         self.desc = forkkv_pool_desc(self.k_base.data_ptr(), self.v_base.data_ptr(), self.k_res.data_ptr(),

@@ -35,8 +35,9 @@
  *   - Fixed geometry: head_dim D = 128, residual rank r = 16, page size P = 16.
  *
  * Pool layouts (device memory, 16-byte aligned)
- *   Base pools k_base, v_base: [n_layers][num_base_pages][num_kv_heads] tiles of
- *   FORKKV_BASE_TILE_BYTES.  A tile holds the 16 rows x 128 bf16 of one page and
+ *   Base pools k_base, v_base: [n_layers][num_kv_heads][num_base_pages] tiles of
+ *   FORKKV_BASE_TILE_BYTES (head-major, so a run of consecutive page ids of one
+ *   head is one contiguous range that a single bulk copy can move).  A tile holds the 16 rows x 128 bf16 of one page and
  *   one KV head in the tensor core's 128-byte-swizzled K-major layout: element
  *   (row t, column d) lives at byte
  *       (d / 64) * 2048 + t * 128 + ((((d % 64) / 8) ^ (t % 8)) * 16) + (d % 8) * 2.
@@ -163,7 +164,7 @@ int32_t forkkv_stats_get(const forkkv_alloc* alloc, forkkv_stats* out);
 
 /* ==== pools ================================================================ */
 typedef struct {
-  void* k_base;            /* [n_layers][num_base_pages][num_kv_heads][4096 B] */
+  void* k_base;            /* [n_layers][num_kv_heads][num_base_pages][4096 B] */
   void* v_base;            /* same shape                                       */
   void* k_res;             /* [n_layers][num_res_pages][512 B]                 */
   void* v_res;             /* same shape                                       */
@@ -196,7 +197,7 @@ int32_t forkkv_cow_copy_rows(const forkkv_pool_desc* pools, const forkkv_cow_job
 
 /* ==== rotation table ======================================================
  * cos/sin of p * theta^(-2i/128) for positions p < n_positions and the 64
- * rotate-half frequencies i (fp16), FORKKV_ROPE_ROW_BYTES per position:
+ * rotate-half frequencies i (bf16), FORKKV_ROPE_ROW_BYTES per position:
  * frequencies (2m, 2m+1) form 8-byte group m = [cos 2m, cos 2m+1, sin 2m, sin 2m+1],
  * stored at 32-byte unit (m / 4) ^ (p % 8), slot m % 4, of the position's row.
  * Angles are reduced exactly in 64-bit fixed point before sin/cos. */
