@@ -149,6 +149,67 @@ def cpu_baseline(w, seconds: float = 12.0) -> dict:
             "machine": platform.machine()}
 
 
+def prefill_flops(w) -> int:
+    """Algorithmic flops of one prefill-chunk call: per (query row, visible key) the score, value and
+    residual-value products; per (key, head) the up-projection; per query row the B_v epilogue."""
+    cfg = w.cfg
+    D, r, G, Hkv = cfg.head_dim, cfg.rank, cfg.group, cfg.n_kv_heads
+    total = 0
+    for a in range(cfg.n_agents):
+        L = int(w.seq_lens[a])
+        vis = sum(min(int(p) + 1, L) for p in w.positions[a].tolist())
+        total += Hkv * (G * vis * (2 * D + 2 * D + 2 * r) + L * 2 * r * D + cfg.q_len * G * 2 * r * D)
+    return total
+
+
+def bench_prefill(args, cfg) -> int:
+    """Prefill-chunk throughput (TFLOP/s against the dense bf16 tensor peak), one layer per call."""
+    import torch
+    from disaggregated_kv_attention_gb300 import build as _build
+    from disaggregated_kv_attention_gb300 import forkkv as fk
+    from disaggregated_kv_attention_gb300 import paged
+    from disaggregated_kv_attention_gb300 import workload as wl
+    _build.build()
+    w = wl.generate(cfg)
+    dev = torch.device("cuda", 0)
+    P = paged.place(w, device=dev)
+    rope = fk.rope_table(cfg.rope_theta, P.max_seq_len, device=dev)
+    out = torch.empty_like(P.q)
+    p, keep = paged.params(P, out, rope=rope, prefill=True)
+    fk.forkkv_residual_attn_prefill_chunk(p)
+    torch.cuda.synchronize()
+    if fk.forkkv_get_device_status():
+        raise RuntimeError("device status set by the prefill kernel")
+    for _ in range(args.warmup):
+        fk.forkkv_residual_attn_prefill_chunk(p)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    time.sleep(0.3)
+    for k in range(args.steps):
+        ev[2 * k].record()
+        fk.forkkv_residual_attn_prefill_chunk(p)
+        ev[2 * k + 1].record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(args.steps)]
+    t = statistics.median(ms) / 1000
+    flops = prefill_flops(w)
+    hbm, tf, tf_sus, src = _peaks()
+    achieved = flops / t / 1e12
+    tokens = cfg.n_agents * cfg.q_len
+    print(json.dumps({
+        "metric": "ResidualAttention prefill-chunk TFLOP/s (% of dense bf16 tensor peak), 1 GPU",
+        "value": achieved, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * t, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": {"workload": f"{cfg.name}: {cfg.description}", "layers": 1},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s", "frac": achieved / tf,
+                     "traffic": _traffic("prefill_kernel"), "peak_source": f"{src} bf16_tflops burst (of {src})",
+                     "alg_flops_per_launch": flops},
+        "tokens_per_s": tokens / t, "gpu_launches": args.steps, "clocks": clk}))
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -168,7 +229,7 @@ def main() -> int:
     from disaggregated_kv_attention_gb300 import workload as wl
     cfg = wl.CONFIGS[args.config]
     if cfg.q_len != 1:
-        raise SystemExit("bench.py times decode workloads (q_len = 1)")
+        return bench_prefill(args, cfg)
     layers = args.layers or cfg.model_layers
     w = wl.generate(cfg)
     fig = workload_figures(w, layers)

@@ -1,35 +1,56 @@
-// ResidualAttention over a prefill chunk for sm_103a (first version: mma.sync).
+// ResidualAttention over a prefill chunk for sm_103a, on the fifth-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
 //
 // Same mathematics as decode (ForkKV L2 sections 4 and 7: deferred RoPE on the
 // up-projected residual keys, associativity of the value path, both
-// accumulators rescaled together), laid out FlashAttention-style because here
-// many query rows share every key tile:
-//   grid  (row tile of 128 (token, query-head) rows, agent, KV head)
-//   block 8 consumer warps (16 rows each) + 1 producer warp
-//   per 64-key stage (4 pages), streamed by bulk async copies:
-//     the 8 warps build the stage's full keys once, in shared memory:
-//       K = bf16(Kb + RoPE_j(Kr . B_k[:, hD:(h+1)D]))      (up-projection on mma)
-//     then each warp:  S = Q K^T, causal mask (key j visible iff j <= position
-//     and j < seq_len), online softmax, O += P Vb, O_r += P Vr;
+// accumulators rescaled together), laid out for a dense contraction:
+//   grid   (tile of 128 (token, query-head) rows, agent, KV head)
+//   warps  0      producer: 128-key blocks (8 pages) of K, V, k_res, v_res tiles
+//                 into a 2-stage ring with 1-D bulk async copies (one per run of
+//                 consecutive page ids)
+//          1      allocates 512 TMEM columns; one lane issues every MMA
+//          2..5   RoPE group, one key per thread: U = Kr . B_k^T arrives in TMEM;
+//                 K = bf16(Kb + RoPE_j(U)) is written to shared memory as the
+//                 128-key operand of the next score MMA
+//          6..9   softmax group, one query row per thread: S from TMEM, causal
+//                 mask, online softmax; P (bf16) is written back over S in TMEM
+//   MMAs per block:  U[128x128]   = Kr[128x16] . B_k^T           (smem x smem)
+//                    S[128x128]   = Q[128x128] . K^T             (smem x smem)
+//                    O[128x128]  += P[128x128] . Vb[128x128]      (tmem x smem)
+//                    O_r[128x16] += P . Vr[128x16]                (tmem x smem)
 //   epilogue: out = (O + O_r . B_v[:, hD:(h+1)D]) / l, B_v applied once per row.
+// Every wait is on an mbarrier with a bounded spin; a timeout sets the device
+// status word instead of hanging.
 #include <math.h>
 
 #include "../internal.h"
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace fkv {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = (kWarps + 1) * 32;
-constexpr int kRowsPerCta = kWarps * 16;
-constexpr int kPagesPerStage = 4;  // 64 keys
-constexpr int kStages = 3;
-constexpr int kStageBytes = kPagesPerStage * (2 * kBaseTile + 16 * kRopeRow + 2 * kResTile);  // 53248
-constexpr int kHeaderBytes = 1024;
-constexpr int kKfullBytes = kPagesPerStage * kBaseTile;  // 16 KiB, double buffered
-constexpr int kQBytes = kWarps * kBaseTile;               // 128 rows x 128 bf16, 16 rows per warp
-constexpr int kSmemBytes = kHeaderBytes + kStages * kStageBytes + 2 * kKfullBytes + kQBytes;
+constexpr int kRows = 128;
+constexpr int kBlockPages = 8;
+constexpr int kBlockKeys = kBlockPages * kPage;
+constexpr int kThreads = 10 * 32;
+
+// shared memory (offsets from a 1024-byte aligned base)
+constexpr int kOffQ = 1024;                     // Q, K-major 128B-swizzled [2][128 rows][128 B]
+constexpr int kOffKF = kOffQ + 32768;           // full keys of one block, same layout
+constexpr int kOffStage = kOffKF + 32768;       // 2 stages
+constexpr int kStageBytes = 73728;
+constexpr int kStK = 0, kStV = 32768, kStKR = 65536, kStVR = 69632;  // 8 K tiles, 8 V tiles, 8 k_res, 8 v_res
+constexpr int kOffBk = kOffStage + 2 * kStageBytes;  // B_k^T, K-major 32B-swizzled [128 d][16 r]
+constexpr int kOffBv = kOffBk + 4096;                // B_v slice [16][128] bf16
+constexpr int kSmemBytes = kOffBv + 4096 + 1024;     // + slack for aligning the base
+
+// tensor memory columns
+constexpr uint32_t kTmU = 0, kTmS = 128, kTmO = 256, kTmOr = 384, kTmCols = 512;
+
+// mbarrier indices
+enum { kFull0, kFull1, kEmpty0, kEmpty1, kUFull, kUFree, kKFReady, kKFFree, kSFull, kPFull, kPVDone, kQReady,
+       kBkReady, kNumBars };
 
 struct PrefillArgs {
   const uint8_t* k_base;
@@ -54,342 +75,390 @@ struct PrefillArgs {
   uint32_t* status;
 };
 
-// stage layout: [4][K tile | V tile] [4][16 rotation rows] [4][k_res | v_res]
-constexpr int kRopeAt = kPagesPerStage * 2 * kBaseTile;
-constexpr int kResAt = kRopeAt + kPagesPerStage * 16 * kRopeRow;
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kStages;
-  uint64_t* kready = empty + kStages;  // [2]: the 8 warps finished building a full-key buffer
-  int32_t* s_meta = reinterpret_cast<int32_t*>(smem + 256);  // [0] = key limit of the CTA
-  uint8_t* stages = smem + kHeaderBytes;
-  uint8_t* kfull = stages + kStages * kStageBytes;
-  uint8_t* qtile = kfull + 2 * kKfullBytes;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 256);
+  int32_t* s_meta = reinterpret_cast<int32_t*>(smem + 272);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, q4 = lane & 3;
   const int agent = blockIdx.y, h = blockIdx.z;
   const int G = a.G;
   const int64_t n_rows = (int64_t)a.q_len * G;
-  const int64_t row0 = (int64_t)blockIdx.x * kRowsPerCta;
+  const int64_t row0 = (int64_t)blockIdx.x * kRows;
   const int32_t L = min(a.seq_lens[agent], a.max_seq_len);
+  int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
+  if ((uint32_t)adapter >= (uint32_t)a.n_adapters) adapter = 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
-    }
-    mbar_init(&kready[0], kWarps);
-    mbar_init(&kready[1], kWarps);
+    mbar_init(&bars[kFull0], 1);
+    mbar_init(&bars[kFull1], 1);
+    mbar_init(&bars[kEmpty0], 5);  // 4 RoPE warps + the MMA commit after the value products
+    mbar_init(&bars[kEmpty1], 5);
+    mbar_init(&bars[kUFull], 1);
+    mbar_init(&bars[kUFree], 4);
+    mbar_init(&bars[kKFReady], 4);
+    mbar_init(&bars[kKFFree], 1);
+    mbar_init(&bars[kSFull], 1);
+    mbar_init(&bars[kPFull], 4);
+    mbar_init(&bars[kPVDone], 1);
+    mbar_init(&bars[kQReady], 4);
+    mbar_init(&bars[kBkReady], 4);
     mbar_fence_init();
     // keys this CTA may see: up to the largest query position of its rows (and L)
     const int t_first = (int)(row0 / G);
-    const int t_last = (int)(min(row0 + kRowsPerCta, n_rows) - 1) / G;
+    const int t_last = (int)((min(row0 + kRows, n_rows) - 1) / G);
     int32_t pmax = -1;
     for (int t = t_first; t <= t_last; ++t) pmax = max(pmax, a.positions[(int64_t)agent * a.q_len + t]);
     if (a.seq_lens[agent] < 1 || a.seq_lens[agent] > a.max_seq_len) flag_status(a.status, kDevBadArg);
-    s_meta[0] = min(pmax + 1, L);
+    if ((uint32_t)(a.adapter_ids ? a.adapter_ids[agent] : agent) >= (uint32_t)a.n_adapters)
+      flag_status(a.status, kDevBadArg);
+    s_meta[0] = max(0, min(pmax + 1, L));
   }
+  if (warp == 1) tc::alloc(s_tmem, kTmCols);
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
+  const uint32_t tm = *s_tmem;
   const int32_t key_limit = s_meta[0];
-  const int n_pages = max(0, (key_limit + kPage - 1) / kPage);
-  const int n_stages = (n_pages + kPagesPerStage - 1) / kPagesPerStage;
-  const int64_t head_base = (int64_t)h * a.num_base_pages * kBaseTile;  // this head's tiles, page-major
+  const int n_pages = (key_limit + kPage - 1) / kPage;
+  const int n_blocks = (n_pages + kBlockPages - 1) / kBlockPages;
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sKF = smem + kOffKF;
+  uint8_t* sBk = smem + kOffBk;
+  uint8_t* sBv = smem + kOffBv;
 
-  int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
-  if ((uint32_t)adapter >= (uint32_t)a.n_adapters) {
-    if (threadIdx.x == 0) flag_status(a.status, kDevBadArg);
-    adapter = 0;
-  }
-
-  if (warp == kWarps) {
+  if (warp == 0) {
     // ------------------------------ producer ------------------------------
-    int issued = 0;
-    bool ok = true;
-    for (int s = 0; s < n_stages && ok; ++s) {
-      const int slot = s % kStages;
-      const uint32_t round = s / kStages;
-      if (s >= kStages) ok = mbar_wait(&empty[slot], (round - 1) & 1, a.status);
-      if (!ok) break;
-      const int pbase = s * kPagesPerStage;
-      const int nvp = min(kPagesPerStage, n_pages - pbase);
-      uint8_t* st = stages + slot * kStageBytes;
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], nvp * (2 * kBaseTile + 16 * kRopeRow + 2 * kResTile));
-      __syncwarp();
+    const int64_t head_base = (int64_t)h * a.num_base_pages;
+    for (int b = 0; b < n_blocks; ++b) {
+      const int stage = b & 1;
+      if (b >= 2 && !mbar_wait(&bars[kEmpty0 + stage], ((b >> 1) - 1) & 1, a.status)) break;
+      const int pbase = b * kBlockPages;
+      const int nvp = min(kBlockPages, n_pages - pbase);
+      int32_t id = 0;
       if (lane < nvp) {
-        const int pi = pbase + lane;
-        int32_t bpage = a.bpt[(int64_t)agent * a.pt_stride + pi];
-        int32_t rpage = a.rpt[(int64_t)agent * a.pt_stride + pi];
-        if ((uint32_t)bpage >= (uint32_t)a.num_base_pages || (uint32_t)rpage >= (uint32_t)a.num_res_pages) {
+        id = a.bpt[(int64_t)agent * a.pt_stride + pbase + lane];
+        if ((uint32_t)id >= (uint32_t)a.num_base_pages) {
           flag_status(a.status, kDevBadPage);
-          bpage = 0;
-          rpage = 0;
+          id = 0;
         }
-        int64_t rrow = (int64_t)pi * 16;
-        if (rrow + 16 > a.rope_positions) {
-          flag_status(a.status, kDevBadArg);
-          rrow = 0;
-        }
-        const int64_t off = head_base + (int64_t)bpage * kBaseTile;
-        bulk_g2s(st + lane * 2 * kBaseTile, a.k_base + off, kBaseTile, &full[slot]);
-        bulk_g2s(st + lane * 2 * kBaseTile + kBaseTile, a.v_base + off, kBaseTile, &full[slot]);
-        bulk_g2s(st + kRopeAt + lane * 16 * kRopeRow, a.rope + rrow * kRopeRow, 16 * kRopeRow, &full[slot]);
-        bulk_g2s(st + kResAt + lane * 2 * kResTile, a.k_res + (int64_t)rpage * kResTile, kResTile, &full[slot]);
-        bulk_g2s(st + kResAt + lane * 2 * kResTile + kResTile, a.v_res + (int64_t)rpage * kResTile, kResTile,
-                 &full[slot]);
-      }
-      issued = s + 1;
-    }
-    for (int s = max(0, issued - kStages); s < issued; ++s) mbar_wait(&full[s % kStages], (s / kStages) & 1, a.status);
-    return;  // nothing below involves the producer
-  }
-
-  // -------------------------------- consumers --------------------------------
-  // rows of this warp: r = row0 + 16*warp + {g, g+8}; row r is (token r / G, query head r % G)
-  int32_t rpos[2];
-  bool rvalid[2];
-  const __nv_bfloat16* qrow[2];
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int64_t r = row0 + 16 * warp + g + 8 * rr;
-    rvalid[rr] = r < n_rows;
-    const int64_t t = rvalid[rr] ? r / G : 0;
-    const int gq = rvalid[rr] ? (int)(r % G) : 0;
-    rpos[rr] = rvalid[rr] ? a.positions[(int64_t)agent * a.q_len + t] : -1;
-    qrow[rr] = a.q + (((int64_t)agent * a.q_len + t) * a.hkv * G + (int64_t)h * G + gq) * kHeadDim;
-  }
-  // this warp's 16 query rows, staged once in shared memory (swizzled 16-row tile)
-  const uint32_t sQ = smem_u32(qtile + warp * kBaseTile);
-  for (int c = lane; c < 16 * 16; c += 32) {
-    const int row = c >> 4, ch = c & 15;
-    const int64_t r = row0 + 16 * warp + row;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < n_rows) {
-      const int64_t t = r / G;
-      const int gq = (int)(r % G);
-      v = *reinterpret_cast<const uint4*>(a.q + (((int64_t)agent * a.q_len + t) * a.hkv * G + (int64_t)h * G + gq) *
-                                                    kHeadDim + ch * 8);
-    }
-    *reinterpret_cast<uint4*>(qtile + warp * kBaseTile + base_off(row, ch * 8)) = v;
-  }
-  __syncwarp();
-  // B_k fragments for the up-projection tiles this warp builds: tiles 4*hs..4*hs+3 and +8
-  const int kp = warp & 3, hs = warp >> 2;
-  uint32_t bk[8][2];
-  {
-    const __nv_bfloat16* B = a.B_k + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim;
-    const int64_t ld = (int64_t)a.hkv * kHeadDim;
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      const int t = 4 * hs + (x & 3) + (x >> 2) * 8;
-      const int n = 8 * t + g;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int k = 8 * e + 2 * q4;
-        __nv_bfloat162 v;
-        v.x = B[k * ld + n];
-        v.y = B[(k + 1) * ld + n];
-        bk[x][e] = *reinterpret_cast<uint32_t*>(&v);
-      }
-    }
-  }
-
-  float o[16][4], orr[2][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) orr[i][e] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-
-  const int mi = lane >> 3;
-  const int lrow_a = (lane & 7) + (mi & 1) * 8;  // non-transposed A loads
-  const int krow_b = (lane & 7) + (mi >> 1) * 8; // B loads: keys
-  const int tkey = (lane & 7) + (mi & 1) * 8;    // transposed B loads: keys
-
-  for (int s = 0; s < n_stages; ++s) {
-    const int slot = s % kStages;
-    if (!mbar_wait(&full[slot], (s / kStages) & 1, a.status)) break;
-    const uint8_t* st = stages + slot * kStageBytes;
-    uint8_t* kf = kfull + (s & 1) * kKfullBytes;
-    const int pbase = s * kPagesPerStage;
-    const int nvp = min(kPagesPerStage, n_pages - pbase);
-
-    // 1. full keys of page kp, column tiles {4hs..4hs+3} and their RoPE partners (+8)
-    if (kp < nvp) {
-      const uint32_t sKr = smem_u32(st + kResAt + kp * 2 * kResTile);
-      const uint32_t sKb = smem_u32(st + kp * 2 * kBaseTile);
-      const uint32_t sR = smem_u32(st + kRopeAt + kp * 16 * kRopeRow);
-      const uint32_t sKf = smem_u32(kf + kp * kBaseTile);
-      uint32_t ka0, ka1, ka2, ka3;
-      ldsm_x4(sKr + res_off(lrow_a, (mi >> 1) * 8), ka0, ka1, ka2, ka3);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        float ulo[4] = {0.f, 0.f, 0.f, 0.f}, uhi[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_bf16(ulo, ka0, ka1, ka2, ka3, bk[x][0], bk[x][1]);
-        mma_bf16(uhi, ka0, ka1, ka2, ka3, bk[x + 4][0], bk[x + 4][1]);
-        const int t = 4 * hs + x;
-        const int m = 4 * t + q4;
-        const int d = 8 * t + 2 * q4;
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int kr = g + 8 * rr;
-          const uint2 cs = ld_shared_u64(sR + kr * kRopeRow + rope_off(kr, m));
-          const float2 c = bf2_to_f2(cs.x), sn = bf2_to_f2(cs.y);
-          const float l0 = ulo[2 * rr], l1 = ulo[2 * rr + 1], h0 = uhi[2 * rr], h1 = uhi[2 * rr + 1];
-          const float2 kbl = bf2_to_f2(ld_shared_u32(sKb + base_off(kr, d)));
-          const float2 kbh = bf2_to_f2(ld_shared_u32(sKb + base_off(kr, d + 64)));
-          const uint32_t lo = pack_bf16(kbl.x + (l0 * c.x - h0 * sn.x), kbl.y + (l1 * c.y - h1 * sn.y));
-          const uint32_t hi = pack_bf16(kbh.x + (h0 * c.x + l0 * sn.x), kbh.y + (h1 * c.y + l1 * sn.y));
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(sKf + base_off(kr, d)), "r"(lo));
-          asm volatile("st.shared.u32 [%0], %1;" ::"r"(sKf + base_off(kr, d + 64)), "r"(hi));
+      } else if (lane >= 8 && lane - 8 < nvp) {
+        id = a.rpt[(int64_t)agent * a.pt_stride + pbase + lane - 8];
+        if ((uint32_t)id >= (uint32_t)a.num_res_pages) {
+          flag_status(a.status, kDevBadPage);
+          id = 0;
         }
       }
+      int32_t ids[8];
+      const int src0 = lane < 2 ? 0 : 8;  // lanes 0, 1: base page ids; lanes 2, 3: residual page ids
+#pragma unroll
+      for (int pg = 0; pg < 8; ++pg) ids[pg] = __shfl_sync(0xffffffffu, id, src0 + pg);
+      uint8_t* st = smem + kOffStage + stage * kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kFull0 + stage], nvp * (2 * kBaseTile + 2 * kResTile));
+      __syncwarp();
+      if (lane < 4) {
+        const uint8_t* pool = lane == 0 ? a.k_base + head_base * kBaseTile
+                              : lane == 1 ? a.v_base + head_base * kBaseTile
+                              : lane == 2 ? a.k_res : a.v_res;
+        uint8_t* dst = st + (lane == 0 ? kStK : lane == 1 ? kStV : lane == 2 ? kStKR : kStVR);
+        const uint32_t tile = lane < 2 ? kBaseTile : kResTile;
+        int r0 = 0;
+        int32_t start = ids[0];
+#pragma unroll
+        for (int pg = 1; pg <= 8; ++pg) {
+          if (pg <= nvp) {
+            const bool end = pg == nvp || ids[pg < 8 ? pg : 7] != ids[pg - 1] + 1;
+            if (end) {
+              bulk_g2s(dst + r0 * tile, pool + (int64_t)start * tile, (pg - r0) * tile, &bars[kFull0 + stage]);
+              r0 = pg;
+              start = ids[pg < 8 ? pg : 7];
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t idU = tc::idesc_bf16(128, 128, 0, 0);
+      const uint32_t idS = tc::idesc_bf16(128, 128, 0, 0);
+      const uint32_t idPV = tc::idesc_bf16(128, 128, 0, 1);
+      const uint32_t idPVr = tc::idesc_bf16(128, 16, 0, 1);
+      const uint32_t aQ = smem_u32(sQ), aKF = smem_u32(sKF), aBk = smem_u32(sBk);
+      bool ok = mbar_wait(&bars[kQReady], 0, a.status) && mbar_wait(&bars[kBkReady], 0, a.status);
+      int issued = 0;
+      for (int b = 0; b < n_blocks && ok; ++b) {
+        const int stage = b & 1;
+        const uint32_t st = smem_u32(smem + kOffStage + stage * kStageBytes);
+        const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
+        ok = mbar_wait(&bars[kFull0 + stage], (b >> 1) & 1, a.status);
+        if (ok && b > 0) ok = mbar_wait(&bars[kUFree], (b - 1) & 1, a.status);
+        if (!ok) break;
+        tc::fence_after();
+        tc::mma_ss(tm + kTmU, tc::smem_desc(st + kStKR, 16, 256, tc::kSwizzle32B),
+                   tc::smem_desc(aBk, 16, 256, tc::kSwizzle32B), idU, 0);
+        tc::commit(&bars[kUFull]);
+        ok = mbar_wait(&bars[kKFReady], b & 1, a.status);
+        if (ok && b > 0) ok = mbar_wait(&bars[kPVDone], (b - 1) & 1, a.status);
+        if (!ok) break;
+        tc::fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          tc::mma_ss(tm + kTmS, tc::smem_desc(aQ + off, 16, 1024, tc::kSwizzle128B),
+                     tc::smem_desc(aKF + off, 16, 1024, tc::kSwizzle128B), idS, ks > 0);
+        }
+        tc::commit(&bars[kSFull]);
+        tc::commit(&bars[kKFFree]);
+        ok = mbar_wait(&bars[kPFull], b & 1, a.status);
+        if (!ok) break;
+        tc::fence_after();
+        for (int ks = 0; ks < nvp; ++ks)
+          tc::mma_ts(tm + kTmO, tm + kTmS + 8 * ks,
+                     tc::smem_desc(st + kStV + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B), idPV, (b > 0 || ks > 0));
+        for (int ks = 0; ks < nvp; ++ks)
+          tc::mma_ts(tm + kTmOr, tm + kTmS + 8 * ks,
+                     tc::smem_desc(st + kStVR + ks * kResTile, 4096, 256, tc::kSwizzle32B), idPVr, (b > 0 || ks > 0));
+        tc::commit(&bars[kPVDone]);
+        tc::commit(&bars[kEmpty0 + stage]);
+        issued = b + 1;
+      }
+      // never leave with MMAs in flight
+      if (issued > 0) mbar_wait(&bars[kPVDone], (issued - 1) & 1, a.status);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&kready[s & 1]);
-    if (!mbar_wait(&kready[s & 1], (s >> 1) & 1, a.status)) break;
-
-    // 2. S = Q K^T over the stage's valid pages
-    float sc[8][4];
+  } else if (warp < 6) {
+    // ------------------------------ RoPE group ------------------------------
+    const int row = 32 * (warp & 3) + lane;  // key row of the block == TMEM lane
+    const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
+    {  // B_k^T: row d, 16 ranks
+      const __nv_bfloat16* B = a.B_k + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim + row;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+      for (int k = 0; k < kRank; ++k)
+        *reinterpret_cast<__nv_bfloat16*>(sBk + tc::sw32_off(row, k)) = B[(int64_t)k * a.hkv * kHeadDim];
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kBkReady]);
+    }
+    const int p = row >> 4, t = row & 15;
+    bool ok = true;
+    for (int b = 0; b < n_blocks && ok; ++b) {
+      const int stage = b & 1;
+      uint8_t* st = smem + kOffStage + stage * kStageBytes;
+      const int j = b * kBlockKeys + row;
+      // this key's rotation row: logical 32-byte unit u sits at unit u ^ (j % 8)
+      uint4 rp[8][2];
+      {
+        const int jr = j < a.rope_positions ? j : 0;
+        const uint4* rrow = reinterpret_cast<const uint4*>(a.rope + (int64_t)jr * kRopeRow);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sc[nt][e] = 0.f;
-#pragma unroll
-    for (int pg = 0; pg < kPagesPerStage; ++pg) {
-      if (pg < nvp) {
-        const uint32_t sKf = smem_u32(kf + pg * kBaseTile);
-#pragma unroll
-        for (int s8 = 0; s8 < 8; ++s8) {
-          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-          ldsm_x4(sQ + base_off(lrow_a, 16 * s8 + (mi >> 1) * 8), a0, a1, a2, a3);
-          ldsm_x4(sKf + base_off(krow_b, 16 * s8 + (mi & 1) * 8), b0, b1, b2, b3);
-          mma_bf16(sc[2 * pg], a0, a1, a2, a3, b0, b1);
-          mma_bf16(sc[2 * pg + 1], a0, a1, a2, a3, b2, b3);
+        for (int u = 0; u < 8; ++u) {
+          rp[u][0] = rrow[(u ^ (j & 7)) * 2];
+          rp[u][1] = rrow[(u ^ (j & 7)) * 2 + 1];
         }
       }
-    }
-    // 3. mask, online softmax (rows g and g+8; four lanes share a row)
-    const int kbase = pbase * kPage;
-    float mx[2] = {-INFINITY, -INFINITY};
+      ok = mbar_wait(&bars[kFull0 + stage], (b >> 1) & 1, a.status) && mbar_wait(&bars[kUFull], b & 1, a.status);
+      if (ok && b > 0) ok = mbar_wait(&bars[kKFFree], (b - 1) & 1, a.status);
+      if (!ok) break;
+      tc::fence_after();
+      const uint8_t* kt = st + kStK + p * kBaseTile;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+      for (int c = 0; c < 64; c += 16) {
+        uint32_t ulo[16], uhi[16];
+        tc::ld16(tl + kTmU + c, ulo);
+        tc::ld16(tl + kTmU + 64 + c, uhi);
+        uint4 kl[2], kh[2];
+        kl[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c));
+        kl[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 8));
+        kh[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 64));
+        kh[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 72));
+        tc::wait_ld();
+        const uint32_t* klw = reinterpret_cast<const uint32_t*>(kl);
+        const uint32_t* khw = reinterpret_cast<const uint32_t*>(kh);
+        uint32_t olo[8], ohi[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int rr = e >> 1;
-        const int j = kbase + 8 * nt + 2 * q4 + (e & 1);
-        const bool vis = (nt >> 1) < nvp && j < L && j <= rpos[rr];
-        sc[nt][e] = vis ? sc[nt][e] * a.scale_log2 : -INFINITY;
-        mx[rr] = fmaxf(mx[rr], sc[nt][e]);
-      }
-    }
-    float alpha[2];
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-      const float mn = fmaxf(mrow[rr], mx[rr]);
-      const float mu = mn == -INFINITY ? 0.f : mn;
-      alpha[rr] = exp2f(mrow[rr] - mu);
-      mrow[rr] = mn;
-      mx[rr] = mu;  // reuse as the subtrahend
-    }
-    float rs[2] = {0.f, 0.f};
-    uint32_t pa[4][4];  // P as the A operand, k-step = page
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const float p0 = exp2f(sc[nt][0] - mx[0]), p1 = exp2f(sc[nt][1] - mx[0]);
-      const float p2 = exp2f(sc[nt][2] - mx[1]), p3 = exp2f(sc[nt][3] - mx[1]);
-      rs[0] += p0 + p1;
-      rs[1] += p2 + p3;
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(p0, p1);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(p2, p3);
-    }
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) lrow[rr] = lrow[rr] * alpha[rr] + rs[rr];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= alpha[0];
-      o[i][1] *= alpha[0];
-      o[i][2] *= alpha[1];
-      o[i][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      orr[i][0] *= alpha[0];
-      orr[i][1] *= alpha[0];
-      orr[i][2] *= alpha[1];
-      orr[i][3] *= alpha[1];
-    }
-    // 4. O += P Vb ; O_r += P Vr
-#pragma unroll
-    for (int pg = 0; pg < kPagesPerStage; ++pg) {
-      if (pg < nvp) {
-        const uint32_t sV = smem_u32(st + pg * 2 * kBaseTile + kBaseTile);
-        const uint32_t sVr = smem_u32(st + kResAt + pg * 2 * kResTile + kResTile);
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(sV + base_off(tkey, 16 * np + (mi >> 1) * 8), b0, b1, b2, b3);
-          mma_bf16(o[2 * np], pa[pg][0], pa[pg][1], pa[pg][2], pa[pg][3], b0, b1);
-          mma_bf16(o[2 * np + 1], pa[pg][0], pa[pg][1], pa[pg][2], pa[pg][3], b2, b3);
+        for (int i2 = 0; i2 < 8; ++i2) {  // elements d = c + 2*i2, c + 2*i2 + 1 (and + 64)
+          const int m = (c >> 1) + i2;     // frequency group
+          const uint4 w = rp[m >> 2][(m & 3) >> 1];
+          const uint32_t cw = (m & 1) ? w.z : w.x, sw = (m & 1) ? w.w : w.y;
+          const float lo0 = __uint_as_float(ulo[2 * i2]), lo1 = __uint_as_float(ulo[2 * i2 + 1]);
+          const float hi0 = __uint_as_float(uhi[2 * i2]), hi1 = __uint_as_float(uhi[2 * i2 + 1]);
+          const float c0 = bf_lo(cw), c1 = bf_hi(cw), s0 = bf_lo(sw), s1 = bf_hi(sw);
+          const float kl0 = bf_lo(klw[i2]) + (lo0 * c0 - hi0 * s0);
+          const float kl1 = bf_hi(klw[i2]) + (lo1 * c1 - hi1 * s1);
+          const float kh0 = bf_lo(khw[i2]) + (hi0 * c0 + lo0 * s0);
+          const float kh1 = bf_hi(khw[i2]) + (hi1 * c1 + lo1 * s1);
+          olo[i2] = pack_bf16(kl0, kl1);
+          ohi[i2] = pack_bf16(kh0, kh1);
         }
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sVr + res_off(tkey, (mi >> 1) * 8), b0, b1, b2, b3);
-        mma_bf16(orr[0], pa[pg][0], pa[pg][1], pa[pg][2], pa[pg][3], b0, b1);
-        mma_bf16(orr[1], pa[pg][0], pa[pg][1], pa[pg][2], pa[pg][3], b2, b3);
+        *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c)) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+        *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 8)) = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+        *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 64)) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+        *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 72)) = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kUFree]);
+      // keys past the sequence: zero their value rows so that 0 * (never-written data) stays 0
+      const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
+      if (j >= L && p < nvp) {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch)
+          *reinterpret_cast<uint4*>(st + kStV + p * kBaseTile + base_off(t, ch * 8)) = z;
+        *reinterpret_cast<uint4*>(st + kStVR + p * kResTile + res_off(t, 0)) = z;
+        *reinterpret_cast<uint4*>(st + kStVR + p * kResTile + res_off(t, 8)) = z;
+      }
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[kKFReady]);
+        mbar_arrive(&bars[kEmpty0 + stage]);
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
-  }
-
-  // epilogue: row sums over the quad, then (O + O_r B_v) / l
+  } else {
+    // ------------------------------ softmax group ------------------------------
+    const int qr = 32 * (warp & 3) + lane;  // query row of the tile == TMEM lane
+    const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int64_t f = row0 + qr;
+    const bool valid = f < n_rows;
+    const int64_t tq = valid ? f / G : 0;
+    const int gq = valid ? (int)(f % G) : 0;
+    const int32_t pos = valid ? a.positions[(int64_t)agent * a.q_len + tq] : -1;
+    const int64_t orow = (((int64_t)agent * a.q_len + tq) * a.hkv * G + (int64_t)h * G + gq) * kHeadDim;
+    {  // Q row into the K-major swizzled tile; B_v slice for the epilogue
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + orow);
 #pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    lrow[rr] += __shfl_xor_sync(0xffffffffu, lrow[rr], 1);
-    lrow[rr] += __shfl_xor_sync(0xffffffffu, lrow[rr], 2);
-  }
-  // normalise, then add (O_r / l) . B_v[:, hD:(h+1)D] with one fp16 mma per 8 output columns:
-  // the O_r fragment (rows x rank) is already the A operand of m16n8k16 (k = rank).
-  float inv[2];
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) inv[rr] = lrow[rr] > 0.f ? 1.f / lrow[rr] : 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    o[i][0] *= inv[0];
-    o[i][1] *= inv[0];
-    o[i][2] *= inv[1];
-    o[i][3] *= inv[1];
-  }
-  const uint32_t ra0 = pack_f16(orr[0][0] * inv[0], orr[0][1] * inv[0]);
-  const uint32_t ra1 = pack_f16(orr[0][2] * inv[1], orr[0][3] * inv[1]);
-  const uint32_t ra2 = pack_f16(orr[1][0] * inv[0], orr[1][1] * inv[0]);
-  const uint32_t ra3 = pack_f16(orr[1][2] * inv[1], orr[1][3] * inv[1]);
-  const __nv_bfloat16* Bv = a.B_v + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim;
-  const int64_t ld = (int64_t)a.hkv * kHeadDim;
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int n = 8 * nt + g;
-    const float b00 = __bfloat162float(Bv[(2 * q4) * ld + n]), b01 = __bfloat162float(Bv[(2 * q4 + 1) * ld + n]);
-    const float b10 = __bfloat162float(Bv[(2 * q4 + 8) * ld + n]), b11 = __bfloat162float(Bv[(2 * q4 + 9) * ld + n]);
-    mma_f16(o[nt], ra0, ra1, ra2, ra3, pack_f16(b00, b01), pack_f16(b10, b11));
-  }
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int d = 8 * nt + 2 * q4;
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      if (!rvalid[rr]) continue;
-      __nv_bfloat16* dst = a.out + (qrow[rr] - a.q) + d;
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(o[nt][2 * rr], o[nt][2 * rr + 1]);
+      for (int ch = 0; ch < 16; ++ch) {
+        const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sQ + tc::sw128_off(128, qr, ch * 8)) = v;
+      }
+      const __nv_bfloat16* Bv = a.B_v + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim;
+      for (int i = qr; i < kRank * kHeadDim / 8; i += 128) {
+        const int k = i / 16, ch = i % 16;
+        *reinterpret_cast<uint4*>(sBv + (k * kHeadDim + ch * 8) * 2) =
+            *reinterpret_cast<const uint4*>(Bv + (int64_t)k * a.hkv * kHeadDim + ch * 8);
+      }
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kQReady]);
     }
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int b = 0; b < n_blocks && ok; ++b) {
+      ok = mbar_wait(&bars[kSFull], b & 1, a.status);
+      if (!ok) break;
+      tc::fence_after();
+      const int kbase = b * kBlockKeys;
+      float bm = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t v0[16], v1[16];
+        tc::ld16(tl + kTmS + c, v0);
+        tc::ld16(tl + kTmS + c + 16, v1);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int j = kbase + c + i;
+          const float s = __uint_as_float(i < 16 ? v0[i] : v1[i - 16]) * a.scale_log2;
+          if (j < L && j <= pos) bm = fmaxf(bm, s);
+        }
+      }
+      const bool need = bm > m + 8.f;  // lazy rescale: only when the max grows by 2^8
+      if (__any_sync(0xffffffffu, need)) {
+        const float mn = need ? bm : m;
+        const float alpha = (need && m != -INFINITY) ? exp2f(m - mn) : 1.f;
+        if (b > 0) {
+          ok = mbar_wait(&bars[kPVDone], (b - 1) & 1, a.status);  // the accumulators are stable
+          tc::fence_after();
+#pragma unroll
+          for (int c = 0; c < 128 + 16; c += 16) {
+            const uint32_t col = c < 128 ? kTmO + c : kTmOr;
+            uint32_t v[16];
+            tc::ld16(tl + col, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tc::st16(tl + col, v);
+          }
+          tc::wait_st();
+        }
+        l *= alpha;
+        m = mn;
+      }
+      const float mu = m == -INFINITY ? 0.f : m;
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t v0[16], v1[16], pw[16];
+        tc::ld16(tl + kTmS + c, v0);
+        tc::ld16(tl + kTmS + c + 16, v1);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pr[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int ii = 2 * i + e;
+            const int j = kbase + c + ii;
+            const float s = __uint_as_float(ii < 16 ? v0[ii] : v1[ii - 16]) * a.scale_log2;
+            pr[e] = (j < L && j <= pos) ? exp2f(s - mu) : 0.f;
+            l += pr[e];
+          }
+          pw[i] = pack_bf16(pr[0], pr[1]);
+        }
+        tc::st16(tl + kTmS + (c >> 1), pw);  // P over the columns of S already read
+      }
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kPFull]);
+    }
+    // epilogue
+    if (ok && n_blocks > 0) ok = mbar_wait(&bars[kPVDone], (n_blocks - 1) & 1, a.status);
+    if (ok) ok = mbar_wait(&bars[kQReady], 0, a.status);  // every thread's part of the B_v slice is in place
+    tc::fence_after();
+    uint32_t orr[16];
+    tc::ld16(tl + kTmOr, orr);
+    tc::wait_ld();
+    const bool have = ok && n_blocks > 0 && l > 0.f;
+    const float inv = have ? 1.f / l : 0.f;
+    const __nv_bfloat16* sbv = reinterpret_cast<const __nv_bfloat16*>(sBv);
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 16) {
+      uint32_t v[16];
+      tc::ld16(tl + kTmO + c, v);
+      tc::wait_ld();
+      uint32_t ow[8];
+#pragma unroll
+      for (int i2 = 0; i2 < 8; ++i2) {
+        float o[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int d = c + 2 * i2 + e;
+          float x = __uint_as_float(v[2 * i2 + e]);
+#pragma unroll
+          for (int k = 0; k < kRank; ++k) x += __uint_as_float(orr[k]) * __bfloat162float(sbv[k * kHeadDim + d]);
+          o[e] = have ? x * inv : 0.f;
+        }
+        ow[i2] = pack_bf16(o[0], o[1]);
+      }
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + orow + c);
+        dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tm, kTmCols);
   }
 }
 
@@ -438,7 +507,7 @@ cudaError_t launch_prefill(const forkkv_attn_params& p, const void* rope_table, 
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   const int64_t rows = (int64_t)p.q_len * G;
-  dim3 grid((unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta), p.n_agents, p.num_kv_heads);
+  dim3 grid((unsigned)((rows + kRows - 1) / kRows), p.n_agents, p.num_kv_heads);
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
   return cudaGetLastError();
 }
