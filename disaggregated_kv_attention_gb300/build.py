@@ -62,6 +62,7 @@ def _stale(objs_srcs) -> bool:
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, s) for s in SOURCES]
     deps += [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "kernels", "common.cuh"),
+             os.path.join(CSRC, "kernels", "tcgen05.cuh"),
              os.path.join(ROOT, "include", "forkkv.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 

@@ -1,44 +1,85 @@
-// ResidualAttention decode for sm_103a.
+// ResidualAttention decode for sm_103a on the fifth-generation tensor cores.
 //
 // Restates ForkKV L2 sections 4 and 7 (deferred RoPE, associativity of the
 // value path, dual-accumulator online softmax) as a split-KV decode:
 //
-//   split kernel  one CTA per (work item, KV head).  A work item is a run of
-//                 logical pages shared by 1, 2, 4 or 8 agents (a trunk of the
-//                 fork tree, or one agent's private pages).  A producer warp
-//                 streams, per stage, the base K/V tiles of the item's pages
-//                 (read ONCE for all agents of the item), every agent's residual
-//                 k/v tiles and the rotation-table rows into shared memory with
-//                 1-D bulk async copies completing on mbarriers.  Each of the 8
-//                 consumer warps owns (agent, page lane) and, per 16-key page:
-//                   U      = Kr . B_k[:, hD:(h+1)D]        (mma, 16 keys x 128)
-//                   K_lora = RoPE_j(U)                     (fp16x2, registers)
-//                   S^T    = Kb . q^T + K_lora . q^T       (mma, keys x heads)
-//                   online softmax over keys; acc and acc_r both rescaled
-//                   acc^T += Vb^T . P^T ; acc_r^T += Vr^T . P^T   (mma)
-//                 Warps of the same agent are merged in shared memory and one
-//                 partial (m, l, acc, acc_r) per (item, agent, head) is written.
-//   combine       one CTA per (agent, KV head): log-sum-exp merge of the
-//                 partials, then out = (acc + acc_r . B_v[:, hD:(h+1)D]) / l,
+//   split kernel  one CTA per (work unit, KV head).  A work unit is a run of
+//                 logical pages shared by up to 4 agents (a trunk of the fork
+//                 tree) or one agent's own pages, walked in 128-key blocks.
+//     warp 0      producer: each block's base K and V tiles (read ONCE for the
+//                 whole agent group) into two K and two V buffers, released
+//                 separately, each agent's residual k/v tiles into a 4-slot ring;
+//                 1-D bulk async copies, one per run of consecutive page ids,
+//                 completing on mbarriers
+//     warp 1      allocates tensor memory; one lane issues, per (block, agent):
+//                   U    = Kr . B_k^T            [128 keys x 128]  smem x smem
+//                   S    = K . Q^T               [128 keys x 16]   K from TMEM
+//                 whichever is ready first (U and K are double-buffered in TMEM)
+//     warps 2..9  RoPE group, one key per thread and half of the columns per
+//                 warp: K = Kb + RoPE_j(U) in fp32, written to tensor memory as
+//                 the A operand of the score product
+//     warps 10..13 softmax group, one key per thread: scores, length mask, block
+//                 maxima across the group, lazy rescale of O (only when the
+//                 running maximum grows by 2^8), P^T to shared memory, l
+//     warp 14     one lane issues, per block and for all its agents at once,
+//                   O^T += Vb^T . P^T  and  R += Vr^T . P^T (rank-16 value path)
+//                 At the end of the unit each (agent, KV head) writes one partial
+//                 (m, l, acc, acc_r) for the combine kernel.
+//   combine       one CTA per (agent, KV head, query head): log-sum-exp merge of
+//                 the partials, then out = (acc + acc_r . B_v[:, hD:(h+1)D]) / l,
 //                 B_v applied once per query head.
-//
-// mma.sync m16n8k16 with the keys on M and the (padded) query heads on N keeps
-// the padding at 8 columns; movmatrix turns the probability fragment into the
-// operand of the value products without a trip through shared memory.
+// Every wait is on an mbarrier with a bounded spin; a timeout sets the device
+// status word instead of hanging.
 #include <math.h>
 
 #include "../internal.h"
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace fkv {
 namespace {
 
-constexpr int kWarps = 8;                    // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;  // + one producer warp
-constexpr int kMaxStages = 8;
-constexpr int kSmemBytes = 227 * 1024;  // the sm_100 family's per-block maximum
-constexpr int kHeaderBytes = 4096;           // mbarriers, agent ids, page-id cache
+constexpr int kMaxGroup = 4;                 // agents per work unit
+constexpr int kBlockPages = 8;               // 128 keys per block
+constexpr int kRopeWarps = 8;                // two per TMEM lane quadrant
+constexpr int kSoftWarp0 = 2 + kRopeWarps;   // first of the four softmax warps
+constexpr int kValueWarp = kSoftWarp0 + 4;   // issues the value products of each block
+constexpr int kThreads = (kValueWarp + 1) * 32;
 constexpr int kPartCols = kHeadDim + kRank;  // 144 floats per (slot, head, query head)
+constexpr int kResSlots = 4;
+
+// shared memory (offsets from a 1024-byte aligned base)
+constexpr int kBlockTiles = kBlockPages * kBaseTile;         // 32 KB: one block of K (or V) tiles
+constexpr int kOffK = 2048;                                  // 2 x K block (after barriers and state)
+constexpr int kOffV = kOffK + 2 * kBlockTiles;               // 2 x V block
+constexpr int kResSlotBytes = kBlockPages * kResTile;        // 4 KB: one step's residual tiles
+constexpr int kVrSlotBytes = 2 * kResSlotBytes;              // v_res tiles, then tiles of ones
+constexpr int kOffVr = kOffV + 2 * kBlockTiles;              // 4 x [v_res | ones]
+constexpr int kOffKr = kOffVr + kResSlots * kVrSlotBytes;    // 4 x k_res slot
+constexpr int kOffQ = kOffKr + kResSlots * kResSlotBytes;    // 4 agents x 2 halves x Q^T [8 rows][128 B]
+constexpr int kOffQZero = kOffQ + kMaxGroup * 2048;          // 1 KB of zeros: query-head rows 8..15
+constexpr int kOffBk = kOffQZero + 1024;                     // 4 x B_k^T [128 d][32 B]
+constexpr int kOffP = kOffBk + kMaxGroup * 4096;             // 2 x P^T [2 atoms (agents 0-1, 2-3)][128 keys][32 B]
+constexpr int kSmemBytes = kOffP + 2 * 8192 + 1024;          // + slack for aligning the base
+// The residual-value product reads 8 stacked 16-row atoms at a 4 KB stride from the slot
+// of a block's first agent: (v_res, ones) of each agent in turn.  Atoms past the agents of
+// the block (rows of the product that are never read) must still lie inside the allocation.
+static_assert(kOffVr + (kResSlots - 1) * kVrSlotBytes + 8 * kResSlotBytes <= kOffBk,
+              "value-product atoms leave the allocation");
+
+// tensor memory columns: U (fp32) and K (bf16 pairs) double-buffered, S double-buffered,
+// O^T [128 d x 8 agents' query heads] and the residual-value product [128 x 32]
+constexpr uint32_t kTmU = 0, kTmKF = 256, kTmS = 384, kTmO = 416, kTmR = 448, kTmCols = 512;
+
+enum {
+  kKFull0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1,
+  kResFull0, kResFull1, kResFull2, kResFull3, kResEmpty0, kResEmpty1, kResEmpty2, kResEmpty3,
+  kUFull0, kUFull1, kUFree0, kUFree1, kKFFull0, kKFFull1, kKFFree0, kKFFree1, kSFull0, kSFull1, kSFree0, kSFree1,
+  kPFull0, kPFull1, kPFree0, kPFree1, kRed0, kRed1, kODone0, kODone1, kQReady, kBkReady,
+  kMmaDone, kValDone, kNumBars
+};
+static_assert(kNumBars * 8 <= 384, "barriers overlap the state that follows them");
+static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have");
 
 struct DecodeArgs {
   const uint8_t* k_base;
@@ -67,16 +108,9 @@ struct DecodeArgs {
 };
 
 struct Item {
-  int32_t p0, p1, na, wpp, slot_base;
-  int32_t agents[8];
+  int32_t p0, p1, na, slot_base;
+  int32_t agents[kMaxGroup];
 };
-
-// Pages per pipeline stage for a group of na agents (8 consumer warps = na x warps-per-agent).
-__device__ __forceinline__ int32_t stage_pages(int32_t na) { return na == 8 ? 2 : na == 1 ? 8 : 4; }
-// Stage layout: [SP][K tile] [SP][V tile] [SP][16 rotation rows] [na][SP][k_res] [na][SP][v_res]
-__device__ __forceinline__ int32_t stage_bytes(int32_t sp, int32_t na) {
-  return sp * (2 * kBaseTile + 16 * kRopeRow) + 2 * na * sp * kResTile;
-}
 
 __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
   Item it;
@@ -85,18 +119,17 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
     it.p0 = p[0];
     it.p1 = p[1];
     it.na = p[2];
-    it.wpp = p[3];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) it.agents[i] = p[4 + i];
+    for (int i = 0; i < kMaxGroup; ++i) it.agents[i] = p[4 + i];
     it.slot_base = p[12];
-    if (it.na != 1 && it.na != 2 && it.na != 4 && it.na != 8) {
+    if (it.na != 1 && it.na != 2 && it.na != 4) {  // the value products stack the slots of 1, 2 or 4 agents
       flag_status(a.status, kDevBadArg);
       it.na = 1;
+      it.p1 = it.p0;
     }
-    it.wpp = 8 / it.na;  // warps per agent
     if (it.slot_base < 0 || it.slot_base + it.na > a.n_slots) {
       flag_status(a.status, kDevBadArg);
-      it.p1 = it.p0;  // empty: writes nothing useful, reads nothing
+      it.p1 = it.p0;  // empty: reads nothing, writes nothing
       it.slot_base = -1;
     }
   } else {
@@ -106,13 +139,12 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
     it.p0 = c * a.chunk_pages;
     it.p1 = min(it.p0 + a.chunk_pages, npg);
     it.na = 1;
-    it.wpp = 8;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) it.agents[i] = agent;
+    for (int i = 0; i < kMaxGroup; ++i) it.agents[i] = agent;
     it.slot_base = blockIdx.x;
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < kMaxGroup; ++i)
     if ((uint32_t)it.agents[i] >= (uint32_t)a.n_agents) {
       flag_status(a.status, kDevBadArg);
       it.agents[i] = 0;
@@ -126,371 +158,593 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
   return it;
 }
 
-__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
-  __nv_bfloat162 r = __hadd2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
+// mbarrier test by every lane, lane 0's answer for all (warp-uniform control flow).
+__device__ __forceinline__ bool warp_test(uint64_t* bar, uint32_t parity) {
+  const uint32_t r = mbar_test(bar, parity) ? 1u : 0u;
+  return __shfl_sync(0xffffffffu, r, 0) != 0;
 }
 
-// Rotate the pair (lo, hi) = (U_d, U_{d+64}) of two adjacent columns by (cos, sin), bf16x2.
-__device__ __forceinline__ void rotate_bf16x2(uint32_t& lo, uint32_t& hi, uint32_t c, uint32_t s) {
-  const __nv_bfloat162 L = *reinterpret_cast<__nv_bfloat162*>(&lo), H = *reinterpret_cast<__nv_bfloat162*>(&hi);
-  const __nv_bfloat162 C = *reinterpret_cast<__nv_bfloat162*>(&c), S = *reinterpret_cast<__nv_bfloat162*>(&s);
-  const __nv_bfloat162 l2 = __hfma2(L, C, __hneg2(__hmul2(H, S)));
-  const __nv_bfloat162 h2 = __hfma2(L, S, __hmul2(H, C));
-  lo = *reinterpret_cast<const uint32_t*>(&l2);
-  hi = *reinterpret_cast<const uint32_t*>(&h2);
+// Copy the nvp (<= 8) page tiles of a block, whose ids sit in lanes 0..nvp-1 of `id`,
+// into consecutive tiles at dst: one bulk copy per run of consecutive ids, issued by
+// lane 0 after raising the byte count `bar` expects (the caller arrives once, after
+// every copy of the phase).  Only the first `rows` rows of the last page are copied
+// when rows < 16; the rest of that tile is zeroed first, since rows past every
+// sequence may never have been written and a zero probability must not meet a NaN.
+// A base tile keeps its rows in two 2048-byte halves (128 bytes a row), a residual
+// tile in one (32 bytes a row).
+__device__ __noinline__ void copy_block(const uint8_t* pool, uint8_t* dst, bool base, int32_t id, int nvp, int rows,
+                                        uint64_t* bar, int lane) {
+  const uint32_t tile = base ? kBaseTile : kResTile, rb = base ? 128u : 32u;
+  const int full = rows < kPage ? nvp - 1 : nvp;  // pages copied whole
+  int32_t ids[kBlockPages];
+#pragma unroll
+  for (int pg = 0; pg < kBlockPages; ++pg) ids[pg] = __shfl_sync(0xffffffffu, id, pg);
+  uint32_t bytes = full * tile;
+  if (full < nvp) {
+    uint8_t* t = dst + full * tile;
+    const uint32_t keep = rows * rb, half = base ? 2048u : tile;  // bytes kept per half
+    for (uint32_t o = keep + 16 * lane; o < half; o += 16 * 32) {
+      *reinterpret_cast<uint4*>(t + o) = make_uint4(0u, 0u, 0u, 0u);
+      if (base) *reinterpret_cast<uint4*>(t + 2048 + o) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    bytes += base ? 2 * keep : keep;
+    tc::fence_proxy_async();
+  }
+  __syncwarp();
+  if (lane == 0) {
+    mbar_expect_tx(bar, bytes);
+    int r0 = 0;
+    int32_t start = ids[0];
+#pragma unroll
+    for (int pg = 1; pg <= kBlockPages; ++pg) {
+      if (pg <= full) {
+        const int32_t next = ids[pg < kBlockPages ? pg : kBlockPages - 1];
+        if (pg == full || next != ids[pg - 1] + 1) {
+          bulk_g2s(dst + r0 * tile, pool + (int64_t)start * tile, (pg - r0) * tile, bar);
+          r0 = pg;
+          start = next;
+        }
+      }
+    }
+    if (full < nvp && rows > 0) {
+      const uint8_t* src = pool + (int64_t)ids[full < kBlockPages ? full : 0] * tile;
+      bulk_g2s(dst + full * tile, src, rows * rb, bar);
+      if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
+    }
+  }
+}
+
+// Reduce eight values per lane over the 32 lanes of a warp (max or sum), transposed so
+// that nine shuffles suffice: lane l ends with the reduction of value l / 4.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce8(const float* v_in, int lane) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = v_in[i];
+  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // lanes with bit 4 set keep values 4..7
+    const bool hi = lane & 16;
+    const float keep = hi ? v[i + 4] : v[i], give = hi ? v[i] : v[i + 4];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, give, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // bit 3: values 2..3 of the four left
+    const bool hi = lane & 8;
+    const float keep = hi ? v[i + 2] : v[i], give = hi ? v[i] : v[i + 2];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, give, 8));
+  }
+  {
+    const bool hi = lane & 4;
+    const float keep = hi ? v[1] : v[0], give = hi ? v[0] : v[1];
+    v[0] = op(keep, __shfl_xor_sync(0xffffffffu, give, 4));
+  }
+  v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 2));
+  v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+  return v[0];
+}
+
+__device__ __forceinline__ float select8(const float* v, int i) {
+  float r = v[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k)
+    if (i == k) r = v[k];
+  return r;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ DecodeArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + kMaxStages;
-  int32_t* s_agents = reinterpret_cast<int32_t*>(smem + 256);  // [8]
-  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + 512);     // [16 stages][32] page ids (producer only)
-  uint8_t* stages = smem + kHeaderBytes;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 384);
+  int32_t* s_L = reinterpret_cast<int32_t*>(smem + 400);    // [4] sequence length of each agent
+  int32_t* s_pos = reinterpret_cast<int32_t*>(smem + 416);  // [4] query position of each agent
+  float* s_red = reinterpret_cast<float*>(smem + 512);      // [2][4 warps][8] block maxima
+  float* s_mref = reinterpret_cast<float*>(smem + 768);     // [4 warps][4 agents][8] reference maxima
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   const Item it = load_item(a);
-  const int na = it.na, wpp = it.wpp;
-  const int SP = stage_pages(na);
-  const int32_t sbytes = stage_bytes(SP, na);
-  const int NS = min(kMaxStages, (kSmemBytes - kHeaderBytes) / sbytes);
+  const int na = it.na;
   const int n_pages = it.p1 - it.p0;
-  const int n_stages = (n_pages + SP - 1) / SP;
-  const int32_t v_at = SP * kBaseTile, rope_at = 2 * SP * kBaseTile, kr_at = rope_at + SP * 16 * kRopeRow;
-  const int32_t vr_at = kr_at + na * SP * kResTile;
+  const int nb = (n_pages + kBlockPages - 1) / kBlockPages;
+  const int N = nb * na;  // (block, agent) steps
+  const int G = a.G;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kMaxStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t count = 1;  // a single arrival: the producer's expect_tx or one MMA commit
+      if (i == kKEmpty0 || i == kKEmpty1 || i == kUFree0 || i == kUFree1 || i == kKFFull0 || i == kKFFull1 ||
+          i == kBkReady)
+        count = kRopeWarps;  // one arrival per RoPE warp
+      if (i == kSFree0 || i == kSFree1 || i == kPFull0 || i == kPFull1 || i == kRed0 || i == kRed1 ||
+          i == kQReady)
+        count = 4;  // one arrival per softmax warp
+      if (i >= kResEmpty0 && i <= kResEmpty3) count = 2;  // the U commit + the value-product commit
+      mbar_init(&bars[i], count);
     }
     mbar_fence_init();
+#pragma unroll
+    for (int x = 0; x < kMaxGroup; ++x) {
+      const int32_t agent = it.agents[x];
+      const int32_t L = a.seq_lens[agent], pos = a.positions[agent];
+      s_L[x] = x < na ? min(L, a.max_seq_len) : 0;
+      s_pos[x] = pos;
+      if (x < na && h == 0 && (L < 1 || L > a.max_seq_len || pos < 0 || pos >= L)) flag_status(a.status, kDevBadArg);
+    }
   }
-  if (threadIdx.x < 8) s_agents[threadIdx.x] = it.agents[threadIdx.x];
+  if (threadIdx.x < 4 * kMaxGroup * 8) s_mref[threadIdx.x] = -INFINITY;
+  for (int i = threadIdx.x; i < kResSlots * kResSlotBytes / 16; i += kThreads) {  // the constant ones tiles
+    const int slot = i / (kResSlotBytes / 16), o = i % (kResSlotBytes / 16);
+    *reinterpret_cast<uint4*>(smem + kOffVr + slot * kVrSlotBytes + kResSlotBytes + 16 * o) =
+        make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  }
+  tc::fence_proxy_async();
+  if (warp == 1) tc::alloc(s_tmem, kTmCols);
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
+  const uint32_t tm = *s_tmem;
 
-  const int64_t head_base = (int64_t)h * a.num_base_pages;  // first tile of this head (page-major)
-  const int g = lane >> 2, q4 = lane & 3;
-
-  // per-warp partial (consumers): acc^T [d][query head], acc_r^T [k][query head], m, l
-  float acc[8][4], accr[4];
-#pragma unroll
-  for (int mb = 0; mb < 8; ++mb)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[mb][e] = 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) accr[e] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  if (warp == kWarps) {
+  if (warp == 0) {
     // ------------------------------ producer ------------------------------
-    // s_ids[stage % 16][32]: [0, SP) base page ids, [8 + ai*SP + pg] residual page id of agent ai, page pg
-    const int32_t lead = s_agents[0];
-    int issued = 0;
-    bool ok = true;
-    for (int s = 0; s < n_stages && ok; ++s) {
-      if ((s & 15) == 0) {
-        int32_t v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {  // 16 independent loads per lane, all in flight together
-          v[i] = -1;
-          const int ss = s + i;
-          if (ss < n_stages) {
-            if (lane < 8) {
-              const int pi = it.p0 + ss * SP + lane;
-              if (lane < SP && pi < it.p1) v[i] = a.bpt[(int64_t)lead * a.pt_stride + pi];
-            } else if (lane < 8 + na * SP) {
-              const int ai = (lane - 8) / SP, pg = (lane - 8) % SP;
-              const int pi = it.p0 + ss * SP + pg;
-              if (pi < it.p1) v[i] = a.rpt[(int64_t)s_agents[ai] * a.pt_stride + pi];
-            }
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          int32_t x = v[i];
-          const int32_t lim = lane < 8 ? a.num_base_pages : a.num_res_pages;
-          if (x != -1 && (uint32_t)x >= (uint32_t)lim) {
+    // Three in-order streams (K blocks, V blocks, residual steps); each copy is issued
+    // as soon as its buffer is free, so K of a block can land while V of the one before
+    // is still in use.  A block's page ids are fetched once, one per lane: lane p < 8
+    // the base page p, lane 8 ai + p the residual page p of agent ai.  Ids of at most two
+    // blocks are live (one register pair per block parity).
+    const uint8_t* kpool = a.k_base + (int64_t)h * a.num_base_pages * kBaseTile;
+    const uint8_t* vpool = a.v_base + (int64_t)h * a.num_base_pages * kBaseTile;
+    int32_t Lmax = 0;  // rows at or past the longest sequence of the group are never read as data
+    for (int x = 0; x < na; ++x) Lmax = max(Lmax, s_L[x]);
+    int kb = 0, vb = 0, rn = 0;
+    int32_t bid0 = 0, bid1 = 0, rid0 = 0, rid1 = 0;
+    uint32_t idle = 0;
+    while (vb < nb || rn < N) {
+      bool prog = false;
+      if (kb < nb && vb >= kb - 1 && rn >= (kb - 1) * na &&
+          (kb < 2 || warp_test(&bars[kKEmpty0 + (kb & 1)], ((kb >> 1) - 1) & 1))) {
+        const int pbase = it.p0 + kb * kBlockPages;
+        const int nvp = min(kBlockPages, it.p1 - pbase);
+        const int pg = lane & 7, ag = lane >> 3;
+        int32_t bid = 0, rid = 0;
+        if (lane < nvp) {
+          bid = a.bpt[(int64_t)it.agents[0] * a.pt_stride + pbase + lane];
+          if ((uint32_t)bid >= (uint32_t)a.num_base_pages) {
             flag_status(a.status, kDevBadPage);
-            x = 0;
+            bid = 0;
           }
-          s_ids[i * 32 + lane] = x;
         }
-        __syncwarp();
+        if (ag < na && pg < nvp) {
+          int32_t agent = it.agents[0];
+#pragma unroll
+          for (int x = 1; x < kMaxGroup; ++x)
+            if (ag == x) agent = it.agents[x];
+          rid = a.rpt[(int64_t)agent * a.pt_stride + pbase + pg];
+          if ((uint32_t)rid >= (uint32_t)a.num_res_pages) {
+            flag_status(a.status, kDevBadPage);
+            rid = 0;
+          }
+        }
+        if (kb & 1) {
+          bid1 = bid;
+          rid1 = rid;
+        } else {
+          bid0 = bid;
+          rid0 = rid;
+        }
+        uint64_t* bar = &bars[kKFull0 + (kb & 1)];
+        copy_block(kpool, smem + kOffK + (kb & 1) * kBlockTiles, true, bid, nvp, kPage, bar, lane);
+        if (lane == 0) mbar_arrive(bar);
+        ++kb;
+        prog = true;
       }
-      const int slot = s % NS;
-      const uint32_t round = s / NS;
-      if (s >= NS) ok = mbar_wait(&empty[slot], (round - 1) & 1, a.status);
+      if (vb < kb && (vb < 2 || warp_test(&bars[kVEmpty0 + (vb & 1)], ((vb >> 1) - 1) & 1))) {
+        const int pbase = it.p0 + vb * kBlockPages;
+        const int nvp = min(kBlockPages, it.p1 - pbase);
+        const int rows = min(kPage, max(0, Lmax - (pbase + nvp - 1) * kPage));  // valid rows of the last page
+        uint64_t* bar = &bars[kVFull0 + (vb & 1)];
+        copy_block(vpool, smem + kOffV + (vb & 1) * kBlockTiles, true, (vb & 1) ? bid1 : bid0, nvp, rows, bar, lane);
+        if (lane == 0) mbar_arrive(bar);
+        ++vb;
+        prog = true;
+      }
+      if (rn < N && rn / na < kb &&
+          (rn < kResSlots || warp_test(&bars[kResEmpty0 + (rn & 3)], ((rn >> 2) - 1) & 1))) {
+        const int rb = rn / na, ag = rn - rb * na;
+        const int pbase = it.p0 + rb * kBlockPages;
+        const int nvp = min(kBlockPages, it.p1 - pbase);
+        const int rows = min(kPage, max(0, s_L[ag] - (pbase + nvp - 1) * kPage));
+        const int32_t rid = __shfl_sync(0xffffffffu, (rb & 1) ? rid1 : rid0, ag * 8 + (lane & 7));
+        uint64_t* bar = &bars[kResFull0 + (rn & 3)];
+        copy_block(a.k_res, smem + kOffKr + (rn & 3) * kResSlotBytes, false, rid, nvp, kPage, bar, lane);
+        copy_block(a.v_res, smem + kOffVr + (rn & 3) * kVrSlotBytes, false, rid, nvp, rows, bar, lane);
+        if (lane == 0) mbar_arrive(bar);
+        ++rn;
+        prog = true;
+      }
+      if (prog) {
+        idle = 0;
+      } else if (++idle > kWaitLimit) {
+        if (lane == 0) flag_status(a.status, kDevTimeout);
+        break;
+      } else {
+        __nanosleep(128);  // leave the issue slots to the compute warps sharing this sub-partition
+      }
+    }
+    // never leave with copies in flight: the last phase of every barrier written to
+    for (int b = max(0, kb - 2); b < kb; ++b) mbar_wait(&bars[kKFull0 + (b & 1)], (b >> 1) & 1, a.status);
+    for (int b = max(0, vb - 2); b < vb; ++b) mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status);
+    for (int n = max(0, rn - kResSlots); n < rn; ++n)
+      mbar_wait(&bars[kResFull0 + (n & 3)], (n >> 2) & 1, a.status);
+  } else if (warp == 1) {
+    // ------------------------- U and score MMA issuer -------------------------
+    // Issues whichever product is ready, the score product first.  (Each MMA costs
+    // the tensor core about the same time however small, so the value products of a
+    // block go out from a second warp, once per block for all its agents.)
+    if (lane == 0) {
+      const uint32_t idU = tc::idesc_bf16(128, 128, 0, 0);
+      const uint32_t idS = tc::idesc_bf16(128, 16, 0, 0);
+      const uint32_t sBase = smem_u32(smem);
+      bool ok = mbar_wait(&bars[kQReady], 0, a.status) && mbar_wait(&bars[kBkReady], 0, a.status);
+      int nu = 0, ns = 0;
+      uint32_t idle = 0;
+      while (ok && ns < N) {
+        bool prog = false;
+        if (ns < nu && (ns < 2 || mbar_test(&bars[kSFree0 + (ns & 1)], ((ns >> 1) - 1) & 1)) &&
+            mbar_test(&bars[kKFFull0 + (ns & 1)], (ns >> 1) & 1)) {  // S = K . Q^T
+          tc::fence_after();
+          const int ai = ns % na;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_ts(tm + kTmS + 16 * (ns & 1), tm + kTmKF + 64 * (ns & 1) + 8 * ks,
+                       tc::smem_desc(sBase + kOffQ + ai * 2048 + (ks >> 2) * 1024 + (ks & 3) * 32, 16,
+                                     kOffQZero - (kOffQ + ai * 2048 + (ks >> 2) * 1024), tc::kSwizzle128B),
+                       idS, ks > 0);
+          tc::commit(&bars[kSFull0 + (ns & 1)]);
+          tc::commit(&bars[kKFFree0 + (ns & 1)]);
+          ++ns;
+          prog = true;
+        }
+        if (nu < N && (nu < 2 || mbar_test(&bars[kUFree0 + (nu & 1)], ((nu >> 1) - 1) & 1)) &&
+            mbar_test(&bars[kResFull0 + (nu & 3)], (nu >> 2) & 1)) {  // U = Kr . B_k^T
+          tc::fence_after();
+          const int ai = nu % na;
+          tc::mma_ss(tm + kTmU + 128 * (nu & 1),
+                     tc::smem_desc(sBase + kOffKr + (nu & 3) * kResSlotBytes, 16, 256, tc::kSwizzle32B),
+                     tc::smem_desc(sBase + kOffBk + ai * 4096, 16, 256, tc::kSwizzle32B), idU, 0);
+          tc::commit(&bars[kUFull0 + (nu & 1)]);
+          tc::commit(&bars[kResEmpty0 + (nu & 3)]);
+          ++nu;
+          prog = true;
+        }
+        if (prog) {
+          idle = 0;
+        } else if (++idle > kWaitLimit) {
+          flag_status(a.status, kDevTimeout);
+          ok = false;
+        } else {
+          __nanosleep(32);
+        }
+      }
+      // never leave with MMAs in flight
+      tc::commit(&bars[kMmaDone]);
+      mbar_wait(&bars[kMmaDone], 0, a.status);
+    }
+    __syncwarp();
+  } else if (warp < kSoftWarp0) {
+    // ------------------------------ RoPE group ------------------------------
+    // Two warps per TMEM lane quadrant; warp half hf owns K columns [32 hf, 32 hf + 32)
+    // and [64 + 32 hf, 96 + 32 hf) of its 32 keys.
+    const int q4 = warp & 3, hf = (warp - 2) >> 2;
+    const int row = 32 * q4 + lane;  // key row of the block == TMEM lane; also the d row of B_k^T
+    const uint32_t tl = tm + ((uint32_t)(32 * q4) << 16);
+    for (int ai = 0; ai < na; ++ai) {  // B_k^T of every agent: this warp's 8 of the 16 ranks of row d
+      int32_t agent = it.agents[0];
+#pragma unroll
+      for (int x = 1; x < kMaxGroup; ++x)
+        if (ai == x) agent = it.agents[x];
+      int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
+      if ((uint32_t)adapter >= (uint32_t)a.n_adapters) {
+        flag_status(a.status, kDevBadArg);
+        adapter = 0;
+      }
+      const __nv_bfloat16* B = a.B_k + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim + row;
+      uint8_t* dst = smem + kOffBk + ai * 4096;
+#pragma unroll
+      for (int k = 8 * hf; k < 8 * hf + 8; ++k)
+        *reinterpret_cast<__nv_bfloat16*>(dst + tc::sw32_off(row, k)) = B[(int64_t)k * a.hkv * kHeadDim];
+    }
+    tc::fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kBkReady]);
+    const int pg = row >> 4, t = row & 15;
+    bool ok = true;
+    uint4 rp[2][4];  // rotation groups of this warp's two column chunks for key j (see below)
+    for (int n = 0; n < N && ok; ++n) {
+      const int b = n / na, ai = n - b * na;
+      const int stage = b & 1;
+      const int pbase = it.p0 + b * kBlockPages;
+      const int j = pbase * kPage + row;
+      if (ai == 0) {
+        // chunk c = 32 hf + 16 cc holds frequency groups m = c/2 .. c/2 + 7: 32-byte units
+        // c/8 and c/8 + 1 of the row, stored at unit u ^ (j % 8)
+        const int jr = j < a.rope_positions ? j : 0;
+        const uint4* rrow = reinterpret_cast<const uint4*>(a.rope + (int64_t)jr * kRopeRow);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int uu = 0; uu < 2; ++uu) {
+            const int u = 4 * hf + 2 * cc + uu;
+            rp[cc][2 * uu] = __ldg(rrow + (u ^ (j & 7)) * 2);
+            rp[cc][2 * uu + 1] = __ldg(rrow + (u ^ (j & 7)) * 2 + 1);
+          }
+        ok = mbar_wait(&bars[kKFull0 + stage], (b >> 1) & 1, a.status);
+        if (!ok) break;
+      }
+      ok = mbar_wait(&bars[kUFull0 + (n & 1)], (n >> 1) & 1, a.status);
+      if (ok && n >= 2) ok = mbar_wait(&bars[kKFFree0 + (n & 1)], ((n >> 1) - 1) & 1, a.status);
       if (!ok) break;
-      const int pbase = it.p0 + s * SP;
-      const int nvp = min(SP, it.p1 - pbase);
-      uint8_t* st = stages + (int64_t)slot * sbytes;
-      const int32_t* ids = s_ids + (s & 15) * 32;
-      if (lane == 0) mbar_arrive_expect_tx(&full[slot], nvp * (2 * kBaseTile + 16 * kRopeRow) + na * nvp * 2 * kResTile);
+      tc::fence_after();
+      const uint8_t* kt = smem + kOffK + stage * kBlockTiles + pg * kBaseTile;
+      const uint32_t tu = tl + kTmU + 128 * (n & 1);
+      const uint32_t kf = tl + kTmKF + 64 * (n & 1);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {  // d in [c, c + 16) and [c + 64, c + 80)
+        const int c = 32 * hf + 16 * cc;
+        uint32_t ulo[16], uhi[16];
+        tc::ld16(tu + c, ulo);
+        tc::ld16(tu + 64 + c, uhi);
+        uint4 kl[2], kh[2];
+        kl[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c));
+        kl[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 8));
+        kh[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 64));
+        kh[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 72));
+        tc::wait_ld();
+        const uint32_t* klw = reinterpret_cast<const uint32_t*>(kl);
+        const uint32_t* khw = reinterpret_cast<const uint32_t*>(kh);
+        uint32_t olo[8], ohi[8];
+#pragma unroll
+        for (int i2 = 0; i2 < 8; ++i2) {  // frequency group m = c/2 + i2: frequencies of d = c + 2 i2, + 1
+          const uint4 w = rp[cc][(i2 >> 2) * 2 + ((i2 & 3) >> 1)];
+          const uint32_t cw = (i2 & 1) ? w.z : w.x, sw = (i2 & 1) ? w.w : w.y;
+          const float c0 = bf_lo(cw), c1 = bf_hi(cw), s0 = bf_lo(sw), s1 = bf_hi(sw);
+          const float lo0 = __uint_as_float(ulo[2 * i2]), lo1 = __uint_as_float(ulo[2 * i2 + 1]);
+          const float hi0 = __uint_as_float(uhi[2 * i2]), hi1 = __uint_as_float(uhi[2 * i2 + 1]);
+          // K = Kb + RoPE_j(U) in fp32, rounded to bf16 once
+          const float kl0 = fmaf(lo0, c0, fmaf(-hi0, s0, bf_lo(klw[i2])));
+          const float kl1 = fmaf(lo1, c1, fmaf(-hi1, s1, bf_hi(klw[i2])));
+          const float kh0 = fmaf(lo0, s0, fmaf(hi0, c0, bf_lo(khw[i2])));
+          const float kh1 = fmaf(lo1, s1, fmaf(hi1, c1, bf_hi(khw[i2])));
+          olo[i2] = pack_bf16(kl0, kl1);
+          ohi[i2] = pack_bf16(kh0, kh1);
+        }
+        tc::st8(kf + (c >> 1), olo);       // K columns d < 64: bf16 pairs (d, d + 1) at column d / 2
+        tc::st8(kf + 32 + (c >> 1), ohi);  // K columns d >= 64
+      }
+      tc::fence_before();
       __syncwarp();
-      if (lane < 2) {
-        // K (lane 0) or V (lane 1) tiles: one bulk copy per run of consecutive page ids
-        const uint8_t* pool = lane == 0 ? a.k_base : a.v_base;
-        uint8_t* dst = st + (lane == 0 ? 0 : v_at);
-        int r0 = 0;
-        for (int pg = 1; pg <= nvp; ++pg) {
-          if (pg == nvp || ids[pg] != ids[pg - 1] + 1) {
-            bulk_g2s(dst + r0 * kBaseTile, pool + (head_base + ids[r0]) * kBaseTile, (pg - r0) * kBaseTile,
-                     &full[slot]);
-            r0 = pg;
-          }
-        }
-      } else if (lane == 2) {
-        int64_t rrow = (int64_t)pbase * 16;
-        if (rrow + 16 * nvp > a.rope_positions) {
-          flag_status(a.status, kDevBadArg);
-          rrow = 0;
-        }
-        bulk_g2s(st + rope_at, a.rope + rrow * kRopeRow, nvp * 16 * kRopeRow, &full[slot]);
-      } else if (lane >= 8 && lane < 8 + na) {
-        // residual k and v tiles of one agent, one copy per run of consecutive page ids
-        const int ai = lane - 8;
-        const int32_t* rid = ids + 8 + ai * SP;
-        int r0 = 0;
-        for (int pg = 1; pg <= nvp; ++pg) {
-          if (pg == nvp || rid[pg] != rid[pg - 1] + 1) {
-            const int64_t src = (int64_t)rid[r0] * kResTile;
-            const uint32_t n = (pg - r0) * kResTile;
-            bulk_g2s(st + kr_at + (ai * SP + r0) * kResTile, a.k_res + src, n, &full[slot]);
-            bulk_g2s(st + vr_at + (ai * SP + r0) * kResTile, a.v_res + src, n, &full[slot]);
-            r0 = pg;
-          }
-        }
+      if (lane == 0) mbar_arrive(&bars[kUFree0 + (n & 1)]);
+      tc::wait_st();
+      tc::fence_proxy_async();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[kKFFull0 + (n & 1)]);
+        if (ai == na - 1) mbar_arrive(&bars[kKEmpty0 + stage]);
       }
-      issued = s + 1;
     }
-    // Drain: never leave the CTA with bulk copies still in flight.
-    for (int s = max(0, issued - NS); s < issued; ++s) mbar_wait(&full[s % NS], (s / NS) & 1, a.status);
+  } else if (warp == kValueWarp) {
+    // ------------------------------ value products ------------------------------
+    // Per block, for all its agents at once (B = P^T of every agent side by side,
+    // 8 columns each):
+    //   O^T += Vb^T . P^T                  [128 d x 8 na]
+    //   R   += [Vr^T; 1](stacked) . P^T     [128 x 8 na]
+    // The second product's A operand stacks, per agent a, Vr^T (rows 32 a .. 32 a + 15)
+    // and a block of ones (rows 32 a + 16 .. 32 a + 31): 16-row atoms 4 KB apart, the
+    // slot layout being [v_res | ones].  Rows 32 a + r, columns 8 a + g of R hold
+    // acc_r^T[r][g] of agent a, rows 32 a + 16.. its l[g] = sum_keys P; the other cells
+    // are cross terms, never read.
+    if (lane == 0) {
+      const uint32_t nP = na > 2 ? 32 : 16;
+      const uint32_t idV = tc::idesc_bf16(128, nP, 1, 1);
+      const uint32_t sBase = smem_u32(smem);
+      bool ok = true;
+      for (int b = 0; b < nb && ok; ++b) {
+        const int n0 = b * na;
+        ok = mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status) &&
+             mbar_wait(&bars[kPFull0 + (b & 1)], (b >> 1) & 1, a.status);
+        for (int x = 0; x < na && ok; ++x) ok = mbar_wait(&bars[kResFull0 + ((n0 + x) & 3)], ((n0 + x) >> 2) & 1, a.status);
+        if (!ok) break;
+        tc::fence_after();
+        const int nvp = min(kBlockPages, it.p1 - (it.p0 + b * kBlockPages));
+        const uint32_t vt = sBase + kOffV + (b & 1) * kBlockTiles;
+        const uint32_t vr = sBase + kOffVr + (n0 & 3) * kVrSlotBytes;
+        const uint32_t pp = sBase + kOffP + (b & 1) * 8192;
+        for (int ks = 0; ks < nvp; ++ks)
+          tc::mma_ss(tm + kTmO, tc::smem_desc(vt + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B),
+                     tc::smem_desc(pp + ks * 512, 4096, 256, tc::kSwizzle32B), idV, (b > 0 || ks > 0));
+        for (int ks = 0; ks < nvp; ++ks)
+          tc::mma_ss(tm + kTmR, tc::smem_desc(vr + ks * kResTile, kResSlotBytes, 256, tc::kSwizzle32B),  // 8 atoms
+                     tc::smem_desc(pp + ks * 512, 4096, 256, tc::kSwizzle32B), idV, (b > 0 || ks > 0));
+        tc::commit(&bars[kPFree0 + (b & 1)]);
+        tc::commit(&bars[kODone0 + (b & 1)]);
+        tc::commit(&bars[kVEmpty0 + (b & 1)]);
+        for (int x = 0; x < na; ++x) tc::commit(&bars[kResEmpty0 + ((n0 + x) & 3)]);
+      }
+      tc::commit(&bars[kValDone]);
+      mbar_wait(&bars[kValDone], 0, a.status);
+    }
+    __syncwarp();
   } else {
-    // ------------------------------ consumers ------------------------------
-    const int ai = warp % na, pl = warp / na;
-    const int32_t agent = s_agents[ai];
-    const int32_t L = a.seq_lens[agent];
-    const int32_t pos = a.positions[agent];
-    const int G = a.G;
-    if (lane == 0 && pl == 0 && h == 0 && (L < 1 || L > a.max_seq_len || pos < 0 || pos >= L))
-      flag_status(a.status, kDevBadArg);
-    int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
-    if ((uint32_t)adapter >= (uint32_t)a.n_adapters) {
-      flag_status(a.status, kDevBadArg);
-      adapter = 0;
+    // ------------------------------ softmax group ------------------------------
+    const int sw_ = warp & 3;
+    const int row = 32 * sw_ + lane;  // key row of the block == TMEM lane (and d row of O^T)
+    const uint32_t tl = tm + ((uint32_t)(32 * sw_) << 16);
+    float* mref = s_mref + sw_ * (kMaxGroup * 8);  // this warp's copy (all four evolve identically)
+    // Q^T of every agent: [2 halves][8 rows (query heads, zero past G)][128 B]; the score
+    // product's second 8-row group (query heads 8..15) reads a shared block of zeros
+    for (int ai = 0; ai < na; ++ai) {
+      int32_t agent = it.agents[0];
+#pragma unroll
+      for (int x = 1; x < kMaxGroup; ++x)
+        if (ai == x) agent = it.agents[x];
+      const int g = row >> 4, ch = row & 15;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (g < G)
+        v = *reinterpret_cast<const uint4*>(a.q + ((int64_t)agent * a.hkv * G + (int64_t)h * G + g) * kHeadDim + ch * 8);
+      *reinterpret_cast<uint4*>(smem + kOffQ + ai * 2048 + tc::sw128_off(8, g, ch * 8)) = v;
     }
+    if (row < 64) *reinterpret_cast<uint4*>(smem + kOffQZero + 16 * row) = make_uint4(0u, 0u, 0u, 0u);
+    tc::fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kQReady]);
 
-    // q^T operand fragments (B of m16n8k16: n = query head g, k = d), bf16
-    uint32_t qb[8][2];
-    {
-      const __nv_bfloat16* qrow = a.q + ((int64_t)agent * a.hkv * G + (int64_t)h * G + g) * kHeadDim;
+    const int gl = lane >> 2;  // query head whose warp-wide reductions this lane ends up holding
+    bool ok = true;
+    for (int n = 0; n < N && ok; ++n) {
+      const int b = n / na, ai = n - b * na;
+      const int pbase = it.p0 + b * kBlockPages;
+      const int j = pbase * kPage + row;
+      const int32_t L = s_L[ai], pos = s_pos[ai];
+      const bool vis = j < L && j <= pos && j < it.p1 * kPage;
+      ok = mbar_wait(&bars[kSFull0 + (n & 1)], (n >> 1) & 1, a.status);
+      if (!ok) break;
+      tc::fence_after();
+      uint32_t sv[8];
+      tc::ld8(tl + kTmS + 16 * (n & 1), sv);
+      tc::wait_ld();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kSFree0 + (n & 1)]);
+      float sc[8], mx[8];
 #pragma unroll
-      for (int s = 0; s < 8; ++s)
+      for (int g = 0; g < 8; ++g) {
+        sc[g] = (vis && g < G) ? __uint_as_float(sv[g]) * a.scale_log2 : -INFINITY;
+        mx[g] = sc[g];
+      }
+      const float wmax = warp_reduce8<true>(mx, lane);  // max over the warp's keys of query head gl
+      float* red = s_red + (n & 1) * 32;
+      if ((lane & 3) == 0) red[sw_ * 8 + gl] = wmax;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kRed0 + (n & 1)]);
+      // while the other warps' maxima come in: probabilities against the current reference
+      float mr[8], ps[8];
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-          qb[s][e] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s + 8 * e + 2 * q4) : 0u;
-    }
-    // B_k operand fragments (B of m16n8k16: k = rank, n = d within the head)
-    uint32_t bk[16][2];
-    {
-      const __nv_bfloat16* B = a.B_k + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim;
-      const int64_t ld = (int64_t)a.hkv * kHeadDim;
+      for (int g = 0; g < 8; ++g) {
+        mr[g] = mref[ai * 8 + g];
+        ps[g] = (vis && g < G) ? ex2(sc[g] - (mr[g] == -INFINITY ? 0.f : mr[g])) : 0.f;
+      }
+      ok = mbar_wait(&bars[kRed0 + (n & 1)], (n >> 1) & 1, a.status);
+      if (!ok) break;
+      // lazy rescale: keep the reference maximum unless the block maximum passes it by 2^8
+      float alpha[8];
+      bool need_any = false;
 #pragma unroll
-      for (int t = 0; t < 16; ++t) {
-        const int n = 8 * t + g;
+      for (int g = 0; g < 8; ++g) {
+        const float bm = fmaxf(fmaxf(red[g], red[8 + g]), fmaxf(red[16 + g], red[24 + g]));
+        const bool need = g < G && bm > mr[g] + 8.f;
+        need_any |= need;
+        alpha[g] = (need && mr[g] != -INFINITY) ? ex2(mr[g] - bm) : 1.f;
+        if (need) mr[g] = bm;
+      }
+      if (need_any) {  // uniform across the group: every warp saw the same maxima
+        const float ml = select8(mr, gl);
+        __syncwarp();
+        if ((lane & 3) == 0) mref[ai * 8 + gl] = ml;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int k = 8 * e + 2 * q4;
-          __nv_bfloat162 v;
-          v.x = B[k * ld + n];
-          v.y = B[(k + 1) * ld + n];
-          bk[t][e] = *reinterpret_cast<uint32_t*>(&v);
+        for (int g = 0; g < 8; ++g) ps[g] = (vis && g < G) ? ex2(sc[g] - mr[g]) : 0.f;
+        if (b > 0) {
+          // O^T and R are stable once the value products of block b - 1 are done (one barrier
+          // per block parity, so a wait is never more than one phase ahead of the barrier)
+          ok = mbar_wait(&bars[kODone0 + ((b - 1) & 1)], ((b - 1) >> 1) & 1, a.status);
+          if (!ok) break;
+          tc::fence_after();
+          uint32_t ov[8], rv[8];
+          tc::ld8(tl + kTmO + 8 * ai, ov);
+          tc::ld8(tl + kTmR + 8 * ai, rv);
+          tc::wait_ld();
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            ov[g] = __float_as_uint(__uint_as_float(ov[g]) * alpha[g]);
+            rv[g] = __float_as_uint(__uint_as_float(rv[g]) * alpha[g]);
+          }
+          tc::st8(tl + kTmO + 8 * ai, ov);
+          tc::st8(tl + kTmR + 8 * ai, rv);
+          tc::wait_st();
+          tc::fence_before();
         }
       }
+      uint32_t pw[4];  // P^T[key][g] in bf16, zero past G or for masked keys
+#pragma unroll
+      for (int g2 = 0; g2 < 4; ++g2) pw[g2] = pack_bf16(ps[2 * g2], ps[2 * g2 + 1]);
+      if (ai == 0 && b >= 2) ok = mbar_wait(&bars[kPFree0 + (b & 1)], ((b >> 1) - 1) & 1, a.status);
+      if (!ok) break;
+      // P^T of agent ai: columns 8 ai .. 8 ai + 7 = atom ai / 2, 16-byte chunk ai % 2 of each row
+      uint8_t* pbuf = smem + kOffP + (b & 1) * 8192 + (ai >> 1) * 4096;
+      *reinterpret_cast<uint4*>(pbuf + tc::sw32_off(row, (ai & 1) * 8)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      if (ai == na - 1) {
+        tc::fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kPFull0 + (b & 1)]);
+      }
     }
-
-    // per-lane shared-memory offsets (loop invariant)
-    const int mi = lane >> 3;
-    const int lrow = (lane & 7) + (mi & 1) * 8, bsel = mi >> 1;  // A fragments of K (keys x d), Kr
-    const int tkey = (lane & 7) + (mi >> 1) * 8, vsel = mi & 1;  // transposed A fragments of V, Vr
-    uint32_t kofs[4], vofs[4];
+    // epilogue: one partial (m, l, acc, acc_r) per (agent, head); after a timeout the
+    // values are meaningless but every wait stays bounded
+    if (it.slot_base >= 0) {
+      if (nb > 0) mbar_wait(&bars[kODone0 + ((nb - 1) & 1)], ((nb - 1) >> 1) & 1, a.status);
+      tc::fence_after();
+      for (int ai = 0; ai < na; ++ai) {
+        uint32_t ov[8], rv[8];
+        tc::ld8(tl + kTmO + 8 * ai, ov);
+        tc::ld8(tl + kTmR + 8 * ai, rv);
+        tc::wait_ld();
+        const int64_t rec0 = ((int64_t)(it.slot_base + ai) * a.hkv + h) * G;
+        const int r = row - 32 * ai;  // row of this lane within agent ai's [acc_r^T ; l] rows of R
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kofs[i] = lrow * 128 + (((2 * i + bsel) ^ (lrow & 7)) << 4);
-      vofs[i] = tkey * 128 + (((2 * i + vsel) ^ (tkey & 7)) << 4);
-    }
-    const uint32_t krofs = res_off(lrow, bsel * 8), vrofs = res_off(tkey, vsel * 8);
-    const uint32_t rrow0 = g * kRopeRow + q4 * 8, rrow1 = (g + 8) * kRopeRow + q4 * 8;
-
-    for (int s = 0; s < n_stages; ++s) {
-      const int slot = s % NS;
-      if (!mbar_wait(&full[slot], (s / NS) & 1, a.status)) break;
-      const int pbase = it.p0 + s * SP;
-      const int nvp = min(SP, it.p1 - pbase);
-      const uint32_t st = smem_u32(stages + (int64_t)slot * sbytes);
-      for (int pg = pl; pg < nvp; pg += wpp) {
-        const uint32_t sK = st + pg * kBaseTile;
-        const uint32_t sV = st + v_at + pg * kBaseTile;
-        const uint32_t sR = st + rope_at + pg * 16 * kRopeRow;
-        const uint32_t sKr = st + kr_at + (ai * SP + pg) * kResTile;
-        const uint32_t sVr = st + vr_at + (ai * SP + pg) * kResTile;
-        const int j0 = (pbase + pg) * kPage;
-
-        // full keys K = Kb + RoPE_j(Kr B_k) as A fragments, and S^T = K q^T
-        float S0[4] = {0.f, 0.f, 0.f, 0.f}, S1[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t ka0, ka1, ka2, ka3;
-        ldsm_x4(sKr + krofs, ka0, ka1, ka2, ka3);
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          float U[4][4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const int t = 2 * s4 + (x & 1) + (x >> 1) * 8;  // tiles 2s4, 2s4+1, 2s4+8, 2s4+9
-            U[x][0] = U[x][1] = U[x][2] = U[x][3] = 0.f;
-            mma_bf16(U[x], ka0, ka1, ka2, ka3, bk[t][0], bk[t][1]);
-          }
-          uint32_t klo[4], khi[4];  // Kb fragments of k-steps s4 (d < 64) and s4 + 4 (d >= 64)
-          ldsm_x4(sK + kofs[s4], klo[0], klo[1], klo[2], klo[3]);
-          ldsm_x4(sK + 2048 + kofs[s4], khi[0], khi[1], khi[2], khi[3]);
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const uint32_t cofs = ((2 * s4 + x) ^ g) << 5;  // frequency group 4(2s4+x)+q4, swizzled by row
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-              const uint2 cs = ld_shared_u64(sR + (rr ? rrow1 : rrow0) + cofs);
-              uint32_t lo = pack_bf16(U[x][2 * rr], U[x][2 * rr + 1]);
-              uint32_t hi = pack_bf16(U[x + 2][2 * rr], U[x + 2][2 * rr + 1]);
-              rotate_bf16x2(lo, hi, cs.x, cs.y);
-              klo[2 * x + rr] = bf2_add(klo[2 * x + rr], lo);
-              khi[2 * x + rr] = bf2_add(khi[2 * x + rr], hi);
+        for (int g = 0; g < 8; ++g)
+          if (g < G) {
+            a.part[(rec0 + g) * kPartCols + row] = nb > 0 ? __uint_as_float(ov[g]) : 0.f;
+            if (r >= 0 && r < kRank) a.part[(rec0 + g) * kPartCols + kHeadDim + r] = nb > 0 ? __uint_as_float(rv[g]) : 0.f;
+            if (r == kRank) {
+              a.ml[(rec0 + g) * 2] = nb > 0 ? mref[ai * 8 + g] : -INFINITY;
+              a.ml[(rec0 + g) * 2 + 1] = nb > 0 ? __uint_as_float(rv[g]) : 0.f;
             }
           }
-          mma_bf16(S0, klo[0], klo[1], klo[2], klo[3], qb[s4][0], qb[s4][1]);
-          mma_bf16(S1, khi[0], khi[1], khi[2], khi[3], qb[s4 + 4][0], qb[s4 + 4][1]);
-        }
-        // mask (only the last pages of an agent need it) + online softmax in base 2
-        float sc[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[e] = (S0[e] + S1[e]) * a.scale_log2;
-        if (!(j0 + kPage - 1 < L && j0 + kPage - 1 <= pos)) {
-          const int ja = j0 + g, jb = j0 + g + 8;
-          if (!(ja < L && ja <= pos)) sc[0] = sc[1] = -INFINITY;
-          if (!(jb < L && jb <= pos)) sc[2] = sc[3] = -INFINITY;
-        }
-        float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-        }
-        // lazy rescale: move the reference maximum only when a score exceeds it by 2^8
-        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-          const float al0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-          const float al1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-          l0 *= al0;
-          l1 *= al1;
-#pragma unroll
-          for (int mb = 0; mb < 8; ++mb) {
-            acc[mb][0] *= al0;
-            acc[mb][1] *= al1;
-            acc[mb][2] *= al0;
-            acc[mb][3] *= al1;
-          }
-          accr[0] *= al0;
-          accr[1] *= al1;
-          accr[2] *= al0;
-          accr[3] *= al1;
-          m0 = mn0;
-          m1 = mn1;
-        }
-        const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
-        const float p0 = exp2f(sc[0] - mu0), p2 = exp2f(sc[2] - mu0);
-        const float p1 = exp2f(sc[1] - mu1), p3 = exp2f(sc[3] - mu1);
-        l0 += p0 + p2;
-        l1 += p1 + p3;
-        // probabilities as the B operand (k = key, n = query head)
-        const uint32_t pb0 = movmatrix_t(pack_bf16(p0, p1));
-        const uint32_t pb1 = movmatrix_t(pack_bf16(p2, p3));
-        // acc^T += Vb^T . P^T ; acc_r^T += Vr^T . P^T
-#pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(sV + (mb >> 2) * 2048 + vofs[mb & 3], r0, r1, r2, r3);
-          mma_bf16(acc[mb], r0, r1, r2, r3, pb0, pb1);
-        }
-        {
-          uint32_t r0, r1, r2, r3;
-          ldsm_x4_t(sVr + vrofs, r0, r1, r2, r3);
-          mma_bf16(accr, r0, r1, r2, r3, pb0, pb1);
-        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-    }
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
   }
-  __syncthreads();  // every warp has left the pipeline: the stage buffers are free
-
-  if (warp < kWarps) {  // park this warp's partial in shared memory
-    float* sw = reinterpret_cast<float*>(stages) + warp * 8 * kPartCols;
-    float* sml = reinterpret_cast<float*>(stages) + kWarps * 8 * kPartCols + warp * 16;
-    const int ga = 2 * q4, gb = 2 * q4 + 1;
-#pragma unroll
-    for (int mb = 0; mb < 8; ++mb) {
-      sw[ga * kPartCols + 16 * mb + g] = acc[mb][0];
-      sw[gb * kPartCols + 16 * mb + g] = acc[mb][1];
-      sw[ga * kPartCols + 16 * mb + g + 8] = acc[mb][2];
-      sw[gb * kPartCols + 16 * mb + g + 8] = acc[mb][3];
-    }
-    sw[ga * kPartCols + kHeadDim + g] = accr[0];
-    sw[gb * kPartCols + kHeadDim + g] = accr[1];
-    sw[ga * kPartCols + kHeadDim + g + 8] = accr[2];
-    sw[gb * kPartCols + kHeadDim + g + 8] = accr[3];
-    if (g == 0) {
-      sml[ga * 2] = m0;
-      sml[ga * 2 + 1] = l0;
-      sml[gb * 2] = m1;
-      sml[gb * 2 + 1] = l1;
-    }
-  }
+  tc::fence_before();
   __syncthreads();
-
-  // merge the warps of each agent and write one partial per (item, agent, head)
-  {
-    const int G = a.G;
-    const float* sbuf = reinterpret_cast<const float*>(stages);
-    const float* smlb = sbuf + kWarps * 8 * kPartCols;
-    const int total = it.slot_base < 0 ? 0 : na * G * kPartCols;
-    for (int idx = threadIdx.x; idx < total; idx += kThreads) {
-      const int ai = idx / (G * kPartCols);
-      const int r = idx % (G * kPartCols);
-      const int gq = r / kPartCols, col = r % kPartCols;
-      float M = -INFINITY;
-      for (int p = 0; p < wpp; ++p) M = fmaxf(M, smlb[(p * na + ai) * 16 + gq * 2]);
-      float v = 0.f, lsum = 0.f;
-      if (M != -INFINITY) {
-        for (int p = 0; p < wpp; ++p) {
-          const int w = p * na + ai;
-          const float wt = exp2f(smlb[w * 16 + gq * 2] - M);
-          v += wt * sbuf[w * 8 * kPartCols + gq * kPartCols + col];
-          lsum += wt * smlb[w * 16 + gq * 2 + 1];
-        }
-      }
-      const int64_t rec = ((int64_t)(it.slot_base + ai) * a.hkv + h) * G + gq;
-      a.part[rec * kPartCols + col] = v;
-      if (col == 0) {
-        a.ml[rec * 2] = M;
-        a.ml[rec * 2 + 1] = lsum;
-      }
-    }
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tm, kTmCols);
   }
 }
 
@@ -602,12 +856,12 @@ DecodeGeometry decode_geometry(const forkkv_attn_params& p) {
     // Split every agent's pages into `chunks` items of `chunk_pages` pages (a multiple
     // of 8, one page per warp per stage) so that A * chunks * Hkv fills two waves.
     const int32_t max_pages = (p.max_seq_len + kPage - 1) / kPage;
-    const int64_t want = 2 * 152;
+    const int64_t want = 152;  // one CTA per SM
     int32_t chunks = (int32_t)((want + (int64_t)p.n_agents * p.num_kv_heads - 1) /
                                ((int64_t)p.n_agents * p.num_kv_heads));
     chunks = max(1, min(chunks, (max_pages + 7) / 8));
     int32_t chunk_pages = (max_pages + chunks - 1) / chunks;
-    chunk_pages = max(8, (chunk_pages + 7) / 8 * 8);
+    chunk_pages = max(kBlockPages, (chunk_pages + kBlockPages - 1) / kBlockPages * kBlockPages);
     chunks = (max_pages + chunk_pages - 1) / chunk_pages;
     g.chunks = max(1, chunks);
     g.chunk_pages = chunk_pages;

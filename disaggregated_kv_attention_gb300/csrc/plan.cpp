@@ -7,7 +7,8 @@
 // physical base page there.  The groups fall out of the page tables alone: walk
 // the logical page index, and split a group of agents whenever their physical
 // pages differ (or some of them end).  Each segment (agent group, page range)
-// is then cut into items of at most 8 agents and a bounded number of stages.
+// is then cut into items of at most 4 agents and a bounded number of 128-key
+// blocks (8 pages).
 #include <algorithm>
 #include <cstdint>
 #include <map>
@@ -22,16 +23,18 @@ struct Segment {
   int32_t p0, p1;
 };
 
-// Pages per pipeline stage of the decode kernel for a group of na agents (it
-// has 8 consumer warps: 8 / na warps per agent, each taking stage pages in turn).
-int32_t pages_per_stage(int32_t na) { return na == 8 ? 2 : na == 1 ? 8 : 4; }
+// Pages per pipeline stage of the decode kernel: one 128-key block, whatever the
+// group size (the block's base tiles are read once and reused by every agent).
+constexpr int32_t kStagePages = 8;
+constexpr int32_t kMaxGroup = 4;
+int32_t pages_per_stage(int32_t) { return kStagePages; }
 
 int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents, int32_t pt_stride,
                    int32_t num_kv_heads, int32_t target_ctas, int32_t* plan, int32_t plan_cap_ints,
                    forkkv_plan_info* info) {
   if (!bpt || !seq_lens || !info || n_agents < 1 || pt_stride < 1 || num_kv_heads < 1 || target_ctas < 0)
     return FORKKV_ERR_INVALID_ARG;
-  if (target_ctas == 0) target_ctas = 2 * 152;
+  if (target_ctas == 0) target_ctas = 152;  // one CTA per SM, one wave
   std::vector<int32_t> npages(n_agents);
   for (int32_t a = 0; a < n_agents; ++a) {
     if (seq_lens[a] < 1) return FORKKV_ERR_INVALID_ARG;
@@ -82,7 +85,7 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
     for (auto it = order.rbegin(); it != order.rend(); ++it) stack.push_back({cls[*it], i});
   }
 
-  // 2. groups of at most 8 agents (8, then 4, 2, 1 for the remainder)
+  // 2. groups of at most 4 agents (4, then 2, 1 for the remainder)
   struct Chunk {
     int32_t agents[8];
     int32_t na, p0, p1, stages;
@@ -92,7 +95,7 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
     size_t k = 0;
     while (k < s.agents.size()) {
       const size_t left = s.agents.size() - k;
-      const int32_t na = left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
+      const int32_t na = left >= kMaxGroup ? kMaxGroup : left >= 2 ? 2 : 1;
       Chunk c{};
       for (int32_t x = 0; x < 8; ++x) c.agents[x] = x < na ? s.agents[k + x] : -1;
       c.na = na;

@@ -207,10 +207,11 @@ int32_t forkkv_rope_table_build(double rope_theta, int32_t n_positions, void* ta
 /* ==== decode work plan =====================================================
  * Splits the key ranges of a decode batch into work items so that pages
  * shared by several agents (a fork tree's trunks) are read once per group of
- * up to 8 agents.  Built on the host from host copies of the page tables.
+ * up to 4 agents.  Built on the host from host copies of the page tables.
  * Item i is FORKKV_PLAN_ITEM_INTS int32:
- *   [0] first logical page  [1] end logical page   [2] n_agents (1..8)
- *   [3] pages per stage      [4..11] agent indices  [12] first partial slot
+ *   [0] first logical page  [1] end logical page   [2] n_agents (1, 2 or 4)
+ *   [3] pages per stage (8)  [4..11] agent indices (slots past n_agents repeat
+ *   the first)               [12] first partial slot
  * followed by the per-agent slot lists (CSR: n_agents+1 offsets, then slots). */
 typedef struct {
   int32_t n_items;     /* CTAs per KV head */
@@ -218,7 +219,7 @@ typedef struct {
   int32_t plan_ints;   /* int32 words written to plan */
 } forkkv_plan_info;
 
-/* target_ctas: desired CTAs over all KV heads (0 = 2 per SM of a GB300). */
+/* target_ctas: desired CTAs over all KV heads (0 = one per SM of a GB300). */
 int32_t forkkv_plan_build(const int32_t* bpt_host, const int32_t* seq_lens_host, int32_t n_agents,
                           int32_t pt_stride, int32_t num_kv_heads, int32_t target_ctas,
                           int32_t* plan, int32_t plan_cap_ints, forkkv_plan_info* info);

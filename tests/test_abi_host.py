@@ -206,7 +206,7 @@ def test_plan_covers_every_page_once(shape, target):
     slot_owner = {}
     for i, it in enumerate(items):
         p0, p1, na, wpp = it[:4]
-        assert na in (1, 2, 4, 8) and wpp == {8: 2, 4: 4, 2: 4, 1: 8}[na] and 0 <= p0 < p1
+        assert na in (1, 2, 4) and wpp == 8 and 0 <= p0 < p1
         ags = list(it[4:4 + na])
         for x, ag in enumerate(ags):
             slot_owner[it[12] + x] = ag
