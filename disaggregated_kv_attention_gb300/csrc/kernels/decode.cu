@@ -52,20 +52,24 @@ constexpr int kResSlots = 4;
 constexpr int kBlockTiles = kBlockPages * kBaseTile;         // 32 KB: one block of K (or V) tiles
 constexpr int kOffK = 2048;                                  // 2 x K block (after barriers and state)
 constexpr int kOffV = kOffK + 2 * kBlockTiles;               // 2 x V block
-constexpr int kResSlotBytes = kBlockPages * kResTile;        // 4 KB: one step's residual tiles
-constexpr int kVrSlotBytes = 2 * kResSlotBytes;              // v_res tiles, then tiles of ones
-constexpr int kOffVr = kOffV + 2 * kBlockTiles;              // 4 x [v_res | ones]
-constexpr int kOffKr = kOffVr + kResSlots * kVrSlotBytes;    // 4 x k_res slot
+constexpr int kResSlotBytes = kBlockPages * kResTile;        // 4 KB: one agent's residual tiles of a block
+// v_res of a block: two groups (block parity) of 5 units of 4 KB, units 0..3 for up to four
+// agents and unit 4 a constant tile of ones.  Agent a of a block of na agents sits in
+// unit 4 - na + a, so the agents and then the ones are consecutive 16-row atoms of the
+// residual-value product's A operand.
+constexpr int kVrGroupBytes = 5 * kResSlotBytes;
+constexpr int kOffVr = kOffV + 2 * kBlockTiles;              // 2 x [4 x v_res | ones]
+constexpr int kOffKr = kOffVr + 2 * kVrGroupBytes;           // 4 x k_res slot
 constexpr int kOffQ = kOffKr + kResSlots * kResSlotBytes;    // 4 agents x 2 halves x Q^T [8 rows][128 B]
 constexpr int kOffQZero = kOffQ + kMaxGroup * 2048;          // 1 KB of zeros: query-head rows 8..15
 constexpr int kOffBk = kOffQZero + 1024;                     // 4 x B_k^T [128 d][32 B]
 constexpr int kOffP = kOffBk + kMaxGroup * 4096;             // 2 x P^T [2 atoms (agents 0-1, 2-3)][128 keys][32 B]
-constexpr int kSmemBytes = kOffP + 2 * 8192 + 1024;          // + slack for aligning the base
-// The residual-value product reads 8 stacked 16-row atoms at a 4 KB stride from the slot
-// of a block's first agent: (v_res, ones) of each agent in turn.  Atoms past the agents of
-// the block (rows of the product that are never read) must still lie inside the allocation.
-static_assert(kOffVr + (kResSlots - 1) * kVrSlotBytes + 8 * kResSlotBytes <= kOffBk,
+constexpr int kSmemBytes = kOffP + 2 * 8192;                 // the dynamic window is 1024-byte aligned (checked)
+// The residual-value product reads 8 atoms from the block's first agent on; the atoms past
+// the ones tile (rows of the product that are never read) must lie inside the allocation.
+static_assert(kOffVr + kVrGroupBytes + 3 * kResSlotBytes + 8 * kResSlotBytes <= kSmemBytes,
               "value-product atoms leave the allocation");
+static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have");
 
 // tensor memory columns: U (fp32) and K (bf16 pairs) double-buffered, S double-buffered,
 // O^T [128 d x 8 agents' query heads] and the residual-value product [128 x 32]
@@ -73,13 +77,12 @@ constexpr uint32_t kTmU = 0, kTmKF = 256, kTmS = 384, kTmO = 416, kTmR = 448, kT
 
 enum {
   kKFull0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1,
-  kResFull0, kResFull1, kResFull2, kResFull3, kResEmpty0, kResEmpty1, kResEmpty2, kResEmpty3,
+  kKrFull0, kKrFull1, kKrFull2, kKrFull3, kKrEmpty0, kKrEmpty1, kKrEmpty2, kKrEmpty3,
   kUFull0, kUFull1, kUFree0, kUFree1, kKFFull0, kKFFull1, kKFFree0, kKFFree1, kSFull0, kSFull1, kSFree0, kSFree1,
   kPFull0, kPFull1, kPFree0, kPFree1, kRed0, kRed1, kODone0, kODone1, kQReady, kBkReady,
   kMmaDone, kValDone, kNumBars
 };
 static_assert(kNumBars * 8 <= 384, "barriers overlap the state that follows them");
-static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have");
 
 struct DecodeArgs {
   const uint8_t* k_base;
@@ -158,27 +161,18 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
   return it;
 }
 
-// mbarrier test by every lane, lane 0's answer for all (warp-uniform control flow).
-__device__ __forceinline__ bool warp_test(uint64_t* bar, uint32_t parity) {
-  const uint32_t r = mbar_test(bar, parity) ? 1u : 0u;
-  return __shfl_sync(0xffffffffu, r, 0) != 0;
-}
-
 // Copy the nvp (<= 8) page tiles of a block, whose ids sit in lanes 0..nvp-1 of `id`,
-// into consecutive tiles at dst: one bulk copy per run of consecutive ids, issued by
-// lane 0 after raising the byte count `bar` expects (the caller arrives once, after
-// every copy of the phase).  Only the first `rows` rows of the last page are copied
-// when rows < 16; the rest of that tile is zeroed first, since rows past every
-// sequence may never have been written and a zero probability must not meet a NaN.
-// A base tile keeps its rows in two 2048-byte halves (128 bytes a row), a residual
-// tile in one (32 bytes a row).
-__device__ __noinline__ void copy_block(const uint8_t* pool, uint8_t* dst, bool base, int32_t id, int nvp, int rows,
-                                        uint64_t* bar, int lane) {
+// into consecutive tiles at dst, completing on `bar` (whose byte count is raised here;
+// the caller arrives once, after every copy of the phase).  Consecutive ids (the usual
+// case: pages handed out in order) go as one bulk copy from lane 0, otherwise every lane
+// copies its own page.  Only the first `rows` rows of the last page are copied when
+// rows < 16; the rest of that tile is zeroed first, since rows past every sequence may
+// never have been written and a zero probability must not meet a NaN.  A base tile keeps
+// its rows in two 2048-byte halves (128 bytes a row), a residual tile in one (32 bytes).
+__device__ __forceinline__ void copy_pages(const uint8_t* pool, uint8_t* dst, bool base, int32_t id, int nvp, int rows,
+                                           uint64_t* bar, int lane) {
   const uint32_t tile = base ? kBaseTile : kResTile, rb = base ? 128u : 32u;
   const int full = rows < kPage ? nvp - 1 : nvp;  // pages copied whole
-  int32_t ids[kBlockPages];
-#pragma unroll
-  for (int pg = 0; pg < kBlockPages; ++pg) ids[pg] = __shfl_sync(0xffffffffu, id, pg);
   uint32_t bytes = full * tile;
   if (full < nvp) {
     uint8_t* t = dst + full * tile;
@@ -190,27 +184,19 @@ __device__ __noinline__ void copy_block(const uint8_t* pool, uint8_t* dst, bool 
     bytes += base ? 2 * keep : keep;
     tc::fence_proxy_async();
   }
+  const int32_t prev = __shfl_up_sync(0xffffffffu, id, 1);
+  const bool one_run = __ballot_sync(0xffffffffu, lane > 0 && lane < full && id != prev + 1) == 0;
+  if (lane == 0) mbar_expect_tx(bar, bytes);
   __syncwarp();
-  if (lane == 0) {
-    mbar_expect_tx(bar, bytes);
-    int r0 = 0;
-    int32_t start = ids[0];
-#pragma unroll
-    for (int pg = 1; pg <= kBlockPages; ++pg) {
-      if (pg <= full) {
-        const int32_t next = ids[pg < kBlockPages ? pg : kBlockPages - 1];
-        if (pg == full || next != ids[pg - 1] + 1) {
-          bulk_g2s(dst + r0 * tile, pool + (int64_t)start * tile, (pg - r0) * tile, bar);
-          r0 = pg;
-          start = next;
-        }
-      }
-    }
-    if (full < nvp && rows > 0) {
-      const uint8_t* src = pool + (int64_t)ids[full < kBlockPages ? full : 0] * tile;
-      bulk_g2s(dst + full * tile, src, rows * rb, bar);
-      if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
-    }
+  if (one_run) {
+    if (lane == 0 && full > 0) bulk_g2s(dst, pool + (int64_t)id * tile, full * tile, bar);
+  } else if (lane < full) {
+    bulk_g2s(dst + lane * tile, pool + (int64_t)id * tile, tile, bar);
+  }
+  if (full < nvp && rows > 0 && lane == full) {  // the lane holding the partial page
+    const uint8_t* src = pool + (int64_t)id * tile;
+    bulk_g2s(dst + full * tile, src, rows * rb, bar);
+    if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
   }
 }
 
@@ -259,8 +245,11 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ DecodeArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023) {  // swizzled operand tiles need a 1024-byte aligned window
+    if (threadIdx.x == 0) flag_status(a.status, kDevBadArg);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 384);
   int32_t* s_L = reinterpret_cast<int32_t*>(smem + 400);    // [4] sequence length of each agent
@@ -286,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (i == kSFree0 || i == kSFree1 || i == kPFull0 || i == kPFull1 || i == kRed0 || i == kRed1 ||
           i == kQReady)
         count = 4;  // one arrival per softmax warp
-      if (i >= kResEmpty0 && i <= kResEmpty3) count = 2;  // the U commit + the value-product commit
+
       mbar_init(&bars[i], count);
     }
     mbar_fence_init();
@@ -300,9 +289,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
   }
   if (threadIdx.x < 4 * kMaxGroup * 8) s_mref[threadIdx.x] = -INFINITY;
-  for (int i = threadIdx.x; i < kResSlots * kResSlotBytes / 16; i += kThreads) {  // the constant ones tiles
-    const int slot = i / (kResSlotBytes / 16), o = i % (kResSlotBytes / 16);
-    *reinterpret_cast<uint4*>(smem + kOffVr + slot * kVrSlotBytes + kResSlotBytes + 16 * o) =
+  for (int i = threadIdx.x; i < 2 * kResSlotBytes / 16; i += kThreads) {  // the two constant ones tiles
+    const int grp = i / (kResSlotBytes / 16), o = i % (kResSlotBytes / 16);
+    *reinterpret_cast<uint4*>(smem + kOffVr + grp * kVrGroupBytes + 4 * kResSlotBytes + 16 * o) =
         make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   }
   tc::fence_proxy_async();
@@ -314,95 +303,81 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
-    // Three in-order streams (K blocks, V blocks, residual steps); each copy is issued
-    // as soon as its buffer is free, so K of a block can land while V of the one before
-    // is still in use.  A block's page ids are fetched once, one per lane: lane p < 8
-    // the base page p, lane 8 ai + p the residual page p of agent ai.  Ids of at most two
-    // blocks are live (one register pair per block parity).
+    // Per block, in order: K tiles, each agent's k_res tiles, then V tiles and each agent's
+    // v_res tiles (released together by the block's value products).  A block's page ids
+    // are fetched once, one per lane: lane p < 8 the base page p, lane 8 a + p the residual
+    // page p of agent a.  Every wait is for the buffer's previous user, two blocks (or four
+    // k_res slots) back.
     const uint8_t* kpool = a.k_base + (int64_t)h * a.num_base_pages * kBaseTile;
     const uint8_t* vpool = a.v_base + (int64_t)h * a.num_base_pages * kBaseTile;
     int32_t Lmax = 0;  // rows at or past the longest sequence of the group are never read as data
     for (int x = 0; x < na; ++x) Lmax = max(Lmax, s_L[x]);
-    int kb = 0, vb = 0, rn = 0;
-    int32_t bid0 = 0, bid1 = 0, rid0 = 0, rid1 = 0;
-    uint32_t idle = 0;
-    while (vb < nb || rn < N) {
-      bool prog = false;
-      if (kb < nb && vb >= kb - 1 && rn >= (kb - 1) * na &&
-          (kb < 2 || warp_test(&bars[kKEmpty0 + (kb & 1)], ((kb >> 1) - 1) & 1))) {
-        const int pbase = it.p0 + kb * kBlockPages;
-        const int nvp = min(kBlockPages, it.p1 - pbase);
-        const int pg = lane & 7, ag = lane >> 3;
-        int32_t bid = 0, rid = 0;
-        if (lane < nvp) {
-          bid = a.bpt[(int64_t)it.agents[0] * a.pt_stride + pbase + lane];
-          if ((uint32_t)bid >= (uint32_t)a.num_base_pages) {
-            flag_status(a.status, kDevBadPage);
-            bid = 0;
-          }
-        }
-        if (ag < na && pg < nvp) {
-          int32_t agent = it.agents[0];
+    // page ids of block b, one per lane (base: lanes 0..7; residual of agent a: lanes 8a..8a+7),
+    // loaded a block ahead so that their latency hides behind the previous block's copies
+    auto load_ids = [&](int b, int32_t& bid, int32_t& rid) {
+      const int pbase = it.p0 + b * kBlockPages;
+      const int nvp = min(kBlockPages, it.p1 - pbase);
+      const int pg = lane & 7, ag = lane >> 3;
+      bid = rid = 0;
+      if (lane < nvp) bid = a.bpt[(int64_t)it.agents[0] * a.pt_stride + pbase + lane];
+      if (ag < na && pg < nvp) {
+        int32_t agent = it.agents[0];
 #pragma unroll
-          for (int x = 1; x < kMaxGroup; ++x)
-            if (ag == x) agent = it.agents[x];
-          rid = a.rpt[(int64_t)agent * a.pt_stride + pbase + pg];
-          if ((uint32_t)rid >= (uint32_t)a.num_res_pages) {
-            flag_status(a.status, kDevBadPage);
-            rid = 0;
-          }
+        for (int x = 1; x < kMaxGroup; ++x)
+          if (ag == x) agent = it.agents[x];
+        rid = a.rpt[(int64_t)agent * a.pt_stride + pbase + pg];
+      }
+    };
+    int kb = 0, kn = 0, vb = 0;  // blocks / k_res steps / blocks of V whose copies went out
+    int32_t bid_next = 0, rid_next = 0;
+    if (nb > 0) load_ids(0, bid_next, rid_next);
+    for (int b = 0; b < nb; ++b) {
+      const int pbase = it.p0 + b * kBlockPages;
+      const int nvp = min(kBlockPages, it.p1 - pbase);
+      int32_t bid = bid_next, rid = rid_next;
+      if (b + 1 < nb) load_ids(b + 1, bid_next, rid_next);
+      if ((uint32_t)bid >= (uint32_t)a.num_base_pages) {
+        flag_status(a.status, kDevBadPage);
+        bid = 0;
+      }
+      if ((uint32_t)rid >= (uint32_t)a.num_res_pages) {
+        flag_status(a.status, kDevBadPage);
+        rid = 0;
+      }
+      if (b >= 2 && !mbar_wait(&bars[kKEmpty0 + (b & 1)], ((b >> 1) - 1) & 1, a.status)) break;
+      copy_pages(kpool, smem + kOffK + (b & 1) * kBlockTiles, true, bid, nvp, kPage, &bars[kKFull0 + (b & 1)], lane);
+      if (lane == 0) mbar_arrive(&bars[kKFull0 + (b & 1)]);
+      kb = b + 1;
+      bool ok = true;
+      for (int x = 0; x < na; ++x) {
+        const int n = b * na + x;
+        if (n >= kResSlots && !mbar_wait(&bars[kKrEmpty0 + (n & 3)], ((n >> 2) - 1) & 1, a.status)) {
+          ok = false;
+          break;
         }
-        if (kb & 1) {
-          bid1 = bid;
-          rid1 = rid;
-        } else {
-          bid0 = bid;
-          rid0 = rid;
-        }
-        uint64_t* bar = &bars[kKFull0 + (kb & 1)];
-        copy_block(kpool, smem + kOffK + (kb & 1) * kBlockTiles, true, bid, nvp, kPage, bar, lane);
-        if (lane == 0) mbar_arrive(bar);
-        ++kb;
-        prog = true;
+        const int32_t r = __shfl_sync(0xffffffffu, rid, x * 8 + (lane & 7));
+        copy_pages(a.k_res, smem + kOffKr + (n & 3) * kResSlotBytes, false, r, nvp, kPage, &bars[kKrFull0 + (n & 3)], lane);
+        if (lane == 0) mbar_arrive(&bars[kKrFull0 + (n & 3)]);
+        kn = n + 1;
       }
-      if (vb < kb && (vb < 2 || warp_test(&bars[kVEmpty0 + (vb & 1)], ((vb >> 1) - 1) & 1))) {
-        const int pbase = it.p0 + vb * kBlockPages;
-        const int nvp = min(kBlockPages, it.p1 - pbase);
-        const int rows = min(kPage, max(0, Lmax - (pbase + nvp - 1) * kPage));  // valid rows of the last page
-        uint64_t* bar = &bars[kVFull0 + (vb & 1)];
-        copy_block(vpool, smem + kOffV + (vb & 1) * kBlockTiles, true, (vb & 1) ? bid1 : bid0, nvp, rows, bar, lane);
-        if (lane == 0) mbar_arrive(bar);
-        ++vb;
-        prog = true;
+      if (!ok) break;
+      if (b >= 2 && !mbar_wait(&bars[kVEmpty0 + (b & 1)], ((b >> 1) - 1) & 1, a.status)) break;
+      uint64_t* vbar = &bars[kVFull0 + (b & 1)];
+      const int vrows = min(kPage, max(0, Lmax - (pbase + nvp - 1) * kPage));  // valid rows of the last page
+      copy_pages(vpool, smem + kOffV + (b & 1) * kBlockTiles, true, bid, nvp, vrows, vbar, lane);
+      for (int x = 0; x < na; ++x) {
+        const int32_t r = __shfl_sync(0xffffffffu, rid, x * 8 + (lane & 7));
+        const int rows = min(kPage, max(0, s_L[x] - (pbase + nvp - 1) * kPage));
+        copy_pages(a.v_res, smem + kOffVr + (b & 1) * kVrGroupBytes + (4 - na + x) * kResSlotBytes, false, r, nvp,
+                   rows, vbar, lane);
       }
-      if (rn < N && rn / na < kb &&
-          (rn < kResSlots || warp_test(&bars[kResEmpty0 + (rn & 3)], ((rn >> 2) - 1) & 1))) {
-        const int rb = rn / na, ag = rn - rb * na;
-        const int pbase = it.p0 + rb * kBlockPages;
-        const int nvp = min(kBlockPages, it.p1 - pbase);
-        const int rows = min(kPage, max(0, s_L[ag] - (pbase + nvp - 1) * kPage));
-        const int32_t rid = __shfl_sync(0xffffffffu, (rb & 1) ? rid1 : rid0, ag * 8 + (lane & 7));
-        uint64_t* bar = &bars[kResFull0 + (rn & 3)];
-        copy_block(a.k_res, smem + kOffKr + (rn & 3) * kResSlotBytes, false, rid, nvp, kPage, bar, lane);
-        copy_block(a.v_res, smem + kOffVr + (rn & 3) * kVrSlotBytes, false, rid, nvp, rows, bar, lane);
-        if (lane == 0) mbar_arrive(bar);
-        ++rn;
-        prog = true;
-      }
-      if (prog) {
-        idle = 0;
-      } else if (++idle > kWaitLimit) {
-        if (lane == 0) flag_status(a.status, kDevTimeout);
-        break;
-      } else {
-        __nanosleep(128);  // leave the issue slots to the compute warps sharing this sub-partition
-      }
+      if (lane == 0) mbar_arrive(vbar);
+      vb = b + 1;
     }
     // never leave with copies in flight: the last phase of every barrier written to
     for (int b = max(0, kb - 2); b < kb; ++b) mbar_wait(&bars[kKFull0 + (b & 1)], (b >> 1) & 1, a.status);
     for (int b = max(0, vb - 2); b < vb; ++b) mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status);
-    for (int n = max(0, rn - kResSlots); n < rn; ++n)
-      mbar_wait(&bars[kResFull0 + (n & 3)], (n >> 2) & 1, a.status);
+    for (int n = max(0, kn - kResSlots); n < kn; ++n) mbar_wait(&bars[kKrFull0 + (n & 3)], (n >> 2) & 1, a.status);
   } else if (warp == 1) {
     // ------------------------- U and score MMA issuer -------------------------
     // Issues whichever product is ready, the score product first.  (Each MMA costs
@@ -433,14 +408,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           prog = true;
         }
         if (nu < N && (nu < 2 || mbar_test(&bars[kUFree0 + (nu & 1)], ((nu >> 1) - 1) & 1)) &&
-            mbar_test(&bars[kResFull0 + (nu & 3)], (nu >> 2) & 1)) {  // U = Kr . B_k^T
+            mbar_test(&bars[kKrFull0 + (nu & 3)], (nu >> 2) & 1)) {  // U = Kr . B_k^T
           tc::fence_after();
           const int ai = nu % na;
           tc::mma_ss(tm + kTmU + 128 * (nu & 1),
                      tc::smem_desc(sBase + kOffKr + (nu & 3) * kResSlotBytes, 16, 256, tc::kSwizzle32B),
                      tc::smem_desc(sBase + kOffBk + ai * 4096, 16, 256, tc::kSwizzle32B), idU, 0);
           tc::commit(&bars[kUFull0 + (nu & 1)]);
-          tc::commit(&bars[kResEmpty0 + (nu & 3)]);
+          tc::commit(&bars[kKrEmpty0 + (nu & 3)]);
           ++nu;
           prog = true;
         }
@@ -565,27 +540,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     // Per block, for all its agents at once (B = P^T of every agent side by side,
     // 8 columns each):
     //   O^T += Vb^T . P^T                  [128 d x 8 na]
-    //   R   += [Vr^T; 1](stacked) . P^T     [128 x 8 na]
-    // The second product's A operand stacks, per agent a, Vr^T (rows 32 a .. 32 a + 15)
-    // and a block of ones (rows 32 a + 16 .. 32 a + 31): 16-row atoms 4 KB apart, the
-    // slot layout being [v_res | ones].  Rows 32 a + r, columns 8 a + g of R hold
-    // acc_r^T[r][g] of agent a, rows 32 a + 16.. its l[g] = sum_keys P; the other cells
-    // are cross terms, never read.
+    //   R   += [Vr^T of each agent; 1] . P^T  [128 x 8 na]
+    // The second product's A operand stacks 16-row atoms 4 KB apart: Vr^T of agents
+    // 0..na-1 (rows 16 a .. 16 a + 15), then a tile of ones (rows 16 na ..).  Rows
+    // 16 a + r, columns 8 a + g of R hold acc_r^T[r][g] of agent a, and rows 16 na ..
+    // hold l[g] = sum over keys of P for every agent; the other cells are cross terms,
+    // never read.
     if (lane == 0) {
       const uint32_t nP = na > 2 ? 32 : 16;
       const uint32_t idV = tc::idesc_bf16(128, nP, 1, 1);
       const uint32_t sBase = smem_u32(smem);
       bool ok = true;
       for (int b = 0; b < nb && ok; ++b) {
-        const int n0 = b * na;
         ok = mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status) &&
              mbar_wait(&bars[kPFull0 + (b & 1)], (b >> 1) & 1, a.status);
-        for (int x = 0; x < na && ok; ++x) ok = mbar_wait(&bars[kResFull0 + ((n0 + x) & 3)], ((n0 + x) >> 2) & 1, a.status);
         if (!ok) break;
         tc::fence_after();
         const int nvp = min(kBlockPages, it.p1 - (it.p0 + b * kBlockPages));
         const uint32_t vt = sBase + kOffV + (b & 1) * kBlockTiles;
-        const uint32_t vr = sBase + kOffVr + (n0 & 3) * kVrSlotBytes;
+        const uint32_t vr = sBase + kOffVr + (b & 1) * kVrGroupBytes + (4 - na) * kResSlotBytes;
         const uint32_t pp = sBase + kOffP + (b & 1) * 8192;
         for (int ks = 0; ks < nvp; ++ks)
           tc::mma_ss(tm + kTmO, tc::smem_desc(vt + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B),
@@ -596,7 +569,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         tc::commit(&bars[kPFree0 + (b & 1)]);
         tc::commit(&bars[kODone0 + (b & 1)]);
         tc::commit(&bars[kVEmpty0 + (b & 1)]);
-        for (int x = 0; x < na; ++x) tc::commit(&bars[kResEmpty0 + ((n0 + x) & 3)]);
       }
       tc::commit(&bars[kValDone]);
       mbar_wait(&bars[kValDone], 0, a.status);
@@ -726,13 +698,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         tc::ld8(tl + kTmR + 8 * ai, rv);
         tc::wait_ld();
         const int64_t rec0 = ((int64_t)(it.slot_base + ai) * a.hkv + h) * G;
-        const int r = row - 32 * ai;  // row of this lane within agent ai's [acc_r^T ; l] rows of R
+        const int r = row - kRank * ai;  // rank held by this lane of agent ai's rows of R
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           if (g < G) {
             a.part[(rec0 + g) * kPartCols + row] = nb > 0 ? __uint_as_float(ov[g]) : 0.f;
             if (r >= 0 && r < kRank) a.part[(rec0 + g) * kPartCols + kHeadDim + r] = nb > 0 ? __uint_as_float(rv[g]) : 0.f;
-            if (r == kRank) {
+            if (row == kRank * na) {  // first row of the ones product: l
               a.ml[(rec0 + g) * 2] = nb > 0 ? mref[ai * 8 + g] : -INFINITY;
               a.ml[(rec0 + g) * 2 + 1] = nb > 0 ? __uint_as_float(rv[g]) : 0.f;
             }
