@@ -16,8 +16,9 @@
 //                   S    = K . Q^T               [128 keys x 16]   K from TMEM
 //                 whichever is ready first (U and K are double-buffered in TMEM)
 //     warps 2..9  RoPE group, one key per thread and half of the columns per
-//                 warp: K = Kb + RoPE_j(U) in fp32, written to tensor memory as
-//                 the A operand of the score product
+//                 warp: K = Kb + RoPE_j(U), the rotation of the (small) residual
+//                 term in bf16x2 and one rounding of K, written to tensor memory
+//                 as the A operand of the score product
 //     warps 10..13 softmax group, one key per thread: scores, length mask, block
 //                 maxima across the group, lazy rescale of O (only when the
 //                 running maximum grows by 2^8), P^T to shared memory, l
@@ -509,16 +510,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         for (int i2 = 0; i2 < 8; ++i2) {  // frequency group m = c/2 + i2: frequencies of d = c + 2 i2, + 1
           const uint4 w = rp[cc][(i2 >> 2) * 2 + ((i2 & 3) >> 1)];
           const uint32_t cw = (i2 & 1) ? w.z : w.x, sw = (i2 & 1) ? w.w : w.y;
-          const float c0 = bf_lo(cw), c1 = bf_hi(cw), s0 = bf_lo(sw), s1 = bf_hi(sw);
-          const float lo0 = __uint_as_float(ulo[2 * i2]), lo1 = __uint_as_float(ulo[2 * i2 + 1]);
-          const float hi0 = __uint_as_float(uhi[2 * i2]), hi1 = __uint_as_float(uhi[2 * i2 + 1]);
-          // K = Kb + RoPE_j(U) in fp32, rounded to bf16 once
-          const float kl0 = fmaf(lo0, c0, fmaf(-hi0, s0, bf_lo(klw[i2])));
-          const float kl1 = fmaf(lo1, c1, fmaf(-hi1, s1, bf_hi(klw[i2])));
-          const float kh0 = fmaf(lo0, s0, fmaf(hi0, c0, bf_lo(khw[i2])));
-          const float kh1 = fmaf(lo1, s1, fmaf(hi1, c1, bf_hi(khw[i2])));
-          olo[i2] = pack_bf16(kl0, kl1);
-          ohi[i2] = pack_bf16(kh0, kh1);
+          // the rotated residual term in bf16x2 (its roundings are at the residual's scale), then
+          // one bf16 rounding of K = Kb + RoPE_j(U)
+          const __nv_bfloat162 C = *reinterpret_cast<const __nv_bfloat162*>(&cw), S = *reinterpret_cast<const __nv_bfloat162*>(&sw);
+          const uint32_t ul = pack_bf16(__uint_as_float(ulo[2 * i2]), __uint_as_float(ulo[2 * i2 + 1]));
+          const uint32_t uh = pack_bf16(__uint_as_float(uhi[2 * i2]), __uint_as_float(uhi[2 * i2 + 1]));
+          const __nv_bfloat162 UL = *reinterpret_cast<const __nv_bfloat162*>(&ul), UH = *reinterpret_cast<const __nv_bfloat162*>(&uh);
+          const __nv_bfloat162 rl = __hfma2(__hneg2(UH), S, __hmul2(UL, C));
+          const __nv_bfloat162 rh = __hfma2(UH, C, __hmul2(UL, S));
+          const __nv_bfloat162 kl2 = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&klw[i2]), rl);
+          const __nv_bfloat162 kh2 = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&khw[i2]), rh);
+          olo[i2] = *reinterpret_cast<const uint32_t*>(&kl2);
+          ohi[i2] = *reinterpret_cast<const uint32_t*>(&kh2);
         }
         tc::st8(kf + (c >> 1), olo);       // K columns d < 64: bf16 pairs (d, d + 1) at column d / 2
         tc::st8(kf + 32 + (c >> 1), ohi);  // K columns d >= 64
