@@ -388,6 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       const uint32_t idU = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idS = tc::idesc_bf16(128, 16, 0, 0);
       const uint32_t sBase = smem_u32(smem);
+      // descriptors are built once and advanced by address (the low field counts 16-byte units)
+      const uint64_t dKr = tc::smem_desc(sBase + kOffKr, 16, 256, tc::kSwizzle32B);
+      const uint64_t dBk = tc::smem_desc(sBase + kOffBk, 16, 256, tc::kSwizzle32B);
       bool ok = mbar_wait(&bars[kQReady], 0, a.status) && mbar_wait(&bars[kBkReady], 0, a.status);
       int nu = 0, ns = 0;
       uint32_t idle = 0;
@@ -397,12 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             mbar_test(&bars[kKFFull0 + (ns & 1)], (ns >> 1) & 1)) {  // S = K . Q^T
           tc::fence_after();
           const int ai = ns % na;
+          const uint32_t q = kOffQ + ai * 2048;  // the two 64-column halves of Q^T at q, q + 1024
+          const uint64_t dq0 = tc::smem_desc(sBase + q, 16, kOffQZero - q, tc::kSwizzle128B);
+          const uint64_t dq1 = tc::smem_desc(sBase + q + 1024, 16, kOffQZero - q - 1024, tc::kSwizzle128B);
+          const uint32_t dS = tm + kTmS + 16 * (ns & 1), aK = tm + kTmKF + 64 * (ns & 1);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ts(tm + kTmS + 16 * (ns & 1), tm + kTmKF + 64 * (ns & 1) + 8 * ks,
-                       tc::smem_desc(sBase + kOffQ + ai * 2048 + (ks >> 2) * 1024 + (ks & 3) * 32, 16,
-                                     kOffQZero - (kOffQ + ai * 2048 + (ks >> 2) * 1024), tc::kSwizzle128B),
-                       idS, ks > 0);
+          for (int ks = 0; ks < 8; ++ks)  // K = 16 per step: 8 TMEM columns of A, 32 bytes of B
+            tc::mma_ts(dS, aK + 8 * ks, (ks < 4 ? dq0 : dq1) + 2 * (ks & 3), idS, ks > 0);
           tc::commit(&bars[kSFull0 + (ns & 1)]);
           tc::commit(&bars[kKFFree0 + (ns & 1)]);
           ++ns;
@@ -412,9 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
             mbar_test(&bars[kKrFull0 + (nu & 3)], (nu >> 2) & 1)) {  // U = Kr . B_k^T
           tc::fence_after();
           const int ai = nu % na;
-          tc::mma_ss(tm + kTmU + 128 * (nu & 1),
-                     tc::smem_desc(sBase + kOffKr + (nu & 3) * kResSlotBytes, 16, 256, tc::kSwizzle32B),
-                     tc::smem_desc(sBase + kOffBk + ai * 4096, 16, 256, tc::kSwizzle32B), idU, 0);
+          tc::mma_ss(tm + kTmU + 128 * (nu & 1), dKr + (nu & 3) * (kResSlotBytes >> 4), dBk + ai * (4096 >> 4), idU, 0);
           tc::commit(&bars[kUFull0 + (nu & 1)]);
           tc::commit(&bars[kKrEmpty0 + (nu & 3)]);
           ++nu;
@@ -553,6 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       const uint32_t nP = na > 2 ? 32 : 16;
       const uint32_t idV = tc::idesc_bf16(128, nP, 1, 1);
       const uint32_t sBase = smem_u32(smem);
+      const uint64_t dV = tc::smem_desc(sBase + kOffV, 2048, 1024, tc::kSwizzle128B);
+      const uint64_t dP = tc::smem_desc(sBase + kOffP, 4096, 256, tc::kSwizzle32B);
+      const uint64_t dR = tc::smem_desc(sBase + kOffVr + (4 - na) * kResSlotBytes, kResSlotBytes, 256, tc::kSwizzle32B);
       bool ok = true;
       for (int b = 0; b < nb && ok; ++b) {
         ok = mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status) &&
@@ -560,15 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         if (!ok) break;
         tc::fence_after();
         const int nvp = min(kBlockPages, it.p1 - (it.p0 + b * kBlockPages));
-        const uint32_t vt = sBase + kOffV + (b & 1) * kBlockTiles;
-        const uint32_t vr = sBase + kOffVr + (b & 1) * kVrGroupBytes + (4 - na) * kResSlotBytes;
-        const uint32_t pp = sBase + kOffP + (b & 1) * 8192;
-        for (int ks = 0; ks < nvp; ++ks)
-          tc::mma_ss(tm + kTmO, tc::smem_desc(vt + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B),
-                     tc::smem_desc(pp + ks * 512, 4096, 256, tc::kSwizzle32B), idV, (b > 0 || ks > 0));
-        for (int ks = 0; ks < nvp; ++ks)
-          tc::mma_ss(tm + kTmR, tc::smem_desc(vr + ks * kResTile, kResSlotBytes, 256, tc::kSwizzle32B),  // 8 atoms
-                     tc::smem_desc(pp + ks * 512, 4096, 256, tc::kSwizzle32B), idV, (b > 0 || ks > 0));
+        const uint64_t dv = dV + (b & 1) * (kBlockTiles >> 4), dp = dP + (b & 1) * (8192 >> 4);
+        const uint64_t dr = dR + (b & 1) * (kVrGroupBytes >> 4);  // 8 atoms of 16 rows, 4 KB apart
+        const uint32_t acc0 = b > 0;
+#pragma unroll
+        for (int ks = 0; ks < kBlockPages; ++ks)  // one page (16 keys) per step
+          if (ks < nvp) tc::mma_ss(tm + kTmO, dv + ks * (kBaseTile >> 4), dp + ks * (512 >> 4), idV, acc0 | (ks > 0));
+#pragma unroll
+        for (int ks = 0; ks < kBlockPages; ++ks)
+          if (ks < nvp) tc::mma_ss(tm + kTmR, dr + ks * (kResTile >> 4), dp + ks * (512 >> 4), idV, acc0 | (ks > 0));
         tc::commit(&bars[kPFree0 + (b & 1)]);
         tc::commit(&bars[kODone0 + (b & 1)]);
         tc::commit(&bars[kVEmpty0 + (b & 1)]);
