@@ -14,7 +14,7 @@
 //     warp 1      allocates tensor memory; one lane issues, per (block, agent):
 //                   U    = Kr . B_k^T            [128 keys x 128]  smem x smem
 //                   S    = K . Q^T               [128 keys x 16]   K from TMEM
-//                 whichever is ready first (U and K are double-buffered in TMEM)
+//                 whichever is ready first (K and S in rings of three in TMEM)
 //     warps 2..9  RoPE group, one key per thread and half of the columns per
 //                 warp: K = Kb + RoPE_j(U), the rotation of the (small) residual
 //                 term in bf16x2 and one rounding of K, written to tensor memory
@@ -72,14 +72,17 @@ static_assert(kOffVr + kVrGroupBytes + 3 * kResSlotBytes + 8 * kResSlotBytes <= 
               "value-product atoms leave the allocation");
 static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have");
 
-// tensor memory columns: U (fp32) and K (bf16 pairs) double-buffered, S double-buffered,
-// O^T [128 d x 8 agents' query heads] and the residual-value product [128 x 32]
-constexpr uint32_t kTmU = 0, kTmKF = 256, kTmS = 384, kTmO = 416, kTmR = 448, kTmCols = 512;
+// tensor memory columns: U (fp32, read out early in a step, so one buffer), K (bf16 pairs)
+// and S in rings of 3, O^T [128 d x 8 agents' query heads] and the residual-value product
+constexpr int kRing = 3;
+constexpr uint32_t kTmU = 0, kTmKF = 128, kTmS = kTmKF + 64 * kRing, kTmO = 384, kTmR = 416, kTmCols = 512;
+static_assert(kTmS + 16 * kRing <= kTmO, "tensor memory regions overlap");
 
 enum {
   kKFull0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1,
   kKrFull0, kKrFull1, kKrFull2, kKrFull3, kKrEmpty0, kKrEmpty1, kKrEmpty2, kKrEmpty3,
-  kUFull0, kUFull1, kUFree0, kUFree1, kKFFull0, kKFFull1, kKFFree0, kKFFree1, kSFull0, kSFull1, kSFree0, kSFree1,
+  kUFull, kUFree, kKFFull0, kKFFull1, kKFFull2, kKFFree0, kKFFree1, kKFFree2, kSFull0, kSFull1, kSFull2,
+  kSFree0, kSFree1, kSFree2,
   kPFull0, kPFull1, kPFree0, kPFree1, kRed0, kRed1, kODone0, kODone1, kQReady, kBkReady,
   kMmaDone, kValDone, kNumBars
 };
@@ -270,10 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;  // a single arrival: the producer's expect_tx or one MMA commit
-      if (i == kKEmpty0 || i == kKEmpty1 || i == kUFree0 || i == kUFree1 || i == kKFFull0 || i == kKFFull1 ||
-          i == kBkReady)
+      if (i == kKEmpty0 || i == kKEmpty1 || i == kUFree || (i >= kKFFull0 && i <= kKFFull2) || i == kBkReady)
         count = kRopeWarps;  // one arrival per RoPE warp
-      if (i == kSFree0 || i == kSFree1 || i == kPFull0 || i == kPFull1 || i == kRed0 || i == kRed1 ||
+      if ((i >= kSFree0 && i <= kSFree2) || i == kPFull0 || i == kPFull1 || i == kRed0 || i == kRed1 ||
           i == kQReady)
         count = 4;  // one arrival per softmax warp
 
@@ -396,28 +398,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       uint32_t idle = 0;
       while (ok && ns < N) {
         bool prog = false;
-        if (ns < nu && (ns < 2 || mbar_test(&bars[kSFree0 + (ns & 1)], ((ns >> 1) - 1) & 1)) &&
-            mbar_test(&bars[kKFFull0 + (ns & 1)], (ns >> 1) & 1)) {  // S = K . Q^T
+        const int sr = ns % kRing, sp = (ns / kRing) & 1;  // ring slot and phase parity of step ns
+        if (ns < nu && (ns < kRing || mbar_test(&bars[kSFree0 + sr], sp ^ 1)) &&
+            mbar_test(&bars[kKFFull0 + sr], sp)) {  // S = K . Q^T
           tc::fence_after();
           const int ai = ns % na;
           const uint32_t q = kOffQ + ai * 2048;  // the two 64-column halves of Q^T at q, q + 1024
           const uint64_t dq0 = tc::smem_desc(sBase + q, 16, kOffQZero - q, tc::kSwizzle128B);
           const uint64_t dq1 = tc::smem_desc(sBase + q + 1024, 16, kOffQZero - q - 1024, tc::kSwizzle128B);
-          const uint32_t dS = tm + kTmS + 16 * (ns & 1), aK = tm + kTmKF + 64 * (ns & 1);
+          const uint32_t dS = tm + kTmS + 16 * sr, aK = tm + kTmKF + 64 * sr;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // K = 16 per step: 8 TMEM columns of A, 32 bytes of B
             tc::mma_ts(dS, aK + 8 * ks, (ks < 4 ? dq0 : dq1) + 2 * (ks & 3), idS, ks > 0);
-          tc::commit(&bars[kSFull0 + (ns & 1)]);
-          tc::commit(&bars[kKFFree0 + (ns & 1)]);
+          tc::commit(&bars[kSFull0 + sr]);
+          tc::commit(&bars[kKFFree0 + sr]);
           ++ns;
           prog = true;
         }
-        if (nu < N && (nu < 2 || mbar_test(&bars[kUFree0 + (nu & 1)], ((nu >> 1) - 1) & 1)) &&
+        if (nu < N && (nu < 1 || mbar_test(&bars[kUFree], (nu - 1) & 1)) &&
             mbar_test(&bars[kKrFull0 + (nu & 3)], (nu >> 2) & 1)) {  // U = Kr . B_k^T
           tc::fence_after();
           const int ai = nu % na;
-          tc::mma_ss(tm + kTmU + 128 * (nu & 1), dKr + (nu & 3) * (kResSlotBytes >> 4), dBk + ai * (4096 >> 4), idU, 0);
-          tc::commit(&bars[kUFull0 + (nu & 1)]);
+          tc::mma_ss(tm + kTmU, dKr + (nu & 3) * (kResSlotBytes >> 4), dBk + ai * (4096 >> 4), idU, 0);
+          tc::commit(&bars[kUFull]);
           tc::commit(&bars[kKrEmpty0 + (nu & 3)]);
           ++nu;
           prog = true;
@@ -486,25 +489,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         ok = mbar_wait(&bars[kKFull0 + stage], (b >> 1) & 1, a.status);
         if (!ok) break;
       }
-      ok = mbar_wait(&bars[kUFull0 + (n & 1)], (n >> 1) & 1, a.status);
-      if (ok && n >= 2) ok = mbar_wait(&bars[kKFFree0 + (n & 1)], ((n >> 1) - 1) & 1, a.status);
+      // U of this step, read out at once (as bf16 pairs) so that the next U can go ahead
+      ok = mbar_wait(&bars[kUFull], n & 1, a.status);
       if (!ok) break;
       tc::fence_after();
+      uint32_t ul[2][8], uh[2][8];  // [chunk][pair]: U columns (c + 2 i, c + 2 i + 1) and + 64
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 32 * hf + 16 * cc;
+        uint32_t lo[16], hi[16];
+        tc::ld16(tl + kTmU + c, lo);
+        tc::ld16(tl + kTmU + 64 + c, hi);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          ul[cc][i] = pack_bf16(__uint_as_float(lo[2 * i]), __uint_as_float(lo[2 * i + 1]));
+          uh[cc][i] = pack_bf16(__uint_as_float(hi[2 * i]), __uint_as_float(hi[2 * i + 1]));
+        }
+      }
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kUFree]);
+      const int kr = n % kRing, kp = (n / kRing) & 1;
+      if (n >= kRing && !mbar_wait(&bars[kKFFree0 + kr], kp ^ 1, a.status)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
       const uint8_t* kt = smem + kOffK + stage * kBlockTiles + pg * kBaseTile;
-      const uint32_t tu = tl + kTmU + 128 * (n & 1);
-      const uint32_t kf = tl + kTmKF + 64 * (n & 1);
+      const uint32_t kf = tl + kTmKF + 64 * kr;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {  // d in [c, c + 16) and [c + 64, c + 80)
         const int c = 32 * hf + 16 * cc;
-        uint32_t ulo[16], uhi[16];
-        tc::ld16(tu + c, ulo);
-        tc::ld16(tu + 64 + c, uhi);
         uint4 kl[2], kh[2];
         kl[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c));
         kl[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 8));
         kh[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 64));
         kh[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 72));
-        tc::wait_ld();
         const uint32_t* klw = reinterpret_cast<const uint32_t*>(kl);
         const uint32_t* khw = reinterpret_cast<const uint32_t*>(kh);
         uint32_t olo[8], ohi[8];
@@ -515,9 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           // the rotated residual term in bf16x2 (its roundings are at the residual's scale), then
           // one bf16 rounding of K = Kb + RoPE_j(U)
           const __nv_bfloat162 C = *reinterpret_cast<const __nv_bfloat162*>(&cw), S = *reinterpret_cast<const __nv_bfloat162*>(&sw);
-          const uint32_t ul = pack_bf16(__uint_as_float(ulo[2 * i2]), __uint_as_float(ulo[2 * i2 + 1]));
-          const uint32_t uh = pack_bf16(__uint_as_float(uhi[2 * i2]), __uint_as_float(uhi[2 * i2 + 1]));
-          const __nv_bfloat162 UL = *reinterpret_cast<const __nv_bfloat162*>(&ul), UH = *reinterpret_cast<const __nv_bfloat162*>(&uh);
+          const __nv_bfloat162 UL = *reinterpret_cast<const __nv_bfloat162*>(&ul[cc][i2]);
+          const __nv_bfloat162 UH = *reinterpret_cast<const __nv_bfloat162*>(&uh[cc][i2]);
           const __nv_bfloat162 rl = __hfma2(__hneg2(UH), S, __hmul2(UL, C));
           const __nv_bfloat162 rh = __hfma2(UH, C, __hmul2(UL, S));
           const __nv_bfloat162 kl2 = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&klw[i2]), rl);
@@ -528,15 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         tc::st8(kf + (c >> 1), olo);       // K columns d < 64: bf16 pairs (d, d + 1) at column d / 2
         tc::st8(kf + 32 + (c >> 1), ohi);  // K columns d >= 64
       }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kUFree0 + (n & 1)]);
       tc::wait_st();
-      tc::fence_proxy_async();
       tc::fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars[kKFFull0 + (n & 1)]);
+        mbar_arrive(&bars[kKFFull0 + kr]);
         if (ai == na - 1) mbar_arrive(&bars[kKEmpty0 + stage]);
       }
     }
@@ -614,15 +630,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       const int j = pbase * kPage + row;
       const int32_t L = s_L[ai], pos = s_pos[ai];
       const bool vis = j < L && j <= pos && j < it.p1 * kPage;
-      ok = mbar_wait(&bars[kSFull0 + (n & 1)], (n >> 1) & 1, a.status);
+      const int sr = n % kRing;
+      ok = mbar_wait(&bars[kSFull0 + sr], (n / kRing) & 1, a.status);
       if (!ok) break;
       tc::fence_after();
       uint32_t sv[8];
-      tc::ld8(tl + kTmS + 16 * (n & 1), sv);
+      tc::ld8(tl + kTmS + 16 * sr, sv);
       tc::wait_ld();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kSFree0 + (n & 1)]);
+      if (lane == 0) mbar_arrive(&bars[kSFree0 + sr]);
       float sc[8], mx[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
