@@ -45,7 +45,8 @@ constexpr int kBlockPages = 8;               // 128 keys per block
 constexpr int kRopeWarps = 8;                // two per TMEM lane quadrant
 constexpr int kSoftWarp0 = 2 + kRopeWarps;   // first of the four softmax warps
 constexpr int kValueWarp = kSoftWarp0 + 4;   // issues the value products of each block
-constexpr int kThreads = (kValueWarp + 1) * 32;
+constexpr int kScoreWarp = kValueWarp + 1;   // issues the score products
+constexpr int kThreads = (kScoreWarp + 1) * 32;
 constexpr int kPartCols = kHeadDim + kRank;  // 144 floats per (slot, head, query head)
 constexpr int kResSlots = 4;
 
@@ -84,7 +85,7 @@ enum {
   kUFull, kUFree, kKFFull0, kKFFull1, kKFFull2, kKFFree0, kKFFree1, kKFFree2, kSFull0, kSFull1, kSFull2,
   kSFree0, kSFree1, kSFree2,
   kPFull0, kPFull1, kPFree0, kPFree1, kRed0, kRed1, kODone0, kODone1, kQReady, kBkReady,
-  kMmaDone, kValDone, kNumBars
+  kMmaDone, kValDone, kSDone, kNumBars
 };
 static_assert(kNumBars * 8 <= 384, "barriers overlap the state that follows them");
 
@@ -234,6 +235,26 @@ __device__ __forceinline__ float warp_reduce8(const float* v_in, int lane) {
   return v[0];
 }
 
+// Reduce four values per lane over a warp (max or sum), transposed: six shuffles, and lane l
+// ends with the reduction of value (l / 8) % 4.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce4(const float* v_in, int lane) {
+  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
+  float v[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // lanes with bit 4 set keep values 2..3
+    const bool hi = lane & 16;
+    const float keep = hi ? v_in[i + 2] : v_in[i], give = hi ? v_in[i] : v_in[i + 2];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, give, 16));
+  }
+  const bool hi = lane & 8;
+  float r = op(hi ? v[1] : v[0], __shfl_xor_sync(0xffffffffu, hi ? v[0] : v[1], 8));
+  r = op(r, __shfl_xor_sync(0xffffffffu, r, 4));
+  r = op(r, __shfl_xor_sync(0xffffffffu, r, 2));
+  r = op(r, __shfl_xor_sync(0xffffffffu, r, 1));
+  return r;
+}
+
 __device__ __forceinline__ float select8(const float* v, int i) {
   float r = v[0];
 #pragma unroll
@@ -248,6 +269,8 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// kG: query heads per KV head rounded up to 4 or 8 (the softmax works on kG score columns).
+template <int kG>
 __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023) {  // swizzled operand tiles need a 1024-byte aligned window
@@ -382,61 +405,54 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     for (int b = max(0, vb - 2); b < vb; ++b) mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status);
     for (int n = max(0, kn - kResSlots); n < kn; ++n) mbar_wait(&bars[kKrFull0 + (n & 3)], (n >> 2) & 1, a.status);
   } else if (warp == 1) {
-    // ------------------------- U and score MMA issuer -------------------------
-    // Issues whichever product is ready, the score product first.  (Each MMA costs
-    // the tensor core about the same time however small, so the value products of a
-    // block go out from a second warp, once per block for all its agents.)
+    // ------------------------------ U issuer ------------------------------
+    //   U = Kr . B_k^T   [128 keys x 128]   per (block, agent), as soon as its k_res tiles
+    //   are in and the rotation warps have read the previous U out
     if (lane == 0) {
       const uint32_t idU = tc::idesc_bf16(128, 128, 0, 0);
-      const uint32_t idS = tc::idesc_bf16(128, 16, 0, 0);
       const uint32_t sBase = smem_u32(smem);
       // descriptors are built once and advanced by address (the low field counts 16-byte units)
       const uint64_t dKr = tc::smem_desc(sBase + kOffKr, 16, 256, tc::kSwizzle32B);
       const uint64_t dBk = tc::smem_desc(sBase + kOffBk, 16, 256, tc::kSwizzle32B);
-      bool ok = mbar_wait(&bars[kQReady], 0, a.status) && mbar_wait(&bars[kBkReady], 0, a.status);
-      int nu = 0, ns = 0;
-      uint32_t idle = 0;
-      while (ok && ns < N) {
-        bool prog = false;
-        const int sr = ns % kRing, sp = (ns / kRing) & 1;  // ring slot and phase parity of step ns
-        if (ns < nu && (ns < kRing || mbar_test(&bars[kSFree0 + sr], sp ^ 1)) &&
-            mbar_test(&bars[kKFFull0 + sr], sp)) {  // S = K . Q^T
-          tc::fence_after();
-          const int ai = ns % na;
-          const uint32_t q = kOffQ + ai * 2048;  // the two 64-column halves of Q^T at q, q + 1024
-          const uint64_t dq0 = tc::smem_desc(sBase + q, 16, kOffQZero - q, tc::kSwizzle128B);
-          const uint64_t dq1 = tc::smem_desc(sBase + q + 1024, 16, kOffQZero - q - 1024, tc::kSwizzle128B);
-          const uint32_t dS = tm + kTmS + 16 * sr, aK = tm + kTmKF + 64 * sr;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // K = 16 per step: 8 TMEM columns of A, 32 bytes of B
-            tc::mma_ts(dS, aK + 8 * ks, (ks < 4 ? dq0 : dq1) + 2 * (ks & 3), idS, ks > 0);
-          tc::commit(&bars[kSFull0 + sr]);
-          tc::commit(&bars[kKFFree0 + sr]);
-          ++ns;
-          prog = true;
-        }
-        if (nu < N && (nu < 1 || mbar_test(&bars[kUFree], (nu - 1) & 1)) &&
-            mbar_test(&bars[kKrFull0 + (nu & 3)], (nu >> 2) & 1)) {  // U = Kr . B_k^T
-          tc::fence_after();
-          const int ai = nu % na;
-          tc::mma_ss(tm + kTmU, dKr + (nu & 3) * (kResSlotBytes >> 4), dBk + ai * (4096 >> 4), idU, 0);
-          tc::commit(&bars[kUFull]);
-          tc::commit(&bars[kKrEmpty0 + (nu & 3)]);
-          ++nu;
-          prog = true;
-        }
-        if (prog) {
-          idle = 0;
-        } else if (++idle > kWaitLimit) {
-          flag_status(a.status, kDevTimeout);
-          ok = false;
-        } else {
-          __nanosleep(32);
-        }
+      bool ok = mbar_wait(&bars[kBkReady], 0, a.status);
+      for (int n = 0; n < N && ok; ++n) {
+        ok = mbar_wait(&bars[kKrFull0 + (n & 3)], (n >> 2) & 1, a.status) &&
+             (n < 1 || mbar_wait(&bars[kUFree], (n - 1) & 1, a.status));
+        if (!ok) break;
+        tc::fence_after();
+        tc::mma_ss(tm + kTmU, dKr + (n & 3) * (kResSlotBytes >> 4), dBk + (n % na) * (4096 >> 4), idU, 0);
+        tc::commit(&bars[kUFull]);
+        tc::commit(&bars[kKrEmpty0 + (n & 3)]);
       }
-      // never leave with MMAs in flight
-      tc::commit(&bars[kMmaDone]);
+      tc::commit(&bars[kMmaDone]);  // never leave with MMAs in flight
       mbar_wait(&bars[kMmaDone], 0, a.status);
+    }
+    __syncwarp();
+  } else if (warp == kScoreWarp) {
+    // ------------------------------ score issuer ------------------------------
+    //   S = K . Q^T      [128 keys x 16]    K from tensor memory, per (block, agent)
+    if (lane == 0) {
+      const uint32_t idS = tc::idesc_bf16(128, 16, 0, 0);
+      const uint32_t sBase = smem_u32(smem);
+      bool ok = mbar_wait(&bars[kQReady], 0, a.status);
+      for (int n = 0; n < N && ok; ++n) {
+        const int sr = n % kRing, sp = (n / kRing) & 1;  // ring slot and phase parity of step n
+        ok = mbar_wait(&bars[kKFFull0 + sr], sp, a.status) &&
+             (n < kRing || mbar_wait(&bars[kSFree0 + sr], sp ^ 1, a.status));
+        if (!ok) break;
+        tc::fence_after();
+        const uint32_t q = kOffQ + (n % na) * 2048;  // the two 64-column halves of Q^T at q, q + 1024
+        const uint64_t dq0 = tc::smem_desc(sBase + q, 16, kOffQZero - q, tc::kSwizzle128B);
+        const uint64_t dq1 = tc::smem_desc(sBase + q + 1024, 16, kOffQZero - q - 1024, tc::kSwizzle128B);
+        const uint32_t dS = tm + kTmS + 16 * sr, aK = tm + kTmKF + 64 * sr;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // K = 16 per step: 8 TMEM columns of A, 32 bytes of B
+          tc::mma_ts(dS, aK + 8 * ks, (ks < 4 ? dq0 : dq1) + 2 * (ks & 3), idS, ks > 0);
+        tc::commit(&bars[kSFull0 + sr]);
+        tc::commit(&bars[kKFFree0 + sr]);
+      }
+      tc::commit(&bars[kSDone]);
+      mbar_wait(&bars[kSDone], 0, a.status);
     }
     __syncwarp();
   } else if (warp < kSoftWarp0) {
@@ -622,7 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[kQReady]);
 
-    const int gl = lane >> 2;  // query head whose warp-wide reductions this lane ends up holding
+    // query head whose warp-wide reductions this lane ends up holding, and the lanes that publish them
+    const int gl = kG == 8 ? lane >> 2 : lane >> 3;
+    const bool publisher = kG == 8 ? (lane & 3) == 0 : (lane & 7) == 0;
     bool ok = true;
     for (int n = 0; n < N && ok; ++n) {
       const int b = n / na, ai = n - b * na;
@@ -634,73 +652,86 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       ok = mbar_wait(&bars[kSFull0 + sr], (n / kRing) & 1, a.status);
       if (!ok) break;
       tc::fence_after();
-      uint32_t sv[8];
-      tc::ld8(tl + kTmS + 16 * sr, sv);
+      uint32_t sv[kG];
+      if constexpr (kG == 8) tc::ld8(tl + kTmS + 16 * sr, sv);
+      else tc::ld4(tl + kTmS + 16 * sr, sv);
       tc::wait_ld();
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kSFree0 + sr]);
-      float sc[8], mx[8];
+      float sc[kG];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        sc[g] = (vis && g < G) ? __uint_as_float(sv[g]) * a.scale_log2 : -INFINITY;
-        mx[g] = sc[g];
-      }
-      const float wmax = warp_reduce8<true>(mx, lane);  // max over the warp's keys of query head gl
+      for (int g = 0; g < kG; ++g) sc[g] = (vis && g < G) ? __uint_as_float(sv[g]) * a.scale_log2 : -INFINITY;
+      float wmax;  // max over the warp's keys of query head gl
+      if constexpr (kG == 8) wmax = warp_reduce8<true>(sc, lane);
+      else wmax = warp_reduce4<true>(sc, lane);
       float* red = s_red + (n & 1) * 32;
-      if ((lane & 3) == 0) red[sw_ * 8 + gl] = wmax;
+      if (publisher) red[sw_ * kG + gl] = wmax;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kRed0 + (n & 1)]);
       // while the other warps' maxima come in: probabilities against the current reference
-      float mr[8], ps[8];
+      float mr[kG], ps[kG];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
+      for (int g = 0; g < kG; ++g) {
         mr[g] = mref[ai * 8 + g];
         ps[g] = (vis && g < G) ? ex2(sc[g] - (mr[g] == -INFINITY ? 0.f : mr[g])) : 0.f;
       }
       ok = mbar_wait(&bars[kRed0 + (n & 1)], (n >> 1) & 1, a.status);
       if (!ok) break;
       // lazy rescale: keep the reference maximum unless the block maximum passes it by 2^8
-      float alpha[8];
+      float alpha[kG];
       bool need_any = false;
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const float bm = fmaxf(fmaxf(red[g], red[8 + g]), fmaxf(red[16 + g], red[24 + g]));
+      for (int g = 0; g < kG; ++g) {
+        const float bm = fmaxf(fmaxf(red[g], red[kG + g]), fmaxf(red[2 * kG + g], red[3 * kG + g]));
         const bool need = g < G && bm > mr[g] + 8.f;
         need_any |= need;
         alpha[g] = (need && mr[g] != -INFINITY) ? ex2(mr[g] - bm) : 1.f;
         if (need) mr[g] = bm;
       }
       if (need_any) {  // uniform across the group: every warp saw the same maxima
-        const float ml = select8(mr, gl);
-        __syncwarp();
-        if ((lane & 3) == 0) mref[ai * 8 + gl] = ml;
+        float ml = mr[0];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) ps[g] = (vis && g < G) ? ex2(sc[g] - mr[g]) : 0.f;
+        for (int g = 1; g < kG; ++g)
+          if (gl == g) ml = mr[g];
+        __syncwarp();
+        if (publisher) mref[ai * 8 + gl] = ml;
+#pragma unroll
+        for (int g = 0; g < kG; ++g) ps[g] = (vis && g < G) ? ex2(sc[g] - mr[g]) : 0.f;
         if (b > 0) {
           // O^T and R are stable once the value products of block b - 1 are done (one barrier
           // per block parity, so a wait is never more than one phase ahead of the barrier)
           ok = mbar_wait(&bars[kODone0 + ((b - 1) & 1)], ((b - 1) >> 1) & 1, a.status);
           if (!ok) break;
           tc::fence_after();
-          uint32_t ov[8], rv[8];
-          tc::ld8(tl + kTmO + 8 * ai, ov);
-          tc::ld8(tl + kTmR + 8 * ai, rv);
+          uint32_t ov[kG], rv[kG];
+          if constexpr (kG == 8) {
+            tc::ld8(tl + kTmO + 8 * ai, ov);
+            tc::ld8(tl + kTmR + 8 * ai, rv);
+          } else {
+            tc::ld4(tl + kTmO + 8 * ai, ov);
+            tc::ld4(tl + kTmR + 8 * ai, rv);
+          }
           tc::wait_ld();
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
+          for (int g = 0; g < kG; ++g) {
             ov[g] = __float_as_uint(__uint_as_float(ov[g]) * alpha[g]);
             rv[g] = __float_as_uint(__uint_as_float(rv[g]) * alpha[g]);
           }
-          tc::st8(tl + kTmO + 8 * ai, ov);
-          tc::st8(tl + kTmR + 8 * ai, rv);
+          if constexpr (kG == 8) {
+            tc::st8(tl + kTmO + 8 * ai, ov);
+            tc::st8(tl + kTmR + 8 * ai, rv);
+          } else {
+            tc::st4(tl + kTmO + 8 * ai, ov);
+            tc::st4(tl + kTmR + 8 * ai, rv);
+          }
           tc::wait_st();
           tc::fence_before();
         }
       }
-      uint32_t pw[4];  // P^T[key][g] in bf16, zero past G or for masked keys
+      uint32_t pw[4] = {0u, 0u, 0u, 0u};  // P^T[key][g] in bf16, zero past G or for masked keys
 #pragma unroll
-      for (int g2 = 0; g2 < 4; ++g2) pw[g2] = pack_bf16(ps[2 * g2], ps[2 * g2 + 1]);
+      for (int g2 = 0; g2 < kG / 2; ++g2) pw[g2] = pack_bf16(ps[2 * g2], ps[2 * g2 + 1]);
       if (ai == 0 && b >= 2) ok = mbar_wait(&bars[kPFree0 + (b & 1)], ((b >> 1) - 1) & 1, a.status);
       if (!ok) break;
       // P^T of agent ai: columns 8 ai .. 8 ai + 7 = atom ai / 2, 16-byte chunk ai % 2 of each row
@@ -880,7 +911,9 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(decode_split_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_split_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
@@ -920,7 +953,10 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   a.part = reinterpret_cast<float*>(ws);
   a.ml = reinterpret_cast<float*>(ws + g.partial_bytes);
   a.status = status;
-  decode_split_kernel<<<dim3(g.n_items, p.num_kv_heads), kThreads, kSmemBytes, stream>>>(a);
+  if (G <= 4)
+    decode_split_kernel<4><<<dim3(g.n_items, p.num_kv_heads), kThreads, kSmemBytes, stream>>>(a);
+  else
+    decode_split_kernel<8><<<dim3(g.n_items, p.num_kv_heads), kThreads, kSmemBytes, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
