@@ -166,42 +166,46 @@ __device__ __forceinline__ Item load_item(const DecodeArgs& a) {
   return it;
 }
 
-// Copy the nvp (<= 8) page tiles of a block, whose ids sit in lanes 0..nvp-1 of `id`,
-// into consecutive tiles at dst, completing on `bar` (whose byte count is raised here;
-// the caller arrives once, after every copy of the phase).  Consecutive ids (the usual
-// case: pages handed out in order) go as one bulk copy from lane 0, otherwise every lane
-// copies its own page.  Only the first `rows` rows of the last page are copied when
-// rows < 16; the rest of that tile is zeroed first, since rows past every sequence may
-// never have been written and a zero probability must not meet a NaN.  A base tile keeps
-// its rows in two 2048-byte halves (128 bytes a row), a residual tile in one (32 bytes).
-__device__ __forceinline__ void copy_pages(const uint8_t* pool, uint8_t* dst, bool base, int32_t id, int nvp, int rows,
-                                           uint64_t* bar, int lane) {
+// Lanes work in groups of 8: an active group copies the nvp (<= 8) page tiles of a block,
+// whose ids sit in its lanes 8 q + p, into consecutive tiles at `dst` (the group's own
+// destination), raising the byte count `bar` expects (the caller arrives).  Consecutive
+// ids go as one bulk copy from the group's first lane, otherwise every lane copies its
+// own page, so the groups of a warp issue side by side.  When rows < 16 only the first
+// rows of the last page are copied and the rest of that tile is zeroed first (rows past
+// every sequence may never have been written, and a zero probability must not meet a
+// NaN).  A base tile keeps its rows in two 2048-byte halves (128 bytes a row), a residual
+// tile in one (32 bytes a row).
+__device__ __forceinline__ void copy_group(const uint8_t* pool, bool base, int32_t id, int nvp, int rows, uint8_t* dst,
+                                          uint64_t* bar, bool active, int lane) {
+  const int p = lane & 7;
   const uint32_t tile = base ? kBaseTile : kResTile, rb = base ? 128u : 32u;
   const int full = rows < kPage ? nvp - 1 : nvp;  // pages copied whole
-  uint32_t bytes = full * tile;
-  if (full < nvp) {
+  if (active && full < nvp) {
     uint8_t* t = dst + full * tile;
     const uint32_t keep = rows * rb, half = base ? 2048u : tile;  // bytes kept per half
-    for (uint32_t o = keep + 16 * lane; o < half; o += 16 * 32) {
+    for (uint32_t o = keep + 16 * p; o < half; o += 16 * 8) {
       *reinterpret_cast<uint4*>(t + o) = make_uint4(0u, 0u, 0u, 0u);
       if (base) *reinterpret_cast<uint4*>(t + 2048 + o) = make_uint4(0u, 0u, 0u, 0u);
     }
-    bytes += base ? 2 * keep : keep;
     tc::fence_proxy_async();
   }
   const int32_t prev = __shfl_up_sync(0xffffffffu, id, 1);
-  const bool one_run = __ballot_sync(0xffffffffu, lane > 0 && lane < full && id != prev + 1) == 0;
-  if (lane == 0) mbar_expect_tx(bar, bytes);
+  const uint32_t breaks = __ballot_sync(0xffffffffu, active && p > 0 && p < full && id != prev + 1);
+  const bool one_run = ((breaks >> (lane & ~7)) & 0xffu) == 0;
+  if (active && p == 0)
+    mbar_expect_tx(bar, full * tile + (full < nvp && rows > 0 ? (base ? 2u : 1u) * rows * rb : 0u));
   __syncwarp();
-  if (one_run) {
-    if (lane == 0 && full > 0) bulk_g2s(dst, pool + (int64_t)id * tile, full * tile, bar);
-  } else if (lane < full) {
-    bulk_g2s(dst + lane * tile, pool + (int64_t)id * tile, tile, bar);
-  }
-  if (full < nvp && rows > 0 && lane == full) {  // the lane holding the partial page
-    const uint8_t* src = pool + (int64_t)id * tile;
-    bulk_g2s(dst + full * tile, src, rows * rb, bar);
-    if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
+  if (active) {
+    if (one_run) {
+      if (p == 0 && full > 0) bulk_g2s(dst, pool + (int64_t)id * tile, full * tile, bar);
+    } else if (p < full) {
+      bulk_g2s(dst + p * tile, pool + (int64_t)id * tile, tile, bar);
+    }
+    if (full < nvp && rows > 0 && p == full) {  // the lane holding the partial page
+      const uint8_t* src = pool + (int64_t)id * tile;
+      bulk_g2s(dst + full * tile, src, rows * rb, bar);
+      if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
+    }
   }
 }
 
@@ -252,14 +256,6 @@ __device__ __forceinline__ float warp_reduce4(const float* v_in, int lane) {
   r = op(r, __shfl_xor_sync(0xffffffffu, r, 4));
   r = op(r, __shfl_xor_sync(0xffffffffu, r, 2));
   r = op(r, __shfl_xor_sync(0xffffffffu, r, 1));
-  return r;
-}
-
-__device__ __forceinline__ float select8(const float* v, int i) {
-  float r = v[0];
-#pragma unroll
-  for (int k = 1; k < 8; ++k)
-    if (i == k) r = v[k];
   return r;
 }
 
@@ -370,33 +366,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         flag_status(a.status, kDevBadPage);
         rid = 0;
       }
+      const int pg = lane & 7, ag = lane >> 3;
+      const bool res_lane = ag < na;  // lanes of the agents' residual groups
+      // K tiles
       if (b >= 2 && !mbar_wait(&bars[kKEmpty0 + (b & 1)], ((b >> 1) - 1) & 1, a.status)) break;
-      copy_pages(kpool, smem + kOffK + (b & 1) * kBlockTiles, true, bid, nvp, kPage, &bars[kKFull0 + (b & 1)], lane);
+      copy_group(kpool, true, bid, nvp, kPage, smem + kOffK + (b & 1) * kBlockTiles, &bars[kKFull0 + (b & 1)],
+                 lane < kBlockPages, lane);
+      __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kKFull0 + (b & 1)]);
       kb = b + 1;
+      // every agent's k_res tiles, one k_res slot (and barrier) per (block, agent) step
       bool ok = true;
-      for (int x = 0; x < na; ++x) {
+      for (int x = 0; x < na && ok; ++x) {
         const int n = b * na + x;
-        if (n >= kResSlots && !mbar_wait(&bars[kKrEmpty0 + (n & 3)], ((n >> 2) - 1) & 1, a.status)) {
-          ok = false;
-          break;
-        }
-        const int32_t r = __shfl_sync(0xffffffffu, rid, x * 8 + (lane & 7));
-        copy_pages(a.k_res, smem + kOffKr + (n & 3) * kResSlotBytes, false, r, nvp, kPage, &bars[kKrFull0 + (n & 3)], lane);
-        if (lane == 0) mbar_arrive(&bars[kKrFull0 + (n & 3)]);
-        kn = n + 1;
+        if (n >= kResSlots) ok = mbar_wait(&bars[kKrEmpty0 + (n & 3)], ((n >> 2) - 1) & 1, a.status);
       }
       if (!ok) break;
+      const int kslot = (b * na + ag) & 3;
+      copy_group(a.k_res, false, rid, nvp, kPage, smem + kOffKr + kslot * kResSlotBytes, &bars[kKrFull0 + kslot],
+                 res_lane, lane);
+      __syncwarp();
+      if (res_lane && pg == 0) mbar_arrive(&bars[kKrFull0 + kslot]);
+      kn = b * na + na;
+      // V tiles and every agent's v_res tiles, on one barrier (released by the block's value products)
       if (b >= 2 && !mbar_wait(&bars[kVEmpty0 + (b & 1)], ((b >> 1) - 1) & 1, a.status)) break;
       uint64_t* vbar = &bars[kVFull0 + (b & 1)];
-      const int vrows = min(kPage, max(0, Lmax - (pbase + nvp - 1) * kPage));  // valid rows of the last page
-      copy_pages(vpool, smem + kOffV + (b & 1) * kBlockTiles, true, bid, nvp, vrows, vbar, lane);
-      for (int x = 0; x < na; ++x) {
-        const int32_t r = __shfl_sync(0xffffffffu, rid, x * 8 + (lane & 7));
-        const int rows = min(kPage, max(0, s_L[x] - (pbase + nvp - 1) * kPage));
-        copy_pages(a.v_res, smem + kOffVr + (b & 1) * kVrGroupBytes + (4 - na + x) * kResSlotBytes, false, r, nvp,
-                   rows, vbar, lane);
-      }
+      const int last = (pbase + nvp - 1) * kPage;  // first key of the block's last page
+      copy_group(vpool, true, bid, nvp, min(kPage, max(0, Lmax - last)), smem + kOffV + (b & 1) * kBlockTiles, vbar,
+                 lane < kBlockPages, lane);
+      const int32_t Lx = res_lane ? s_L[ag] : 0;
+      copy_group(a.v_res, false, rid, nvp, min(kPage, max(0, Lx - last)),
+                 smem + kOffVr + (b & 1) * kVrGroupBytes + (4 - na + ag) * kResSlotBytes, vbar, res_lane, lane);
+      __syncwarp();
       if (lane == 0) mbar_arrive(vbar);
       vb = b + 1;
     }
