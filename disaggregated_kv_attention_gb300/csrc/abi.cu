@@ -75,7 +75,7 @@ int32_t check_attn(const forkkv_attn_params* p, bool decode) {
     return FORKKV_ERR_INVALID_ARG;
   }
   if (p->plan) {
-    if (!decode || p->plan_items < 1 || p->plan_slots < 1) return FORKKV_ERR_INVALID_ARG;
+    if (!decode || p->plan_items < 1 || p->plan_slots < 1 || p->plan_ctas < 1) return FORKKV_ERR_INVALID_ARG;
   }
   return FORKKV_OK;
 }

@@ -25,7 +25,7 @@ cudaError_t launch_rope_table(const uint32_t* turns_hi_lo, int32_t n_positions, 
 
 // Decode: partial-result workspace geometry.
 struct DecodeGeometry {
-  int32_t n_items;        // CTAs per KV head
+  int32_t n_items;        // work items (a unit per item and KV head)
   int32_t n_slots;        // partial slots
   int32_t chunk_pages;    // no-plan mode: pages per item
   int32_t chunks;         // no-plan mode: items per agent

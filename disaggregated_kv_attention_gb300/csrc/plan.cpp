@@ -10,8 +10,12 @@
 // is then cut into items of at most 4 agents and a bounded number of 128-key
 // blocks (8 pages).
 #include <algorithm>
+#include <array>
+#include <climits>
 #include <cstdint>
+#include <functional>
 #include <map>
+#include <queue>
 #include <vector>
 
 #include "../../include/forkkv.h"
@@ -34,7 +38,7 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
                    forkkv_plan_info* info) {
   if (!bpt || !seq_lens || !info || n_agents < 1 || pt_stride < 1 || num_kv_heads < 1 || target_ctas < 0)
     return FORKKV_ERR_INVALID_ARG;
-  if (target_ctas == 0) target_ctas = 152;  // one CTA per SM, one wave
+  if (target_ctas == 0) target_ctas = 152;  // one persistent CTA per SM
   std::vector<int32_t> npages(n_agents);
   for (int32_t a = 0; a < n_agents; ++a) {
     if (seq_lens[a] < 1) return FORKKV_ERR_INVALID_ARG;
@@ -108,51 +112,106 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
     }
   }
 
-  // 3. the largest stage cap T whose item count still reaches target_ctas / Hkv
-  const int64_t want = std::max<int64_t>(1, (target_ctas + num_kv_heads - 1) / num_kv_heads);
+  // 3. a stage cap T per item (chunks are cut into near-equal items of at most T blocks)
+  //    and a spread of the (item, head) units over the CTAs.  A unit's cost is counted in
+  //    pipeline steps: one per (block, agent), about one more per block for its shared
+  //    value products and base tiles, and about two for starting the unit and writing its
+  //    partials.  Units go largest first to the least loaded CTA (LPT); T is the cap whose
+  //    spread ends soonest, the larger one on ties (fewer partials to merge).
+  const int32_t C_max = target_ctas;
   int32_t max_stages = 1;
   for (const Chunk& c : chunks) max_stages = std::max(max_stages, c.stages);
-  auto count = [&](int32_t T) {
-    int64_t n = 0;
-    for (const Chunk& c : chunks) n += (c.stages + T - 1) / T;
-    return n;
+  auto unit_cost = [](int32_t blocks, int32_t na) { return (int64_t)blocks * (na + 1) + 2; };
+  struct Unit {
+    int64_t cost;
+    int32_t code;
   };
-  int32_t lo = 1, hi = max_stages;
-  while (lo < hi) {  // largest T with count(T) >= want
-    const int32_t mid = lo + (hi - lo + 1) / 2;
-    if (count(mid) >= want)
-      lo = mid;
-    else
-      hi = mid - 1;
+  // items of cap T: (chunk index, first stage, end stage)
+  auto make_items = [&](int32_t T, std::vector<std::array<int32_t, 3>>& out) {
+    out.clear();
+    for (size_t ci = 0; ci < chunks.size(); ++ci) {
+      const Chunk& c = chunks[ci];
+      const int32_t parts = (c.stages + T - 1) / T;
+      for (int32_t k = 0; k < parts; ++k)
+        out.push_back({(int32_t)ci, (int32_t)((int64_t)c.stages * k / parts),
+                       (int32_t)((int64_t)c.stages * (k + 1) / parts)});
+    }
+  };
+  // LPT spread of the units of `its` over at most C_max CTAs; returns the makespan
+  auto spread = [&](const std::vector<std::array<int32_t, 3>>& its, std::vector<std::vector<int32_t>>* lists) {
+    std::vector<Unit> units;
+    units.reserve(its.size() * num_kv_heads);
+    for (size_t i = 0; i < its.size(); ++i) {
+      const int64_t cost = unit_cost(its[i][2] - its[i][1], chunks[its[i][0]].na);
+      for (int32_t h = 0; h < num_kv_heads; ++h) units.push_back({cost, (int32_t)(i * num_kv_heads + h)});
+    }
+    std::stable_sort(units.begin(), units.end(), [](const Unit& x, const Unit& y) { return x.cost > y.cost; });
+    const int32_t C = (int32_t)std::min<int64_t>(C_max, (int64_t)units.size());
+    using Load = std::pair<int64_t, int32_t>;  // (load, CTA): the least loaded, then the lowest index
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int32_t c = 0; c < C; ++c) heap.push({0, c});
+    if (lists) lists->assign(C, {});
+    int64_t makespan = 0;
+    for (const Unit& u : units) {
+      Load l = heap.top();
+      heap.pop();
+      l.first += u.cost;
+      makespan = std::max(makespan, l.first);
+      if (lists) (*lists)[l.second].push_back(u.code);
+      heap.push(l);
+    }
+    return makespan;
+  };
+  // caps from the longest chunk down, while the units stay within 16 per CTA; a cap that
+  // cuts every chunk into as many items as the previous one makes the same items
+  std::vector<std::array<int32_t, 3>> its;
+  int32_t T = max_stages;
+  int64_t best = -1, last_count = -1;
+  for (int32_t t = max_stages; t >= 1; --t) {
+    int64_t count = 0;
+    for (const Chunk& c : chunks) count += (c.stages + t - 1) / t;
+    if (count == last_count) continue;
+    last_count = count;
+    if (t < max_stages && count * num_kv_heads > 16 * (int64_t)C_max) break;
+    make_items(t, its);
+    const int64_t m = spread(its, nullptr);
+    if (best < 0 || m < best) {
+      best = m;
+      T = t;
+    }
   }
-  const int32_t T = lo;
+  make_items(T, its);
+  std::vector<std::vector<int32_t>> lists;
+  spread(its, &lists);
 
-  // 4. items (near-equal stage counts per chunk), slots and the per-agent slot lists
+  // 4. items, slots, the per-agent slot lists and the CTAs' unit lists
   std::vector<int32_t> items;
   std::vector<std::vector<int32_t>> agent_slots(n_agents);
   int32_t n_items = 0, n_slots = 0;
-  for (const Chunk& c : chunks) {
+  for (const auto& itm : its) {
+    const Chunk& c = chunks[itm[0]];
     const int32_t wpp = pages_per_stage(c.na);
-    const int32_t parts = (c.stages + T - 1) / T;
-    for (int32_t k = 0; k < parts; ++k) {
-      const int32_t s0 = (int32_t)((int64_t)c.stages * k / parts), s1 = (int32_t)((int64_t)c.stages * (k + 1) / parts);
-      const int32_t p0 = c.p0 + s0 * wpp, p1 = std::min(c.p1, c.p0 + s1 * wpp);
-      int32_t rec[FORKKV_PLAN_ITEM_INTS] = {0};
-      rec[0] = p0;
-      rec[1] = p1;
-      rec[2] = c.na;
-      rec[3] = wpp;
-      for (int32_t x = 0; x < 8; ++x) rec[4 + x] = x < c.na ? c.agents[x] : c.agents[0];
-      rec[12] = n_slots;
-      items.insert(items.end(), rec, rec + FORKKV_PLAN_ITEM_INTS);
-      for (int32_t x = 0; x < c.na; ++x) agent_slots[c.agents[x]].push_back(n_slots + x);
-      n_slots += c.na;
-      ++n_items;
-    }
+    const int32_t p0 = c.p0 + itm[1] * wpp, p1 = std::min(c.p1, c.p0 + itm[2] * wpp);
+    int32_t rec[FORKKV_PLAN_ITEM_INTS] = {0};
+    rec[0] = p0;
+    rec[1] = p1;
+    rec[2] = c.na;
+    rec[3] = wpp;
+    for (int32_t x = 0; x < 8; ++x) rec[4 + x] = x < c.na ? c.agents[x] : c.agents[0];
+    rec[12] = n_slots;
+    items.insert(items.end(), rec, rec + FORKKV_PLAN_ITEM_INTS);
+    for (int32_t x = 0; x < c.na; ++x) agent_slots[c.agents[x]].push_back(n_slots + x);
+    n_slots += c.na;
+    ++n_items;
   }
-  const int64_t need = (int64_t)items.size() + n_agents + 1 + n_slots;
+  const int32_t n_ctas = (int32_t)lists.size();
+  const int64_t n_units = (int64_t)n_items * num_kv_heads;
+  const int64_t need = (int64_t)items.size() + n_agents + 1 + n_slots + n_ctas + 1 + n_units;
+  if (need > INT32_MAX) return FORKKV_ERR_INVALID_ARG;
   info->n_items = n_items;
   info->n_slots = n_slots;
+  info->n_ctas = n_ctas;
+  info->n_units = (int32_t)n_units;
   info->plan_ints = (int32_t)need;
   if (!plan) return FORKKV_OK;  // size query
   if (need > plan_cap_ints) return FORKKV_ERR_INVALID_ARG;
@@ -165,6 +224,14 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
     for (int32_t s : agent_slots[a]) sl[k++] = s;
   }
   off[n_agents] = k;
+  int32_t* cta_off = sl + n_slots;
+  int32_t* units = cta_off + n_ctas + 1;
+  k = 0;
+  for (int32_t c = 0; c < n_ctas; ++c) {
+    cta_off[c] = k;
+    for (int32_t u : lists[c]) units[k++] = u;
+  }
+  cta_off[n_ctas] = k;
   return FORKKV_OK;
 }
 

@@ -56,7 +56,8 @@ class forkkv_pool_desc(ctypes.Structure):
 
 
 class forkkv_plan_info(ctypes.Structure):
-    _fields_ = [("n_items", ctypes.c_int32), ("n_slots", ctypes.c_int32), ("plan_ints", ctypes.c_int32)]
+    _fields_ = [("n_items", ctypes.c_int32), ("n_slots", ctypes.c_int32), ("n_ctas", ctypes.c_int32),
+                ("n_units", ctypes.c_int32), ("plan_ints", ctypes.c_int32)]
 
 
 class forkkv_attn_params(ctypes.Structure):
@@ -70,6 +71,7 @@ class forkkv_attn_params(ctypes.Structure):
         ("adapter_ids", ctypes.c_void_p), ("n_adapters", ctypes.c_int32), ("rope_table", ctypes.c_void_p),
         ("rope_table_positions", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("sm_scale", ctypes.c_float),
         ("plan", ctypes.c_void_p), ("plan_items", ctypes.c_int32), ("plan_slots", ctypes.c_int32),
+        ("plan_ctas", ctypes.c_int32),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
@@ -295,6 +297,7 @@ def attn_params(pools: Pools, layer: int, q: torch.Tensor, out: torch.Tensor, bp
     p.sm_scale = sm_scale
     if plan is not None:
         p.plan, p.plan_items, p.plan_slots = plan.data_ptr(), plan_info.n_items, plan_info.n_slots
+        p.plan_ctas = plan_info.n_ctas
     return p
 
 

@@ -207,19 +207,27 @@ int32_t forkkv_rope_table_build(double rope_theta, int32_t n_positions, void* ta
 /* ==== decode work plan =====================================================
  * Splits the key ranges of a decode batch into work items so that pages
  * shared by several agents (a fork tree's trunks) are read once per group of
- * up to 4 agents.  Built on the host from host copies of the page tables.
- * Item i is FORKKV_PLAN_ITEM_INTS int32:
- *   [0] first logical page  [1] end logical page   [2] n_agents (1, 2 or 4)
- *   [3] pages per stage (8)  [4..11] agent indices (slots past n_agents repeat
- *   the first)               [12] first partial slot
- * followed by the per-agent slot lists (CSR: n_agents+1 offsets, then slots). */
+ * up to 4 agents, and deals the (item, KV head) units over persistent CTAs so
+ * that their estimated costs balance.  Built on the host from host copies of
+ * the page tables.  Layout, all int32:
+ *   items      n_items records of FORKKV_PLAN_ITEM_INTS:
+ *              [0] first logical page  [1] end logical page  [2] n_agents (1, 2
+ *              or 4)  [3] pages per stage (8)  [4..11] agent indices (slots past
+ *              n_agents repeat the first)  [12] first partial slot
+ *   slot CSR   n_agents + 1 offsets, then n_slots slots (each agent's partials)
+ *   cta_off    n_ctas + 1 offsets into units
+ *   units      n_units codes item * num_kv_heads + head, CTA c taking
+ *              units[cta_off[c] .. cta_off[c + 1]) in that order */
 typedef struct {
-  int32_t n_items;     /* CTAs per KV head */
+  int32_t n_items;     /* work items */
   int32_t n_slots;     /* partial-result slots */
+  int32_t n_ctas;      /* CTAs of the decode kernel (grid size) */
+  int32_t n_units;     /* n_items * num_kv_heads */
   int32_t plan_ints;   /* int32 words written to plan */
 } forkkv_plan_info;
 
-/* target_ctas: desired CTAs over all KV heads (0 = one per SM of a GB300). */
+/* target_ctas: CTAs to spread the units over (0 = one per SM of a GB300); the
+ * plan uses at most that many. */
 int32_t forkkv_plan_build(const int32_t* bpt_host, const int32_t* seq_lens_host, int32_t n_agents,
                           int32_t pt_stride, int32_t num_kv_heads, int32_t target_ctas,
                           int32_t* plan, int32_t plan_cap_ints, forkkv_plan_info* info);
@@ -252,8 +260,9 @@ typedef struct {
   double rope_theta;       /* used when rope_table is NULL */
   float sm_scale;          /* 0 -> 1/sqrt(128) */
   const int32_t* plan;     /* device copy of a forkkv_plan_build plan, or NULL (decode only) */
-  int32_t plan_items;
+  int32_t plan_items;      /* the plan's n_items, n_slots and n_ctas */
   int32_t plan_slots;
+  int32_t plan_ctas;
   void* workspace;         /* device scratch, >= the *_workspace_size bytes, 256-byte aligned */
   size_t workspace_bytes;
 } forkkv_attn_params;

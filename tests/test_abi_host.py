@@ -200,8 +200,18 @@ def test_plan_covers_every_page_once(shape, target):
     plan, info = fk.forkkv_plan_build(bpt, lens, hkv, target)
     items = plan[:info.n_items * fk.PLAN_ITEM_INTS].reshape(info.n_items, fk.PLAN_ITEM_INTS)
     off = plan[info.n_items * fk.PLAN_ITEM_INTS:][:A + 1]
-    slots = plan[info.n_items * fk.PLAN_ITEM_INTS + A + 1:]
-    assert info.plan_ints == plan.size and len(slots) == info.n_slots
+    rest = plan[info.n_items * fk.PLAN_ITEM_INTS + A + 1:]
+    slots, rest = rest[:info.n_slots], rest[info.n_slots:]
+    cta_off, units = rest[:info.n_ctas + 1], rest[info.n_ctas + 1:]
+    assert info.plan_ints == plan.size and len(units) == info.n_units == info.n_items * hkv
+    # the schedule: at most target (152 for 0) CTAs, none idle, every (item, head) unit once
+    assert 1 <= info.n_ctas <= (target or 152)
+    assert cta_off[0] == 0 and cta_off[-1] == info.n_units and np.all(np.diff(cta_off) >= 1)
+    assert sorted(units.tolist()) == list(range(info.n_units))
+    # greedy list scheduling bound: no CTA ends later than the mean load plus one unit
+    cost = np.array([((it[1] - it[0] + 7) // 8) * (it[2] + 1) + 2 for it in items]).repeat(hkv)
+    loads = np.array([cost[units[cta_off[c]:cta_off[c + 1]]].sum() for c in range(info.n_ctas)])
+    assert loads.max() <= cost.sum() / info.n_ctas + cost.max()
     cover = {}
     slot_owner = {}
     for i, it in enumerate(items):
