@@ -81,18 +81,19 @@ static_assert(kOffVr + kVrGroupBytes + 3 * kResSlotBytes + 8 * kResSlotBytes <= 
               "value-product atoms leave the allocation");
 static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have");
 
-// tensor memory columns: U (fp32, read out early in a step, so one buffer), K (bf16 pairs)
-// and S in rings of 3, O^T [128 d x 8 agents' query heads] and the residual-value product
-constexpr int kRing = 3;
-constexpr uint32_t kTmU = 0, kTmKF = 128, kTmS = kTmKF + 64 * kRing, kTmO = 384, kTmR = 416, kTmCols = 512;
-static_assert(kTmS + 16 * kRing <= kTmO, "tensor memory regions overlap");
+// tensor memory columns: U (fp32) in two buffers, so that the next step's U is computed
+// while the rotation warps read this one; K (bf16 pairs) in a ring of 2 and S in a ring of
+// 3; O^T [128 d x 8 agents' query heads] and the residual-value product
+constexpr int kKfRing = 2, kSRing = 3;
+constexpr uint32_t kTmU = 0, kTmKF = 256, kTmS = kTmKF + 64 * kKfRing, kTmO = 448, kTmR = 480, kTmCols = 512;
+static_assert(kTmS + 16 * kSRing <= kTmO && kTmR + 32 <= kTmCols, "tensor memory regions overlap");
 
 enum {
   kKFull0, kKFull1, kVFull0, kVFull1, kKEmpty0, kKEmpty1, kVEmpty0, kVEmpty1,
   kKrFull0, kKrFull1, kKrFull2, kKrFull3, kKrEmpty0, kKrEmpty1, kKrEmpty2, kKrEmpty3,
-  kUFull, kUFree, kKFFull0, kKFFull1, kKFFull2, kKFFree0, kKFFree1, kKFFree2, kSFull0, kSFull1, kSFull2,
+  kUFull0, kUFull1, kUFree0, kUFree1, kKFFull0, kKFFull1, kKFFree0, kKFFree1, kSFull0, kSFull1, kSFull2,
   kSFree0, kSFree1, kSFree2,
-  kPFull0, kPFull1, kPFree0, kPFree1, kRed0, kRed1, kODone0, kODone1, kUUnit, kSUnit, kEpiDone,
+  kPFull0, kPFull1, kPFree0, kPFree1, kRed0, kRed1, kODone0, kODone1, kUUnit, kSUnit, kEpiDone, kUnitReady0, kUnitReady1, kUnitFree0, kUnitFree1,
   kMmaDone, kValDone, kSDone, kNumBars
 };
 static_assert(kNumBars * 8 <= 384, "barriers overlap the state that follows them");
@@ -115,10 +116,8 @@ struct DecodeArgs {
   const uint8_t* rope;
   int32_t rope_positions;
   float scale_log2;
-  const int32_t* plan;     // items (FORKKV_PLAN_ITEM_INTS each), or null: one item per (agent, chunk)
-  const int32_t* cta_off;  // plan mode: [n_ctas + 1] into units
-  const int32_t* units;    // plan mode: item * hkv + head, grouped by CTA
-  int32_t n_items, n_ctas;
+  const int32_t* units;  // plan's unit records (FORKKV_PLAN_UNIT_INTS each), or null: units by formula
+  int32_t n_units;       // plan: records; no plan: n_items * hkv
   int32_t chunk_pages, chunks;
   int32_t n_agents, max_seq_len, n_slots;
   float* part;
@@ -126,143 +125,163 @@ struct DecodeArgs {
   uint32_t* status;
 };
 
-// One unit of work: an item (a page range walked by a group of agents) for one KV head.
-struct Unit {
-  int32_t p0, p1, na, slot_base, h;
-  int32_t agents[kMaxGroup];
-  __device__ __forceinline__ int blocks() const { return (p1 - p0 + kBlockPages - 1) / kBlockPages; }
-  __device__ __forceinline__ int32_t agent(int x) const {
-    int32_t r = agents[0];
-#pragma unroll
-    for (int i = 1; i < kMaxGroup; ++i)
-      if (x == i) r = agents[i];
-    return r;
-  }
+// A unit of work is an item (a page range walked by a group of agents) for one KV head.  The
+// producer warp describes each unit of its CTA, in order, in a ring of two descriptors in
+// shared memory (kUnitInts int32 each, one field per lane when built) that the other warps
+// read at the start of the unit.
+constexpr int kUnitInts = 24;
+enum {
+  kUfP0, kUfP1, kUfNa, kUfH, kUfSlot, kUfEnd,  // page range, agents, KV head, first slot, end of list
+  kUfAgent = 6, kUfL = 10, kUfPos = 14, kUfAdapter = 18  // per agent (4 each): index, keys, position, adapter
 };
+constexpr int kOffUnits = 1408;  // 2 x kUnitInts int32 in the header of shared memory
+static_assert(kOffUnits + 2 * kUnitInts * 4 <= 2048, "unit ring overlaps the operand tiles");
 
-// Units of this CTA: [*first, *first + *count) of the plan's unit list, or every gridDim.x-th
-// (agent chunk, head) pair without a plan.
-__device__ __forceinline__ void cta_units(const DecodeArgs& a, int& first, int& count) {
-  if (a.plan) {
-    first = a.cta_off[blockIdx.x];
-    count = a.cta_off[blockIdx.x + 1] - first;
-    if (first < 0 || count < 0 || first + count > a.cta_off[a.n_ctas]) {
-      flag_status(a.status, kDevBadArg);
-      first = count = 0;
+// The first unit of this CTA: plan record blockIdx.x, or unit code blockIdx.x (-1: none).
+__device__ __forceinline__ int32_t first_unit(const DecodeArgs& a) {
+  return (int32_t)blockIdx.x < a.n_units ? (int32_t)blockIdx.x : -1;
+}
+
+// Raw material of unit r, one int per lane: the plan record's words, or without a plan the
+// unit agent's sequence length (lane 0), from which its chunk bounds follow.
+__device__ __forceinline__ int32_t unit_raw(const DecodeArgs& a, int32_t r, int lane) {
+  if (r < 0) return 0;
+  if (a.units) return lane < FORKKV_PLAN_UNIT_INTS ? __ldg(a.units + (int64_t)r * FORKKV_PLAN_UNIT_INTS + lane) : 0;
+  const int32_t agent = r / a.hkv / a.chunks;
+  return lane == 0 ? __ldg(a.seq_lens + agent) : 0;
+}
+
+// Field `lane` of unit r's descriptor (lanes >= kUnitInts: 0) and, in `next`, the CTA's unit
+// after it (-1: none).  Every lane checks the whole record (an invalid unit becomes empty and
+// raises kDevBadArg); lanes of the per-agent fields issue their loads here and do not wait.
+__device__ __forceinline__ int32_t unit_field(const DecodeArgs& a, int32_t r, int32_t raw, int lane, int32_t& next) {
+  if (r < 0) {
+    next = -1;
+    return lane == kUfEnd ? 1 : 0;
+  }
+  int32_t p0, p1, na, h, slot, ag[kMaxGroup];
+  if (a.units) {
+    p0 = __shfl_sync(0xffffffffu, raw, 0);
+    p1 = __shfl_sync(0xffffffffu, raw, 1);
+    na = __shfl_sync(0xffffffffu, raw, 2);
+    h = __shfl_sync(0xffffffffu, raw, 3);
+    slot = __shfl_sync(0xffffffffu, raw, 4);
+    next = __shfl_sync(0xffffffffu, raw, 5);
+#pragma unroll
+    for (int x = 0; x < kMaxGroup; ++x) ag[x] = __shfl_sync(0xffffffffu, raw, 6 + x);
+    bool bad = false;
+    if (na != 1 && na != 2 && na != 4) {  // the value products stack the slots of 1, 2 or 4 agents
+      bad = true;
+      na = 1;
+    }
+    if (slot < 0 || slot + na > a.n_slots) {
+      bad = true;
+      slot = -1;  // empty: reads nothing, writes nothing
+    }
+    if (next != -1 && (next <= r || next >= a.n_units)) {  // links only go forward
+      bad = true;
+      next = -1;
+    }
+    if (bad) {
+      if (lane == 0) flag_status(a.status, kDevBadArg);
+      p1 = p0;
     }
   } else {
-    const int total = a.n_items * a.hkv;
-    first = blockIdx.x;
-    count = blockIdx.x < total ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int32_t item = r / a.hkv, agent = item / a.chunks, c = item % a.chunks;
+    h = r - item * a.hkv;
+    const int32_t L = min(__shfl_sync(0xffffffffu, raw, 0), a.max_seq_len);
+    p0 = c * a.chunk_pages;
+    p1 = min(p0 + a.chunk_pages, (L + kPage - 1) / kPage);
+    na = 1;
+    slot = item;
+#pragma unroll
+    for (int x = 0; x < kMaxGroup; ++x) ag[x] = agent;
+    next = r + (int32_t)gridDim.x < a.n_units ? r + (int32_t)gridDim.x : -1;
+  }
+  bool bad = (uint32_t)h >= (uint32_t)a.hkv || p0 < 0 || p1 > a.pt_stride;
+#pragma unroll
+  for (int x = 0; x < kMaxGroup; ++x) bad |= (uint32_t)ag[x] >= (uint32_t)a.n_agents;
+  if (bad) {
+    if (lane == 0) flag_status(a.status, kDevBadArg);
+    h = 0;
+    p0 = p1 = 0;
+#pragma unroll
+    for (int x = 0; x < kMaxGroup; ++x) ag[x] = 0;
+  }
+  if (p1 < p0) p1 = p0;
+  const int x = (lane - kUfAgent) & 3;  // agent of the per-agent field lanes
+  int32_t agx = ag[0];
+#pragma unroll
+  for (int i = 1; i < kMaxGroup; ++i)
+    if (x == i) agx = ag[i];
+  switch (lane < kUfAgent ? lane : kUfAgent + 4 * ((lane - kUfAgent) >> 2)) {
+    case kUfP0: return p0;
+    case kUfP1: return p1;
+    case kUfNa: return na;
+    case kUfH: return h;
+    case kUfSlot: return slot;
+    case kUfEnd: return 0;
+    case kUfAgent: return agx;
+    case kUfL: return x < na ? __ldg(a.seq_lens + agx) : 0;  // clipped and checked at publication
+    case kUfPos: return __ldg(a.positions + agx);
+    case kUfAdapter: return a.adapter_ids ? __ldg(a.adapter_ids + agx) : agx;
+    default: return 0;
   }
 }
 
-__device__ __forceinline__ Unit load_unit(const DecodeArgs& a, int first, int k) {
-  Unit u;
-  int32_t item, head;
-  if (a.plan) {
-    const int32_t code = a.units[first + k];
-    item = code / a.hkv;
-    head = code - item * a.hkv;
-  } else {
-    const int32_t code = first + k * gridDim.x;
-    item = code / a.hkv;
-    head = code - item * a.hkv;
-  }
-  u.h = head;
-  if (a.plan) {
-    if ((uint32_t)item >= (uint32_t)a.n_items) {
-      flag_status(a.status, kDevBadArg);
-      item = 0;
-    }
-    const int32_t* p = a.plan + (int64_t)item * FORKKV_PLAN_ITEM_INTS;
-    u.p0 = p[0];
-    u.p1 = p[1];
-    u.na = p[2];
-#pragma unroll
-    for (int i = 0; i < kMaxGroup; ++i) u.agents[i] = p[4 + i];
-    u.slot_base = p[12];
-    if (u.na != 1 && u.na != 2 && u.na != 4) {  // the value products stack the slots of 1, 2 or 4 agents
-      flag_status(a.status, kDevBadArg);
-      u.na = 1;
-      u.p1 = u.p0;
-    }
-    if (u.slot_base < 0 || u.slot_base + u.na > a.n_slots) {
-      flag_status(a.status, kDevBadArg);
-      u.p1 = u.p0;  // empty: reads nothing, writes nothing
-      u.slot_base = -1;
-    }
-  } else {
-    const int32_t agent = item / a.chunks, c = item % a.chunks;
-    const int32_t L = min(a.seq_lens[agent], a.max_seq_len);
-    const int32_t npg = (L + kPage - 1) / kPage;
-    u.p0 = c * a.chunk_pages;
-    u.p1 = min(u.p0 + a.chunk_pages, npg);
-    u.na = 1;
-#pragma unroll
-    for (int i = 0; i < kMaxGroup; ++i) u.agents[i] = agent;
-    u.slot_base = item;
-  }
-  if ((uint32_t)u.h >= (uint32_t)a.hkv) {
-    flag_status(a.status, kDevBadArg);
-    u.h = 0;
-    u.p1 = u.p0;
-  }
-#pragma unroll
-  for (int i = 0; i < kMaxGroup; ++i)
-    if ((uint32_t)u.agents[i] >= (uint32_t)a.n_agents) {
-      flag_status(a.status, kDevBadArg);
-      u.agents[i] = 0;
-      u.p1 = u.p0;
-    }
-  if (u.p0 < 0 || u.p1 > a.pt_stride) {
-    flag_status(a.status, kDevBadArg);
-    u.p0 = u.p1 = 0;
-  }
-  if (u.p1 < u.p0) u.p1 = u.p0;
-  return u;
+// Descriptor field at publication, when the agents' loads have landed: each agent's length
+// clipped to max_seq_len, after the checks on it and on its query position.
+__device__ __forceinline__ int32_t unit_finish(const DecodeArgs& a, int32_t v, int lane) {
+  const int32_t pos = __shfl_down_sync(0xffffffffu, v, kUfPos - kUfL);  // lane kUfL + x: agent x's position
+  const int32_t na = __shfl_sync(0xffffffffu, v, kUfNa);
+  const int32_t end = __shfl_sync(0xffffffffu, v, kUfEnd);
+  if (lane < kUfL || lane >= kUfL + kMaxGroup || end) return v;
+  if (lane - kUfL >= na) return 0;
+  if (v < 1 || v > a.max_seq_len || pos < 0 || pos >= v) flag_status(a.status, kDevBadArg);
+  return min(v, a.max_seq_len);
 }
 
-// Lanes work in groups of 8: an active group copies the nvp (<= 8) page tiles of a block,
-// whose ids sit in its lanes 8 q + p, into consecutive tiles at `dst` (the group's own
-// destination), raising the byte count `bar` expects (the caller arrives).  Consecutive
-// ids go as one bulk copy from the group's first lane, otherwise every lane copies its
-// own page, so the groups of a warp issue side by side.  When rows < 16 only the first
-// rows of the last page are copied and the rest of that tile is zeroed first (rows past
-// every sequence may never have been written, and a zero probability must not meet a
-// NaN).  A base tile keeps its rows in two 2048-byte halves (128 bytes a row), a residual
-// tile in one (32 bytes a row).
-__device__ __forceinline__ void copy_group(const uint8_t* pool, bool base, int32_t id, int nvp, int rows, uint8_t* dst,
-                                          uint64_t* bar, bool active, int lane) {
-  const int p = lane & 7;
+// Page copies of one block, by groups of 8 lanes: group q holds the ids of the block's nvp
+// (<= 8) pages in its lanes 8 q + p.  A base tile keeps its rows in two 2048-byte halves (128
+// bytes a row), a residual tile in one (32 bytes a row).  When rows < 16 only the first rows
+// of the last page are copied.
+
+// Bytes the copies of one group deliver.
+__device__ __forceinline__ uint32_t tile_bytes(bool base, int nvp, int rows) {
+  const uint32_t tile = base ? kBaseTile : kResTile, rb = base ? 128u : 32u;
+  return rows < kPage ? (uint32_t)(nvp - 1) * tile + (base ? 2u : 1u) * (uint32_t)rows * rb : (uint32_t)nvp * tile;
+}
+
+// Zero the rows of the last page that are not copied (rows past every sequence may never have
+// been written, and a zero probability must not meet a NaN).  Lane p of the group.
+__device__ __forceinline__ void zero_tail(bool base, int nvp, int rows, uint8_t* dst, int p) {
+  if (rows >= kPage) return;
+  const uint32_t tile = base ? kBaseTile : kResTile, rb = base ? 128u : 32u;
+  uint8_t* t = dst + (nvp - 1) * tile;
+  const uint32_t half = base ? 2048u : tile;  // bytes per half
+  for (uint32_t o = rows * rb + 16 * p; o < half; o += 16 * 8) {
+    *reinterpret_cast<uint4*>(t + o) = make_uint4(0u, 0u, 0u, 0u);
+    if (base) *reinterpret_cast<uint4*>(t + 2048 + o) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Lane p of a group issues its share of the copies, with no warp-wide operation: consecutive
+// ids (one_run) as one bulk copy from the group's first lane, otherwise one copy per page; the
+// lane holding a partial last page copies its rows.  The barrier's expected bytes are raised
+// by the caller in the same arrival that completes its count.
+__device__ __forceinline__ void copy_tiles(const uint8_t* pool, bool base, int32_t id, int nvp, int rows, uint8_t* dst,
+                                           uint64_t* bar, bool one_run, int p) {
   const uint32_t tile = base ? kBaseTile : kResTile, rb = base ? 128u : 32u;
   const int full = rows < kPage ? nvp - 1 : nvp;  // pages copied whole
-  if (active && full < nvp) {
-    uint8_t* t = dst + full * tile;
-    const uint32_t keep = rows * rb, half = base ? 2048u : tile;  // bytes kept per half
-    for (uint32_t o = keep + 16 * p; o < half; o += 16 * 8) {
-      *reinterpret_cast<uint4*>(t + o) = make_uint4(0u, 0u, 0u, 0u);
-      if (base) *reinterpret_cast<uint4*>(t + 2048 + o) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    tc::fence_proxy_async();
+  if (one_run) {
+    if (p == 0 && full > 0) bulk_g2s(dst, pool + (int64_t)id * tile, full * tile, bar);
+  } else if (p < full) {
+    bulk_g2s(dst + p * tile, pool + (int64_t)id * tile, tile, bar);
   }
-  const int32_t prev = __shfl_up_sync(0xffffffffu, id, 1);
-  const uint32_t breaks = __ballot_sync(0xffffffffu, active && p > 0 && p < full && id != prev + 1);
-  const bool one_run = ((breaks >> (lane & ~7)) & 0xffu) == 0;
-  if (active && p == 0)
-    mbar_expect_tx(bar, full * tile + (full < nvp && rows > 0 ? (base ? 2u : 1u) * rows * rb : 0u));
-  __syncwarp();
-  if (active) {
-    if (one_run) {
-      if (p == 0 && full > 0) bulk_g2s(dst, pool + (int64_t)id * tile, full * tile, bar);
-    } else if (p < full) {
-      bulk_g2s(dst + p * tile, pool + (int64_t)id * tile, tile, bar);
-    }
-    if (full < nvp && rows > 0 && p == full) {  // the lane holding the partial page
-      const uint8_t* src = pool + (int64_t)id * tile;
-      bulk_g2s(dst + full * tile, src, rows * rb, bar);
-      if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
-    }
+  if (full < nvp && rows > 0 && p == full) {
+    const uint8_t* src = pool + (int64_t)id * tile;
+    bulk_g2s(dst + full * tile, src, rows * rb, bar);
+    if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
   }
 }
 
@@ -338,20 +357,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   float* s_red = reinterpret_cast<float*>(smem + 512);      // [2][4 warps][8] block maxima
   float* s_mref = reinterpret_cast<float*>(smem + 768);     // [4 warps][4 agents][8] reference maxima
   int32_t* s_lp = reinterpret_cast<int32_t*>(smem + 1280);  // [4 warps][4 agents][2] length, position
+  int32_t* s_units = reinterpret_cast<int32_t*>(smem + kOffUnits);  // [2][kUnitInts] unit descriptors
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
-  int first, n_units;
-  cta_units(a, first, n_units);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;  // a single arrival: the producer's expect_tx or one MMA commit
-      if (i == kKEmpty0 || i == kKEmpty1 || i == kUFree || (i >= kKFFull0 && i <= kKFFull2))
+      if (i == kKEmpty0 || i == kKEmpty1 || i == kUFree0 || i == kUFree1 || i == kKFFull0 || i == kKFFull1)
         count = kRopeWarps;  // one arrival per RoPE warp
       if ((i >= kSFree0 && i <= kSFree2) || i == kPFull0 || i == kPFull1 || i == kRed0 || i == kRed1 ||
           i == kEpiDone)
         count = 4;  // one arrival per softmax warp
+      if (i == kUnitFree0 || i == kUnitFree1) count = kThreads / 32 - 1;  // every warp but the producer
       mbar_init(&bars[i], count);
     }
     mbar_fence_init();
@@ -369,94 +388,151 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   tc::fence_after();
   const uint32_t tm = *s_tmem;
 
+  // Unit k of this CTA as published by the producer: wait for its descriptor, and release
+  // the ring slot once the caller has copied what it needs (`take`).
+  auto unit_wait = [&](int k) { return mbar_wait(&bars[kUnitReady0 + (k & 1)], (k >> 1) & 1, a.status); };
+  auto unit_at = [&](int k, int f) -> int32_t { return s_units[(k & 1) * kUnitInts + f]; };
+  auto unit_release = [&](int k) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kUnitFree0 + (k & 1)]);
+  };
+  auto blocks_of = [](int32_t p0, int32_t p1) { return (p1 - p0 + kBlockPages - 1) / kBlockPages; };
+
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
-    // Per block, in order: K tiles, each agent's k_res tiles, then V tiles and each agent's
-    // v_res tiles (released together by the block's value products).  A block's page ids are
-    // fetched one block ahead, one per lane: lane p < 8 the base page p, lane 8 a + p the
-    // residual page p of agent a.  Every wait is for the buffer's previous user, two blocks
-    // (or four k_res slots) back.
-    int gb = 0, gn = 0;  // blocks and steps of every earlier unit
-    int kb = 0, kn = 0, vb = 0;  // blocks / k_res steps / blocks of V whose copies went out
+    // Describes the units in the ring (descriptors built two ahead, so that the loads behind
+    // one land while earlier units run) and copies, block by block: the K tiles, each agent's
+    // k_res tiles as soon as that agent's slot (four steps back) is free, then the V tiles
+    // with every agent's v_res tiles.  Every wait is for a buffer's previous user.  Page ids
+    // come one per lane (lane p < 8 the base page p, lane 8 a + p the residual page p of agent
+    // a) and are requested a block ahead.
+    const int pg = lane & 7, ag = lane >> 3;
+    int32_t r_nxt;
+    const int32_t r0 = first_unit(a);
+    int32_t cur = unit_field(a, r0, unit_raw(a, r0, lane), lane, r_nxt);  // next descriptor to publish
+    int32_t raw_nxt = unit_raw(a, r_nxt, lane);                            // raw record of the one after
+    int n_pub = 0;
     bool ok = true;
-    for (int k = 0; k < n_units && ok; ++k) {
-      const Unit u = load_unit(a, first, k);
-      const int na = u.na, nb = u.blocks();
-      const uint8_t* kpool = a.k_base + (int64_t)u.h * a.num_base_pages * kBaseTile;
-      const uint8_t* vpool = a.v_base + (int64_t)u.h * a.num_base_pages * kBaseTile;
-      const int pg = lane & 7, ag = lane >> 3;
-      const bool res_lane = ag < na;  // lanes of the agents' residual groups
-      const int32_t my_agent = u.agent(res_lane ? ag : 0);
-      const int32_t Lx = res_lane ? min(a.seq_lens[my_agent], a.max_seq_len) : 0;
-      int32_t Lmax = Lx;  // rows at or past the longest sequence of the group are never read as data
-#pragma unroll
-      for (int o = 8; o < 32; o <<= 1) Lmax = max(Lmax, __shfl_xor_sync(0xffffffffu, Lmax, o));
-      auto load_ids = [&](int b, int32_t& bid, int32_t& rid) {
-        const int pbase = u.p0 + b * kBlockPages;
-        const int nvp = min(kBlockPages, u.p1 - pbase);
-        bid = rid = 0;
-        if (lane < nvp) bid = a.bpt[(int64_t)u.agents[0] * a.pt_stride + pbase + lane];
-        if (res_lane && pg < nvp) rid = a.rpt[(int64_t)my_agent * a.pt_stride + pbase + pg];
-      };
-      int32_t bid_next = 0, rid_next = 0;
-      if (nb > 0) load_ids(0, bid_next, rid_next);
-      for (int b = 0; b < nb; ++b) {
-        const int g = gb + b;  // global block
-        const int pbase = u.p0 + b * kBlockPages;
-        const int nvp = min(kBlockPages, u.p1 - pbase);
-        int32_t bid = bid_next, rid = rid_next;
-        if (b + 1 < nb) load_ids(b + 1, bid_next, rid_next);
-        if ((uint32_t)bid >= (uint32_t)a.num_base_pages) {
-          flag_status(a.status, kDevBadPage);
-          bid = 0;
-        }
-        if ((uint32_t)rid >= (uint32_t)a.num_res_pages) {
-          flag_status(a.status, kDevBadPage);
-          rid = 0;
-        }
-        // K tiles
-        if (g >= 2 && !mbar_wait(&bars[kKEmpty0 + (g & 1)], ((g >> 1) - 1) & 1, a.status)) {
-          ok = false;
-          break;
-        }
-        copy_group(kpool, true, bid, nvp, kPage, smem + kOffK + (g & 1) * kBlockTiles, &bars[kKFull0 + (g & 1)],
-                   lane < kBlockPages, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kKFull0 + (g & 1)]);
-        kb = g + 1;
-        // every agent's k_res tiles, one k_res slot (and barrier) per (block, agent) step
-        for (int x = 0; x < na && ok; ++x) {
-          const int n = gn + b * na + x;
-          if (n >= kResSlots) ok = mbar_wait(&bars[kKrEmpty0 + (n & 3)], ((n >> 2) - 1) & 1, a.status);
-        }
-        if (!ok) break;
-        const int kslot = (gn + b * na + ag) & 3;
-        copy_group(a.k_res, false, rid, nvp, kPage, smem + kOffKr + kslot * kResSlotBytes, &bars[kKrFull0 + kslot],
-                   res_lane, lane);
-        __syncwarp();
-        if (res_lane && pg == 0) mbar_arrive(&bars[kKrFull0 + kslot]);
-        kn = gn + b * na + na;
-        // V tiles and every agent's v_res tiles, on one barrier (released by the block's value products)
-        if (g >= 2 && !mbar_wait(&bars[kVEmpty0 + (g & 1)], ((g >> 1) - 1) & 1, a.status)) {
-          ok = false;
-          break;
-        }
-        uint64_t* vbar = &bars[kVFull0 + (g & 1)];
-        const int last = (pbase + nvp - 1) * kPage;  // first key of the block's last page
-        copy_group(vpool, true, bid, nvp, min(kPage, max(0, Lmax - last)), smem + kOffV + (g & 1) * kBlockTiles, vbar,
-                   lane < kBlockPages, lane);
-        copy_group(a.v_res, false, rid, nvp, min(kPage, max(0, Lx - last)),
-                   smem + kOffVr + (g & 1) * kVrGroupBytes + (4 - na + ag) * kResSlotBytes, vbar, res_lane, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(vbar);
-        vb = g + 1;
+    // publish `cur` as unit n_pub once its ring slot is free; build the next descriptor
+    auto publish = [&]() -> int32_t {
+      if (n_pub >= 2) ok = ok && mbar_wait(&bars[kUnitFree0 + (n_pub & 1)], ((n_pub >> 1) - 1) & 1, a.status);
+      const int32_t v = unit_finish(a, cur, lane);
+      if (lane < kUnitInts) s_units[(n_pub & 1) * kUnitInts + lane] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kUnitReady0 + (n_pub & 1)]);
+      ++n_pub;
+      if (__shfl_sync(0xffffffffu, v, kUfEnd) == 0) {
+        const int32_t r = r_nxt;
+        cur = unit_field(a, r, raw_nxt, lane, r_nxt);
+        raw_nxt = unit_raw(a, r_nxt, lane);
       }
-      gb += nb;
-      gn += nb * na;
+      return v;
+    };
+    struct Blk {  // what the copies of one block need
+      int32_t bid, rid, h, na, pbase, nvp, Lmax, Lx;
+    };
+    int kbl = 0, knb = 0;  // the cursor: next block within its unit, and the unit's blocks
+    bool ended = false;
+    int32_t kp0 = 0, kp1 = 0, kna = 1, kh = 0, kag0 = 0, kagx = 0, kLx = 0, kLmax = 0;
+    // the cursor's next block into x, its page ids requested (not waited for); false at the end
+    auto next_block = [&](Blk& x) -> bool {
+      while (kbl >= knb) {
+        if (ended || !ok) return false;
+        const int32_t d = publish();
+        if (__shfl_sync(0xffffffffu, d, kUfEnd) != 0) {
+          ended = true;
+          return false;
+        }
+        kp0 = __shfl_sync(0xffffffffu, d, kUfP0);
+        kp1 = __shfl_sync(0xffffffffu, d, kUfP1);
+        kna = __shfl_sync(0xffffffffu, d, kUfNa);
+        kh = __shfl_sync(0xffffffffu, d, kUfH);
+        kag0 = __shfl_sync(0xffffffffu, d, kUfAgent);
+        kagx = __shfl_sync(0xffffffffu, d, kUfAgent + (ag & 3));
+        kLx = __shfl_sync(0xffffffffu, d, kUfL + (ag & 3));
+        if (ag >= kna) kLx = 0;
+        kLmax = kLx;  // rows at or past the longest sequence of the group are never read as data
+#pragma unroll
+        for (int o = 8; o < 32; o <<= 1) kLmax = max(kLmax, __shfl_xor_sync(0xffffffffu, kLmax, o));
+        knb = blocks_of(kp0, kp1);
+        kbl = 0;
+      }
+      x.pbase = kp0 + kbl * kBlockPages;
+      x.nvp = min(kBlockPages, kp1 - x.pbase);
+      x.h = kh;
+      x.na = kna;
+      x.Lmax = kLmax;
+      x.Lx = kLx;
+      x.bid = x.rid = 0;
+      if (lane < x.nvp) x.bid = a.bpt[(int64_t)kag0 * a.pt_stride + x.pbase + lane];
+      if (ag < kna && pg < x.nvp) x.rid = a.rpt[(int64_t)kagx * a.pt_stride + x.pbase + pg];
+      ++kbl;
+      return true;
+    };
+    Blk nx{};
+    bool more = next_block(nx);
+    int g = 0, kn = 0;  // blocks copied, k_res steps copied
+    while (ok && more) {
+      Blk b = nx;
+      more = next_block(nx);  // the next block's ids go out now
+      if ((uint32_t)b.bid >= (uint32_t)a.num_base_pages) {
+        flag_status(a.status, kDevBadPage);
+        b.bid = 0;
+      }
+      if ((uint32_t)b.rid >= (uint32_t)a.num_res_pages) {
+        flag_status(a.status, kDevBadPage);
+        b.rid = 0;
+      }
+      const int32_t pb = __shfl_up_sync(0xffffffffu, b.bid, 1), pr = __shfl_up_sync(0xffffffffu, b.rid, 1);
+      const bool brun = __ballot_sync(0xffffffffu, lane < 8 && pg > 0 && pg < b.nvp && b.bid != pb + 1) == 0;
+      const bool rrun = ((__ballot_sync(0xffffffffu, pg > 0 && pg < b.nvp && b.rid != pr + 1) >> (lane & ~7)) & 0xffu) == 0;
+      // K tiles
+      if (g >= 2 && !(ok = mbar_wait(&bars[kKEmpty0 + (g & 1)], ((g >> 1) - 1) & 1, a.status))) break;
+      uint64_t* kbar = &bars[kKFull0 + (g & 1)];
+      if (lane == 0) mbar_arrive_expect_tx(kbar, tile_bytes(true, b.nvp, kPage));
+      if (lane < 8)
+        copy_tiles(a.k_base + (int64_t)b.h * a.num_base_pages * kBaseTile, true, b.bid, b.nvp, kPage,
+                   smem + kOffK + (g & 1) * kBlockTiles, kbar, brun, pg);
+      // each agent's k_res tiles, into the slot of its (block, agent) step
+      for (int x = 0; x < b.na && ok; ++x) {
+        const int n = kn + x, kslot = n & 3;
+        if (n >= kResSlots && !(ok = mbar_wait(&bars[kKrEmpty0 + kslot], ((n >> 2) - 1) & 1, a.status))) break;
+        uint64_t* rbar = &bars[kKrFull0 + kslot];
+        if (lane == 8 * x) mbar_arrive_expect_tx(rbar, tile_bytes(false, b.nvp, kPage));
+        if (ag == x) copy_tiles(a.k_res, false, b.rid, b.nvp, kPage, smem + kOffKr + kslot * kResSlotBytes, rbar, rrun, pg);
+      }
+      if (!ok) break;
+      kn += b.na;
+      // V tiles and every agent's v_res tiles, on one barrier (released by the block's value
+      // products); one arrival raises the bytes of every group
+      if (g >= 2 && !(ok = mbar_wait(&bars[kVEmpty0 + (g & 1)], ((g >> 1) - 1) & 1, a.status))) break;
+      uint64_t* vbar = &bars[kVFull0 + (g & 1)];
+      const int last = (b.pbase + b.nvp - 1) * kPage;  // first key of the block's last page
+      const int vrows = min(kPage, max(0, b.Lmax - last));
+      const int rrows = min(kPage, max(0, b.Lx - last));  // this lane group's agent
+      uint8_t* vdst = smem + kOffV + (g & 1) * kBlockTiles;
+      uint8_t* rdst = smem + kOffVr + (g & 1) * kVrGroupBytes + (4 - b.na + ag) * kResSlotBytes;
+      const bool ract = ag < b.na;
+      if (__any_sync(0xffffffffu, (lane < 8 && vrows < kPage) || (ract && rrows < kPage))) {
+        if (lane < 8) zero_tail(true, b.nvp, vrows, vdst, pg);
+        if (ract) zero_tail(false, b.nvp, rrows, rdst, pg);
+        tc::fence_proxy_async();
+        __syncwarp();
+      }
+      uint32_t bytes = ract && pg == 0 ? tile_bytes(false, b.nvp, rrows) : 0u;
+      bytes += __shfl_xor_sync(0xffffffffu, bytes, 8);
+      bytes += __shfl_xor_sync(0xffffffffu, bytes, 16);
+      if (lane == 0) mbar_arrive_expect_tx(vbar, bytes + tile_bytes(true, b.nvp, vrows));
+      if (lane < 8)
+        copy_tiles(a.v_base + (int64_t)b.h * a.num_base_pages * kBaseTile, true, b.bid, b.nvp, vrows, vdst, vbar, brun, pg);
+      if (ract) copy_tiles(a.v_res, false, b.rid, b.nvp, rrows, rdst, vbar, rrun, pg);
+      ++g;
     }
     // never leave with copies in flight: the last phase of every barrier written to
-    for (int b = max(0, kb - 2); b < kb; ++b) mbar_wait(&bars[kKFull0 + (b & 1)], (b >> 1) & 1, a.status);
-    for (int b = max(0, vb - 2); b < vb; ++b) mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status);
+    for (int b = max(0, g - 2); b < g; ++b) {
+      mbar_wait(&bars[kKFull0 + (b & 1)], (b >> 1) & 1, a.status);
+      mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status);
+    }
     for (int n = max(0, kn - kResSlots); n < kn; ++n) mbar_wait(&bars[kKrFull0 + (n & 3)], (n >> 2) & 1, a.status);
   } else if (warp == 1) {
     // ------------------------------ U issuer ------------------------------
@@ -469,9 +545,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const uint64_t dBk = tc::smem_desc(sBase + kOffBk, 2048, 1024, tc::kSwizzle128B);
     int gn = 0;
     bool ok = true;
-    for (int k = 0; k < n_units && ok; ++k) {
-      const Unit u = load_unit(a, first, k);
-      const int na = u.na, N = u.blocks() * na;
+    for (int k = 0; ok; ++k) {
+      if (!unit_wait(k)) break;
+      const int32_t p0 = unit_at(k, kUfP0), p1 = unit_at(k, kUfP1), na = unit_at(k, kUfNa), h = unit_at(k, kUfH);
+      const bool end = unit_at(k, kUfEnd) != 0;
+      int32_t adapter = unit_at(k, kUfAdapter + (lane & 3));
+      unit_release(k);
+      if (end) break;
+      const int N = blocks_of(p0, p1) * na;
+      if ((lane & 3) < na && (uint32_t)adapter >= (uint32_t)a.n_adapters) {
+        flag_status(a.status, kDevBadArg);
+        adapter = 0;
+      }
       if (k > 0) {  // every U of the previous unit is done with B_k
         if (lane == 0) {
           tc::commit(&bars[kUUnit]);
@@ -481,17 +566,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         if (!ok) break;
       }
       for (int x = 0; x < na; ++x) {
-        int32_t adapter = a.adapter_ids ? a.adapter_ids[u.agent(x)] : u.agent(x);
-        if ((uint32_t)adapter >= (uint32_t)a.n_adapters) {
-          flag_status(a.status, kDevBadArg);
-          adapter = 0;
-        }
-        const __nv_bfloat16* B = a.B_k + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)u.h * kHeadDim;
+        int32_t ad = __shfl_sync(0xffffffffu, adapter, x);
+        if ((uint32_t)ad >= (uint32_t)a.n_adapters) ad = 0;
+        const __nv_bfloat16* B = a.B_k + (int64_t)ad * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim;
+        uint4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {  // 16 ranks x 16 chunks of 8 d
           const int c = lane + 32 * i, r = c >> 4, ch = c & 15;
-          *reinterpret_cast<uint4*>(smem + kOffBk + x * 4096 + base_off(r, ch * 8)) =
-              *reinterpret_cast<const uint4*>(B + (int64_t)r * a.hkv * kHeadDim + ch * 8);
+          v[i] = *reinterpret_cast<const uint4*>(B + (int64_t)r * a.hkv * kHeadDim + ch * 8);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = lane + 32 * i, r = c >> 4, ch = c & 15;
+          *reinterpret_cast<uint4*>(smem + kOffBk + x * 4096 + base_off(r, ch * 8)) = v[i];
         }
       }
       tc::fence_proxy_async();
@@ -500,11 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         for (int n = 0; n < N && ok; ++n) {
           const int m = gn + n;
           ok = mbar_wait(&bars[kKrFull0 + (m & 3)], (m >> 2) & 1, a.status) &&
-               (m < 1 || mbar_wait(&bars[kUFree], (m - 1) & 1, a.status));
+               (m < 2 || mbar_wait(&bars[kUFree0 + (m & 1)], ((m >> 1) - 1) & 1, a.status));
           if (!ok) break;
           tc::fence_after();
-          tc::mma_ss(tm + kTmU, dKr + (m & 3) * (kResSlotBytes >> 4), dBk + (n % na) * (4096 >> 4), idU, 0);
-          tc::commit(&bars[kUFull]);
+          tc::mma_ss(tm + kTmU + 128 * (m & 1), dKr + (m & 3) * (kResSlotBytes >> 4), dBk + (n % na) * (4096 >> 4),
+                     idU, 0);
+          tc::commit(&bars[kUFull0 + (m & 1)]);
           tc::commit(&bars[kKrEmpty0 + (m & 3)]);
         }
       }
@@ -525,9 +613,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const uint32_t sBase = smem_u32(smem);
     int gn = 0;
     bool ok = true;
-    for (int k = 0; k < n_units && ok; ++k) {
-      const Unit u = load_unit(a, first, k);
-      const int na = u.na, N = u.blocks() * na;
+    for (int k = 0; ok; ++k) {
+      if (!unit_wait(k)) break;
+      const int32_t p0 = unit_at(k, kUfP0), p1 = unit_at(k, kUfP1), na = unit_at(k, kUfNa), h = unit_at(k, kUfH);
+      const bool end = unit_at(k, kUfEnd) != 0;
+      const int32_t agent_l = unit_at(k, kUfAgent + (lane & 3));
+      unit_release(k);
+      if (end) break;
+      const int N = blocks_of(p0, p1) * na;
       if (k > 0) {  // every S of the previous unit is done with Q^T
         if (lane == 0) {
           tc::commit(&bars[kSUnit]);
@@ -536,36 +629,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
-      for (int x = 0; x < na; ++x) {
-        const int32_t agent = u.agent(x);
+      uint4 v[kMaxGroup][4];
+#pragma unroll
+      for (int x = 0; x < kMaxGroup; ++x) {
+        const int32_t agent = __shfl_sync(0xffffffffu, agent_l, x);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {  // 8 query-head rows x 16 chunks of 8 d
           const int c = lane + 32 * i, g = c >> 4, ch = c & 15;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (g < G)
-            v = *reinterpret_cast<const uint4*>(a.q + ((int64_t)agent * a.hkv * G + (int64_t)u.h * G + g) * kHeadDim + ch * 8);
-          *reinterpret_cast<uint4*>(smem + kOffQ + x * 2048 + tc::sw128_off(8, g, ch * 8)) = v;
+          v[x][i] = make_uint4(0u, 0u, 0u, 0u);
+          if (x < na && g < G)
+            v[x][i] = *reinterpret_cast<const uint4*>(a.q + ((int64_t)agent * a.hkv * G + (int64_t)h * G + g) * kHeadDim +
+                                                      ch * 8);
         }
       }
+#pragma unroll
+      for (int x = 0; x < kMaxGroup; ++x)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = lane + 32 * i, g = c >> 4, ch = c & 15;
+          if (x < na) *reinterpret_cast<uint4*>(smem + kOffQ + x * 2048 + tc::sw128_off(8, g, ch * 8)) = v[x][i];
+        }
       tc::fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
         for (int n = 0; n < N && ok; ++n) {
           const int m = gn + n;
-          const int sr = m % kRing, sp = (m / kRing) & 1;  // ring slot and phase parity of step m
-          ok = mbar_wait(&bars[kKFFull0 + sr], sp, a.status) &&
-               (m < kRing || mbar_wait(&bars[kSFree0 + sr], sp ^ 1, a.status));
+          const int kr = m & 1, sr = m % kSRing, sp = (m / kSRing) & 1;  // ring slots of step m
+          ok = mbar_wait(&bars[kKFFull0 + kr], (m >> 1) & 1, a.status) &&
+               (m < kSRing || mbar_wait(&bars[kSFree0 + sr], sp ^ 1, a.status));
           if (!ok) break;
           tc::fence_after();
           const uint32_t q = kOffQ + (n % na) * 2048;  // the two 64-column halves of Q^T at q, q + 1024
           const uint64_t dq0 = tc::smem_desc(sBase + q, 16, kOffQZero - q, tc::kSwizzle128B);
           const uint64_t dq1 = tc::smem_desc(sBase + q + 1024, 16, kOffQZero - q - 1024, tc::kSwizzle128B);
-          const uint32_t dS = tm + kTmS + 16 * sr, aK = tm + kTmKF + 64 * sr;
+          const uint32_t dS = tm + kTmS + 16 * sr, aK = tm + kTmKF + 64 * kr;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // K = 16 per step: 8 TMEM columns of A, 32 bytes of B
             tc::mma_ts(dS, aK + 8 * ks, (ks < 4 ? dq0 : dq1) + 2 * (ks & 3), idS, ks > 0);
           tc::commit(&bars[kSFull0 + sr]);
-          tc::commit(&bars[kKFFree0 + sr]);
+          tc::commit(&bars[kKFFree0 + kr]);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -587,14 +689,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     int gb = 0, gn = 0;
     bool ok = true;
     uint4 rp[2][4];  // rotation groups of this warp's two column chunks for key j (see below)
-    for (int k = 0; k < n_units && ok; ++k) {
-      const Unit u = load_unit(a, first, k);
-      const int na = u.na, N = u.blocks() * na;
+    for (int k = 0; ok; ++k) {
+      if (!unit_wait(k)) break;
+      const int32_t p0 = unit_at(k, kUfP0), p1 = unit_at(k, kUfP1), na = unit_at(k, kUfNa);
+      const bool end = unit_at(k, kUfEnd) != 0;
+      unit_release(k);
+      if (end) break;
+      const int N = blocks_of(p0, p1) * na;
       for (int n = 0; n < N && ok; ++n) {
         const int b = n / na, ai = n - b * na;
         const int g = gb + b, m = gn + n;  // global block and step
         const int stage = g & 1;
-        const int pbase = u.p0 + b * kBlockPages;
+        const int pbase = p0 + b * kBlockPages;
         const int j = pbase * kPage + row;
         if (ai == 0) {
           // chunk c = 32 hf + 16 cc holds frequency groups m = c/2 .. c/2 + 7: 32-byte units
@@ -612,8 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           ok = mbar_wait(&bars[kKFull0 + stage], (g >> 1) & 1, a.status);
           if (!ok) break;
         }
-        // U of this step, read out at once (as bf16 pairs) so that the next U can go ahead
-        ok = mbar_wait(&bars[kUFull], m & 1, a.status);
+        // U of this step, read out at once (as bf16 pairs) so that its buffer frees early
+        ok = mbar_wait(&bars[kUFull0 + (m & 1)], (m >> 1) & 1, a.status);
         if (!ok) break;
         tc::fence_after();
         uint32_t ul[2][8], uh[2][8];  // [chunk][pair]: U columns (c + 2 i, c + 2 i + 1) and + 64
@@ -621,8 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         for (int cc = 0; cc < 2; ++cc) {
           const int c = 32 * hf + 16 * cc;
           uint32_t lo[16], hi[16];
-          tc::ld16(tl + kTmU + c, lo);
-          tc::ld16(tl + kTmU + 64 + c, hi);
+          tc::ld16(tl + kTmU + 128 * (m & 1) + c, lo);
+          tc::ld16(tl + kTmU + 128 * (m & 1) + 64 + c, hi);
           tc::wait_ld();
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -632,9 +738,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         }
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kUFree]);
-        const int kr = m % kRing, kp = (m / kRing) & 1;
-        if (m >= kRing && !mbar_wait(&bars[kKFFree0 + kr], kp ^ 1, a.status)) {
+        if (lane == 0) mbar_arrive(&bars[kUFree0 + (m & 1)]);
+        const int kr = m & 1;
+        if (m >= kKfRing && !mbar_wait(&bars[kKFFree0 + kr], ((m >> 1) - 1) & 1, a.status)) {
           ok = false;
           break;
         }
@@ -680,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           if (ai == na - 1) mbar_arrive(&bars[kKEmpty0 + stage]);
         }
       }
-      gb += u.blocks();
+      gb += blocks_of(p0, p1);
       gn += N;
     }
   } else if (warp == kValueWarp) {
@@ -701,9 +807,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       const uint64_t dP = tc::smem_desc(sBase + kOffP, 4096, 256, tc::kSwizzle32B);
       int gb = 0;
       bool ok = true;
-      for (int k = 0; k < n_units && ok; ++k) {
-        const Unit u = load_unit(a, first, k);
-        const int na = u.na, nb = u.blocks();
+      for (int k = 0; ok; ++k) {
+        if (!unit_wait(k)) break;
+        const int32_t p0 = unit_at(k, kUfP0), p1 = unit_at(k, kUfP1), na = unit_at(k, kUfNa);
+        const bool end = unit_at(k, kUfEnd) != 0;
+        mbar_arrive(&bars[kUnitFree0 + (k & 1)]);
+        if (end) break;
+        const int nb = blocks_of(p0, p1);
         const uint32_t idV = tc::idesc_bf16(128, na > 2 ? 32 : 16, 1, 1);
         const uint64_t dR =
             tc::smem_desc(sBase + kOffVr + (4 - na) * kResSlotBytes, kResSlotBytes, 256, tc::kSwizzle32B);
@@ -714,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
                mbar_wait(&bars[kPFull0 + (g & 1)], (g >> 1) & 1, a.status);
           if (!ok) break;
           tc::fence_after();
-          const int nvp = min(kBlockPages, u.p1 - (u.p0 + b * kBlockPages));
+          const int nvp = min(kBlockPages, p1 - (p0 + b * kBlockPages));
           const uint64_t dv = dV + (g & 1) * (kBlockTiles >> 4), dp = dP + (g & 1) * (8192 >> 4);
           const uint64_t dr = dR + (g & 1) * (kVrGroupBytes >> 4);  // 8 atoms of 16 rows, 4 KB apart
           const uint32_t acc0 = b > 0;
@@ -746,29 +856,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const bool publisher = kG == 8 ? (lane & 3) == 0 : (lane & 7) == 0;
     int gb = 0, gn = 0;
     bool ok = true;
-    for (int k = 0; k < n_units && ok; ++k) {
-      const Unit u = load_unit(a, first, k);
-      const int na = u.na, nb = u.blocks(), N = nb * na;
+    for (int k = 0; ok; ++k) {
+      if (!unit_wait(k)) break;
+      const int32_t p0 = unit_at(k, kUfP0), p1 = unit_at(k, kUfP1), na = unit_at(k, kUfNa), h = unit_at(k, kUfH);
+      const int32_t slot_base = unit_at(k, kUfSlot);
+      const bool end = unit_at(k, kUfEnd) != 0;
       __syncwarp();
       mref[lane] = -INFINITY;  // 4 agents x 8 query heads
       if (lane < kMaxGroup) {
-        const int32_t agent = u.agent(lane);
-        const int32_t L = a.seq_lens[agent], pos = a.positions[agent];
-        lp[2 * lane] = lane < na ? min(L, a.max_seq_len) : 0;
-        lp[2 * lane + 1] = pos;
-        if (lane < na && sw_ == 0 && u.h == 0 && (L < 1 || L > a.max_seq_len || pos < 0 || pos >= L))
-          flag_status(a.status, kDevBadArg);
+        lp[2 * lane] = unit_at(k, kUfL + lane);  // 0 past the unit's agents
+        lp[2 * lane + 1] = unit_at(k, kUfPos + lane);
       }
-      __syncwarp();
+      unit_release(k);
+      if (end) break;
+      const int nb = blocks_of(p0, p1), N = nb * na;
       for (int n = 0; n < N && ok; ++n) {
         const int b = n / na, ai = n - b * na;
         const int g = gb + b, m = gn + n;  // global block and step
-        const int pbase = u.p0 + b * kBlockPages;
+        const int pbase = p0 + b * kBlockPages;
         const int j = pbase * kPage + row;
         const int32_t L = lp[2 * ai], pos = lp[2 * ai + 1];
-        const bool vis = j < L && j <= pos && j < u.p1 * kPage;
-        const int sr = m % kRing;
-        ok = mbar_wait(&bars[kSFull0 + sr], (m / kRing) & 1, a.status);
+        const bool vis = j < L && j <= pos && j < p1 * kPage;
+        const int sr = m % kSRing;
+        ok = mbar_wait(&bars[kSFull0 + sr], (m / kSRing) & 1, a.status);
         if (!ok) break;
         tc::fence_after();
         uint32_t sv[kG];
@@ -867,13 +977,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       const int glast = gb + nb - 1;
       if (nb > 0) ok = mbar_wait(&bars[kODone0 + (glast & 1)], (glast >> 1) & 1, a.status);
       tc::fence_after();
-      if (u.slot_base >= 0) {
+      if (slot_base >= 0) {
         for (int ai = 0; ai < na; ++ai) {
           uint32_t ov[8], rv[8];
           tc::ld8(tl + kTmO + 8 * ai, ov);
           tc::ld8(tl + kTmR + 8 * ai, rv);
           tc::wait_ld();
-          const int64_t rec0 = ((int64_t)(u.slot_base + ai) * a.hkv + u.h) * G;
+          const int64_t rec0 = ((int64_t)(slot_base + ai) * a.hkv + h) * G;
           const int r = row - kRank * ai;  // rank held by this lane of agent ai's rows of R
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -1072,15 +1182,15 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   a.rope_positions = p.rope_table ? p.rope_table_positions : (p.max_seq_len + kPage - 1) / kPage * kPage;
   const float scale = p.sm_scale > 0.f ? p.sm_scale : 1.0f / sqrtf((float)kHeadDim);
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.plan = p.plan;
-  a.n_items = g.n_items;
-  if (p.plan) {  // the schedule follows the items and the per-agent slot lists
-    a.cta_off = p.plan + (int64_t)p.plan_items * FORKKV_PLAN_ITEM_INTS + p.n_agents + 1 + p.plan_slots;
-    a.units = a.cta_off + p.plan_ctas + 1;
-    a.n_ctas = p.plan_ctas;
+  int32_t n_ctas;
+  if (p.plan) {  // the unit records follow the items and the per-agent slot lists
+    a.units = p.plan + (int64_t)p.plan_items * FORKKV_PLAN_ITEM_INTS + p.n_agents + 1 + p.plan_slots;
+    a.n_units = p.plan_items * p.num_kv_heads;
+    n_ctas = p.plan_ctas;
   } else {  // every (item, head) pair, dealt round-robin over at most one CTA per SM
-    a.cta_off = a.units = nullptr;
-    a.n_ctas = (int32_t)std::min<int64_t>((int64_t)g.n_items * p.num_kv_heads, std::max(1, sm_count));
+    a.units = nullptr;
+    a.n_units = g.n_items * p.num_kv_heads;
+    n_ctas = (int32_t)std::min<int64_t>(a.n_units, std::max(1, sm_count));
   }
   a.chunk_pages = g.chunk_pages;
   a.chunks = g.chunks;
@@ -1091,9 +1201,9 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   a.ml = reinterpret_cast<float*>(ws + g.partial_bytes);
   a.status = status;
   if (G <= 4)
-    decode_split_kernel<4><<<a.n_ctas, kThreads, kSmemBytes, stream>>>(a);
+    decode_split_kernel<4><<<n_ctas, kThreads, kSmemBytes, stream>>>(a);
   else
-    decode_split_kernel<8><<<a.n_ctas, kThreads, kSmemBytes, stream>>>(a);
+    decode_split_kernel<8><<<n_ctas, kThreads, kSmemBytes, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

@@ -112,30 +112,45 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
     }
   }
 
-  // 3. a stage cap T per item (chunks are cut into near-equal items of at most T blocks)
-  //    and a spread of the (item, head) units over the CTAs.  A unit's cost is counted in
-  //    pipeline steps: one per (block, agent), about one more per block for its shared
-  //    value products and base tiles, and about two for starting the unit and writing its
-  //    partials.  Units go largest first to the least loaded CTA (LPT); T is the cap whose
-  //    spread ends soonest, the larger one on ties (fewer partials to merge).
+  // 3. a stage cap per group size (chunks are cut into near-equal items of at most that many
+  //    blocks) and a spread of the (item, head) units over the CTAs.  A unit's cost is its
+  //    time on one SM as measured for the decode kernel on a GB300 (ns): a block takes about
+  //    930 per agent, and no less than 2400 however few agents share it (the copies and the
+  //    value products of a block then set the pace); starting a unit and writing its
+  //    partials add about 3000.  Units go largest first to the least loaded CTA (LPT).  The
+  //    caps are chosen by coordinate descent on the makespan, each from the longest chunk
+  //    down, keeping the larger cap on ties (fewer partials to merge).
   const int32_t C_max = target_ctas;
-  int32_t max_stages = 1;
-  for (const Chunk& c : chunks) max_stages = std::max(max_stages, c.stages);
-  auto unit_cost = [](int32_t blocks, int32_t na) { return (int64_t)blocks * (na + 1) + 2; };
+  auto gi = [](int32_t na) { return na >= 4 ? 2 : na - 1; };  // group-size class of a chunk
+  int32_t max_stages[3] = {1, 1, 1};
+  bool present[3] = {false, false, false};
+  for (const Chunk& c : chunks) {
+    max_stages[gi(c.na)] = std::max(max_stages[gi(c.na)], c.stages);
+    present[gi(c.na)] = true;
+  }
+  auto unit_cost = [](int32_t blocks, int32_t na) {
+    return (int64_t)blocks * std::max<int64_t>(930 * (int64_t)na, 2400) + 3000;
+  };
   struct Unit {
     int64_t cost;
     int32_t code;
   };
-  // items of cap T: (chunk index, first stage, end stage)
-  auto make_items = [&](int32_t T, std::vector<std::array<int32_t, 3>>& out) {
+  // items under caps T: (chunk index, first stage, end stage)
+  auto make_items = [&](const int32_t* T, std::vector<std::array<int32_t, 3>>& out) {
     out.clear();
     for (size_t ci = 0; ci < chunks.size(); ++ci) {
       const Chunk& c = chunks[ci];
-      const int32_t parts = (c.stages + T - 1) / T;
+      const int32_t t = T[gi(c.na)];
+      const int32_t parts = (c.stages + t - 1) / t;
       for (int32_t k = 0; k < parts; ++k)
         out.push_back({(int32_t)ci, (int32_t)((int64_t)c.stages * k / parts),
                        (int32_t)((int64_t)c.stages * (k + 1) / parts)});
     }
+  };
+  auto count_items = [&](const int32_t* T) {
+    int64_t n = 0;
+    for (const Chunk& c : chunks) n += (c.stages + T[gi(c.na)] - 1) / T[gi(c.na)];
+    return n;
   };
   // LPT spread of the units of `its` over at most C_max CTAs; returns the makespan
   auto spread = [&](const std::vector<std::array<int32_t, 3>>& its, std::vector<std::vector<int32_t>>* lists) {
@@ -162,22 +177,28 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
     }
     return makespan;
   };
-  // caps from the longest chunk down, while the units stay within 16 per CTA; a cap that
-  // cuts every chunk into as many items as the previous one makes the same items
   std::vector<std::array<int32_t, 3>> its;
-  int32_t T = max_stages;
-  int64_t best = -1, last_count = -1;
-  for (int32_t t = max_stages; t >= 1; --t) {
-    int64_t count = 0;
-    for (const Chunk& c : chunks) count += (c.stages + t - 1) / t;
-    if (count == last_count) continue;
-    last_count = count;
-    if (t < max_stages && count * num_kv_heads > 16 * (int64_t)C_max) break;
-    make_items(t, its);
-    const int64_t m = spread(its, nullptr);
-    if (best < 0 || m < best) {
-      best = m;
-      T = t;
+  int32_t T[3] = {max_stages[0], max_stages[1], max_stages[2]};
+  make_items(T, its);
+  int64_t best = spread(its, nullptr);
+  for (int round = 0; round < 2; ++round) {
+    for (int g = 0; g < 3; ++g) {
+      if (!present[g]) continue;
+      int32_t trial[3] = {T[0], T[1], T[2]};
+      int64_t last_count = -1;
+      for (int32_t t = max_stages[g]; t >= 1; --t) {
+        trial[g] = t;
+        const int64_t count = count_items(trial);
+        if (count == last_count) continue;  // the same items as the previous cap
+        last_count = count;
+        if (count * num_kv_heads > 16 * (int64_t)C_max) break;  // at most 16 units per CTA
+        make_items(trial, its);
+        const int64_t m = spread(its, nullptr);
+        if (m < best) {
+          best = m;
+          T[g] = t;
+        }
+      }
     }
   }
   make_items(T, its);
@@ -206,7 +227,7 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
   }
   const int32_t n_ctas = (int32_t)lists.size();
   const int64_t n_units = (int64_t)n_items * num_kv_heads;
-  const int64_t need = (int64_t)items.size() + n_agents + 1 + n_slots + n_ctas + 1 + n_units;
+  const int64_t need = (int64_t)items.size() + n_agents + 1 + n_slots + n_units * FORKKV_PLAN_UNIT_INTS;
   if (need > INT32_MAX) return FORKKV_ERR_INVALID_ARG;
   info->n_items = n_items;
   info->n_slots = n_slots;
@@ -224,14 +245,28 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
     for (int32_t s : agent_slots[a]) sl[k++] = s;
   }
   off[n_agents] = k;
-  int32_t* cta_off = sl + n_slots;
-  int32_t* units = cta_off + n_ctas + 1;
-  k = 0;
+  // unit records: CTA c starts at record c, its later units follow from n_ctas on, each
+  // record naming the next one of its CTA
+  int32_t* units = sl + n_slots;
+  std::fill(units, units + n_units * FORKKV_PLAN_UNIT_INTS, 0);
+  int32_t later = n_ctas;
   for (int32_t c = 0; c < n_ctas; ++c) {
-    cta_off[c] = k;
-    for (int32_t u : lists[c]) units[k++] = u;
+    int32_t r = c;
+    for (size_t j = 0; j < lists[c].size(); ++j) {
+      const int32_t code = lists[c][j];
+      const int32_t* it = &items[(size_t)(code / num_kv_heads) * FORKKV_PLAN_ITEM_INTS];
+      int32_t* u = units + (int64_t)r * FORKKV_PLAN_UNIT_INTS;
+      const int32_t next = j + 1 < lists[c].size() ? later++ : -1;
+      u[0] = it[0];                   // first logical page
+      u[1] = it[1];                   // end logical page
+      u[2] = it[2];                   // agents in the group
+      u[3] = code % num_kv_heads;     // KV head
+      u[4] = it[12];                  // first partial slot
+      u[5] = next;                    // the CTA's next unit
+      for (int32_t x = 0; x < kMaxGroup; ++x) u[6 + x] = it[4 + x];
+      r = next;
+    }
   }
-  cta_off[n_ctas] = k;
   return FORKKV_OK;
 }
 

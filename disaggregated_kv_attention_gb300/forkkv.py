@@ -26,6 +26,7 @@ BASE_TILE_BYTES = 4096
 RES_TILE_BYTES = 512
 ROPE_ROW_BYTES = 256
 PLAN_ITEM_INTS = 16
+PLAN_UNIT_INTS = 16
 JOB_BASE = 0
 JOB_RES = 1
 FORK_SHARE_RES = 1

@@ -81,6 +81,7 @@ extern "C" {
 #define FORKKV_RES_TILE_BYTES 512      /* 16 rows x 16 bf16                  */
 #define FORKKV_ROPE_ROW_BYTES 256      /* one position of the rotation table */
 #define FORKKV_PLAN_ITEM_INTS 16       /* int32 per decode work item         */
+#define FORKKV_PLAN_UNIT_INTS 16       /* int32 per decode unit record       */
 
 /* Message for a status code (static string). */
 const char* forkkv_strerror(int32_t code);
@@ -215,9 +216,12 @@ int32_t forkkv_rope_table_build(double rope_theta, int32_t n_positions, void* ta
  *              or 4)  [3] pages per stage (8)  [4..11] agent indices (slots past
  *              n_agents repeat the first)  [12] first partial slot
  *   slot CSR   n_agents + 1 offsets, then n_slots slots (each agent's partials)
- *   cta_off    n_ctas + 1 offsets into units
- *   units      n_units codes item * num_kv_heads + head, CTA c taking
- *              units[cta_off[c] .. cta_off[c + 1]) in that order */
+ *   units      n_units = n_items * num_kv_heads records of FORKKV_PLAN_UNIT_INTS,
+ *              one per (item, KV head): [0] first logical page  [1] end logical
+ *              page  [2] n_agents  [3] KV head  [4] first partial slot  [5] record
+ *              of the same CTA's next unit, or -1  [6..9] agent indices  [10..15]
+ *              zero.  CTA c of the decode kernel starts at record c (c < n_ctas)
+ *              and follows the links. */
 typedef struct {
   int32_t n_items;     /* work items */
   int32_t n_slots;     /* partial-result slots */

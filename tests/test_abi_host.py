@@ -201,17 +201,34 @@ def test_plan_covers_every_page_once(shape, target):
     items = plan[:info.n_items * fk.PLAN_ITEM_INTS].reshape(info.n_items, fk.PLAN_ITEM_INTS)
     off = plan[info.n_items * fk.PLAN_ITEM_INTS:][:A + 1]
     rest = plan[info.n_items * fk.PLAN_ITEM_INTS + A + 1:]
-    slots, rest = rest[:info.n_slots], rest[info.n_slots:]
-    cta_off, units = rest[:info.n_ctas + 1], rest[info.n_ctas + 1:]
-    assert info.plan_ints == plan.size and len(units) == info.n_units == info.n_items * hkv
-    # the schedule: at most target (152 for 0) CTAs, none idle, every (item, head) unit once
+    slots, units = rest[:info.n_slots], rest[info.n_slots:]
+    assert info.plan_ints == plan.size and units.size == info.n_units * fk.PLAN_UNIT_INTS
+    assert info.n_units == info.n_items * hkv
+    units = units.reshape(info.n_units, fk.PLAN_UNIT_INTS)
+    # the schedule: at most target (152 for 0) CTAs, none idle, every (item, head) unit once,
+    # each record a copy of its item's fields
     assert 1 <= info.n_ctas <= (target or 152)
-    assert cta_off[0] == 0 and cta_off[-1] == info.n_units and np.all(np.diff(cta_off) >= 1)
-    assert sorted(units.tolist()) == list(range(info.n_units))
+    by_slot = {it[12]: i for i, it in enumerate(items)}
+    records, pairs, loads = set(), set(), []
+    cost = lambda it: ((it[1] - it[0] + 7) // 8) * max(930 * it[2], 2400) + 3000
+    for c in range(info.n_ctas):
+        r, load = c, 0
+        while r != -1:
+            assert 0 <= r < info.n_units and r not in records and (r < info.n_ctas) == (r == c)
+            records.add(r)
+            u = units[r]
+            i = by_slot[u[4]]
+            it = items[i]
+            assert list(u[:3]) == list(it[:3]) and list(u[6:10]) == list(it[4:8]) and not u[10:].any()
+            assert 0 <= u[3] < hkv and (i, u[3]) not in pairs
+            pairs.add((i, u[3]))
+            load += cost(it)
+            r = u[5]
+        loads.append(load)
+    assert len(records) == len(pairs) == info.n_units
     # greedy list scheduling bound: no CTA ends later than the mean load plus one unit
-    cost = np.array([((it[1] - it[0] + 7) // 8) * (it[2] + 1) + 2 for it in items]).repeat(hkv)
-    loads = np.array([cost[units[cta_off[c]:cta_off[c + 1]]].sum() for c in range(info.n_ctas)])
-    assert loads.max() <= cost.sum() / info.n_ctas + cost.max()
+    all_costs = [cost(it) for it in items] * hkv
+    assert max(loads) <= sum(all_costs) / info.n_ctas + max(all_costs)
     cover = {}
     slot_owner = {}
     for i, it in enumerate(items):
