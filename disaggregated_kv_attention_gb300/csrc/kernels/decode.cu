@@ -49,6 +49,7 @@ namespace fkv {
 namespace {
 
 constexpr int kMaxGroup = 4;                 // agents per work unit
+constexpr int kMaxGroupQ = 8;                // query heads per KV head
 constexpr int kBlockPages = 8;               // 128 keys per block
 constexpr int kRopeWarps = 8;                // two per TMEM lane quadrant
 constexpr int kSoftWarp0 = 2 + kRopeWarps;   // first of the four softmax warps
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     // k_res tiles as soon as that agent's slot (four steps back) is free, then the V tiles
     // with every agent's v_res tiles.  Every wait is for a buffer's previous user.  Page ids
     // come one per lane (lane p < 8 the base page p, lane 8 a + p the residual page p of agent
-    // a) and are requested a block ahead.
+    // a) and are requested two blocks ahead.
     const int pg = lane & 7, ag = lane >> 3;
     int32_t r_nxt;
     const int32_t r0 = first_unit(a);
@@ -469,12 +470,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       ++kbl;
       return true;
     };
-    Blk nx{};
+    Blk nx{}, nx2{};  // the next two blocks
     bool more = next_block(nx);
+    bool more2 = more && next_block(nx2);
     int g = 0, kn = 0;  // blocks copied, k_res steps copied
     while (ok && more) {
       Blk b = nx;
-      more = next_block(nx);  // the next block's ids go out now
+      nx = nx2;
+      more = more2;
+      if (more2) more2 = next_block(nx2);  // the ids of the block after next go out now
       if ((uint32_t)b.bid >= (uint32_t)a.num_base_pages) {
         flag_status(a.status, kDevBadPage);
         b.bid = 0;
@@ -1027,18 +1031,21 @@ struct CombineArgs {
   __nv_bfloat16* out;        // [A][Hq][128]
 };
 
-constexpr int kCombineSlots = 1024;  // slots handled per pass
+constexpr int kCombineChunk = 16;  // slots merged per pass (their partials held in registers)
 
-// One CTA per (agent, KV head, query head): log-sum-exp merge of the agent's
-// partials, then out = (acc + acc_r B_v[:, hD:(h+1)D]) / l.  All partial loads
-// of a pass are independent, so their latencies overlap.
-__global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__ CombineArgs a) {
-  const int agent = blockIdx.x, h = blockIdx.y, gq = blockIdx.z, d = threadIdx.x;
-  const int G = a.G;
-  __shared__ float s_w[kCombineSlots];
-  __shared__ int32_t s_slot[kCombineSlots];
-  __shared__ float s_red[4];
-  __shared__ float s_accr[kRank];
+// One CTA per (agent, KV head), one thread per (query head, d): log-sum-exp merge of the
+// agent's partials, then out = (acc + acc_r B_v[:, hD:(h+1)D]) / l.  A pass brings the slot
+// ids, then every (m, l) and this thread's partial of each slot at once, so that only three
+// rounds of loads stand between the launch and the result; the running maximum carries
+// across passes.
+__global__ void __launch_bounds__(kMaxGroupQ * kHeadDim) decode_combine_kernel(const __grid_constant__ CombineArgs a) {
+  const int agent = blockIdx.x, h = blockIdx.y, G = a.G;
+  const int tid = threadIdx.x, gq = tid / kHeadDim, d = tid % kHeadDim;
+  __shared__ int32_t s_slot[kCombineChunk];
+  __shared__ float s_m[kMaxGroupQ][kCombineChunk], s_l[kMaxGroupQ][kCombineChunk];
+  __shared__ float s_accr[kMaxGroupQ][kRank];
+  __shared__ float s_lsum[kMaxGroupQ];
+  __shared__ float s_bv[kRank][kHeadDim];  // B_v[:, hD:(h+1)D] of the agent's adapter
   int32_t s_begin, s_end;
   if (a.csr_off) {
     s_begin = a.csr_off[agent];
@@ -1048,62 +1055,71 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     s_end = s_begin + a.chunks;
   }
   if (s_begin < 0 || s_end < s_begin || s_end > a.n_slots) {
-    if (d == 0) flag_status(a.status, kDevBadArg);
+    if (tid == 0) flag_status(a.status, kDevBadArg);
     s_end = s_begin = 0;
   }
   int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
   if ((uint32_t)adapter >= (uint32_t)a.n_adapters) adapter = 0;
-  const __nv_bfloat16* Bv = a.B_v + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim + d;
-  float bv[kRank];
-#pragma unroll
-  for (int k = 0; k < kRank; ++k) bv[k] = __bfloat162float(Bv[(int64_t)k * a.hkv * kHeadDim]);
+  const __nv_bfloat16* Bv = a.B_v + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim;
+  for (int i = tid; i < kRank * kHeadDim; i += blockDim.x)
+    s_bv[i / kHeadDim][i % kHeadDim] = __bfloat162float(Bv[(int64_t)(i / kHeadDim) * a.hkv * kHeadDim + i % kHeadDim]);
 
-  // pass 1: global maximum of the reference maxima
-  float M = -INFINITY;
-  for (int i = s_begin + d; i < s_end; i += 128) {
-    int32_t slot = a.csr_off ? a.csr_slots[i] : i;
-    if ((uint32_t)slot >= (uint32_t)a.n_slots) slot = -1;
-    if (slot >= 0) M = fmaxf(M, a.ml[(((int64_t)slot * a.hkv + h) * G + gq) * 2]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if ((d & 31) == 0) s_red[d >> 5] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-
-  float acc = 0.f, accr = 0.f, lsum = 0.f;
-  for (int b0 = s_begin; b0 < s_end; b0 += kCombineSlots) {
-    const int nb = min(kCombineSlots, s_end - b0);
-    __syncthreads();
-    for (int i = d; i < nb; i += 128) {
-      int32_t slot = a.csr_off ? a.csr_slots[b0 + i] : b0 + i;
-      float w = 0.f;
-      if ((uint32_t)slot < (uint32_t)a.n_slots) {
-        const float m = a.ml[(((int64_t)slot * a.hkv + h) * G + gq) * 2];
-        w = (m == -INFINITY || M == -INFINITY) ? 0.f : exp2f(m - M);
-      } else {
-        slot = 0;
+  float M = -INFINITY, acc = 0.f, accr = 0.f, lsum = 0.f;
+  for (int b0 = s_begin; b0 < s_end; b0 += kCombineChunk) {
+    const int nb = min(kCombineChunk, s_end - b0);
+    __syncthreads();  // the previous pass is done with the shared arrays
+    if (tid < nb) {
+      int32_t slot = a.csr_off ? a.csr_slots[b0 + tid] : b0 + tid;
+      if ((uint32_t)slot >= (uint32_t)a.n_slots) {
+        flag_status(a.status, kDevBadArg);
+        slot = -1;
       }
-      s_w[i] = w;
-      s_slot[i] = slot;
+      s_slot[tid] = slot;
     }
     __syncthreads();
-#pragma unroll 8
-    for (int i = 0; i < nb; ++i) {
-      const float w = s_w[i];
-      const int64_t rec = ((int64_t)s_slot[i] * a.hkv + h) * G + gq;
-      acc += w * a.part[rec * kPartCols + d];
-      if (d < kRank) accr += w * a.part[rec * kPartCols + kHeadDim + d];
-      if (d == 0) lsum += w * a.ml[rec * 2 + 1];
+    for (int i = tid; i < nb * G; i += blockDim.x) {  // (m, l) of every (slot, query head) of the pass
+      const int gi = i / nb, si = i - gi * nb, slot = s_slot[si];
+      const int64_t rec = ((int64_t)max(slot, 0) * a.hkv + h) * G + gi;
+      s_m[gi][si] = slot >= 0 ? a.ml[rec * 2] : -INFINITY;
+      s_l[gi][si] = slot >= 0 ? a.ml[rec * 2 + 1] : 0.f;
+    }
+    float pv[kCombineChunk], pr[kCombineChunk];  // this thread's partials of the pass
+#pragma unroll
+    for (int i = 0; i < kCombineChunk; ++i) {
+      pv[i] = pr[i] = 0.f;
+      if (i < nb) {
+        const int64_t rec = ((int64_t)max(s_slot[i], 0) * a.hkv + h) * G + gq;
+        pv[i] = a.part[rec * kPartCols + d];
+        if (d < kRank) pr[i] = a.part[rec * kPartCols + kHeadDim + d];
+      }
+    }
+    __syncthreads();
+    float Mn = M;
+    for (int i = 0; i < nb; ++i) Mn = fmaxf(Mn, s_m[gq][i]);
+    if (Mn != -INFINITY) {
+      const float sc = M == -INFINITY ? 0.f : exp2f(M - Mn);  // rescale what earlier passes gathered
+      acc *= sc;
+      accr *= sc;
+      lsum *= sc;
+#pragma unroll
+      for (int i = 0; i < kCombineChunk; ++i)
+        if (i < nb) {
+          const float m = s_m[gq][i];
+          const float w = m == -INFINITY ? 0.f : exp2f(m - Mn);
+          acc += w * pv[i];
+          accr += w * pr[i];
+          lsum += w * s_l[gq][i];
+        }
+      M = Mn;
     }
   }
-  if (d < kRank) s_accr[d] = accr;
-  if (d == 0) s_red[0] = lsum;
+  if (d < kRank) s_accr[gq][d] = accr;
+  if (d == 0) s_lsum[gq] = lsum;
   __syncthreads();
   float o = acc;
 #pragma unroll
-  for (int k = 0; k < kRank; ++k) o += s_accr[k] * bv[k];
-  lsum = s_red[0];
+  for (int k = 0; k < kRank; ++k) o += s_accr[gq][k] * s_bv[k][d];
+  lsum = s_lsum[gq];
   o = lsum > 0.f ? o / lsum : 0.f;
   a.out[((int64_t)agent * a.hkv * G + (int64_t)h * G + gq) * kHeadDim + d] = __float2bfloat16_rn(o);
 }
@@ -1221,7 +1237,7 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   c.adapter_ids = p.adapter_ids;
   c.n_adapters = p.n_adapters;
   c.out = static_cast<__nv_bfloat16*>(p.out);
-  decode_combine_kernel<<<dim3(p.n_agents, p.num_kv_heads, G), 128, 0, stream>>>(c);
+  decode_combine_kernel<<<dim3(p.n_agents, p.num_kv_heads), G * kHeadDim, 0, stream>>>(c);
   return cudaGetLastError();
 }
 
