@@ -118,6 +118,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// Named barrier `id` (1..15) among `count` threads (a multiple of 32; whole warps take part).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // One-dimensional bulk copy global -> shared completing on an mbarrier
 // (dst, src 16-byte aligned; bytes a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

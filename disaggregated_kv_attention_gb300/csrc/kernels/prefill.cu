@@ -12,12 +12,16 @@
 //          2..5   RoPE group, one key per thread: U = Kr . B_k^T arrives in TMEM;
 //                 K = bf16(Kb + RoPE_j(U)) is written to shared memory as the
 //                 128-key operand of the next score MMA
-//          6..9   softmax group, one query row per thread: S from TMEM, causal
-//                 mask, online softmax; P (bf16) is written back over S in TMEM
+//          6..13  softmax group, two warps per query row (half of the keys each):
+//                 S from TMEM, causal mask, online softmax; P (bf16) is written
+//                 back over S in TMEM
 //   MMAs per block:  U[128x128]   = Kr[128x16] . B_k^T           (smem x smem)
 //                    S[128x128]   = Q[128x128] . K^T             (smem x smem)
 //                    O[128x128]  += P[128x128] . Vb[128x128]      (tmem x smem)
 //                    O_r[128x16] += P . Vr[128x16]                (tmem x smem)
+//   U, S and P of a block share one of two TMEM buffers (by block parity), so
+//   the next block's U, rotation and S run while this block's softmax does;
+//   the MMA warp issues, per block, U and S of block b, then P.V of block b - 1.
 //   epilogue: out = (O + O_r . B_v[:, hD:(h+1)D]) / l, B_v applied once per row.
 // Every wait is on an mbarrier with a bounded spin; a timeout sets the device
 // status word instead of hanging.
@@ -33,10 +37,12 @@ namespace {
 constexpr int kRows = 128;
 constexpr int kBlockPages = 8;
 constexpr int kBlockKeys = kBlockPages * kPage;
-constexpr int kThreads = 10 * 32;
+constexpr int kSoftWarp0 = 6;  // warps 2..5 rotate keys, 6..13 run the softmax
+constexpr int kThreads = 14 * 32;
 
 // shared memory (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 1024;                     // Q, K-major 128B-swizzled [2][128 rows][128 B]
+constexpr int kOffPmax = 1024;                  // [2 parities][2 halves][128 rows] partial row maxima
+constexpr int kOffQ = 3072;                     // Q, K-major 128B-swizzled [2][128 rows][128 B]
 constexpr int kOffKF = kOffQ + 32768;           // full keys of one block, same layout
 constexpr int kOffStage = kOffKF + 32768;       // 2 stages
 constexpr int kStageBytes = 73728;
@@ -44,13 +50,15 @@ constexpr int kStK = 0, kStV = 32768, kStKR = 65536, kStVR = 69632;  // 8 K tile
 constexpr int kOffBk = kOffStage + 2 * kStageBytes;  // B_k^T, K-major 32B-swizzled [128 d][16 r]
 constexpr int kOffBv = kOffBk + 4096;                // B_v slice [16][128] bf16
 constexpr int kSmemBytes = kOffBv + 4096 + 1024;     // + slack for aligning the base
+static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have");
 
-// tensor memory columns
-constexpr uint32_t kTmU = 0, kTmS = 128, kTmO = 256, kTmOr = 384, kTmCols = 512;
+// tensor memory columns: two buffers (U, then S, then P over S) by block parity, O, O_r
+constexpr uint32_t kTmBuf = 0, kTmO = 256, kTmOr = 384, kTmCols = 512;
 
 // mbarrier indices
-enum { kFull0, kFull1, kEmpty0, kEmpty1, kUFull, kUFree, kKFReady, kKFFree, kSFull, kPFull, kPVDone, kQReady,
-       kBkReady, kNumBars };
+enum { kFull0, kFull1, kEmpty0, kEmpty1, kUFull0, kUFull1, kKFReady, kKFFree, kSFull0, kSFull1, kPFull0, kPFull1,
+       kPVDone0, kPVDone1, kQReady, kBkReady, kMmaDone, kNumBars };
+static_assert(kNumBars * 8 <= 256, "barriers overlap the state that follows them");
 
 struct PrefillArgs {
   const uint8_t* k_base;
@@ -82,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 256);
   int32_t* s_meta = reinterpret_cast<int32_t*>(smem + 272);
+  float* s_pmax = reinterpret_cast<float*>(smem + kOffPmax);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int agent = blockIdx.y, h = blockIdx.z;
@@ -97,15 +106,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bars[kFull1], 1);
     mbar_init(&bars[kEmpty0], 5);  // 4 RoPE warps + the MMA commit after the value products
     mbar_init(&bars[kEmpty1], 5);
-    mbar_init(&bars[kUFull], 1);
-    mbar_init(&bars[kUFree], 4);
+    mbar_init(&bars[kUFull0], 1);
+    mbar_init(&bars[kUFull1], 1);
     mbar_init(&bars[kKFReady], 4);
     mbar_init(&bars[kKFFree], 1);
-    mbar_init(&bars[kSFull], 1);
-    mbar_init(&bars[kPFull], 4);
-    mbar_init(&bars[kPVDone], 1);
-    mbar_init(&bars[kQReady], 4);
+    mbar_init(&bars[kSFull0], 1);
+    mbar_init(&bars[kSFull1], 1);
+    mbar_init(&bars[kPFull0], 8);  // every softmax warp
+    mbar_init(&bars[kPFull1], 8);
+    mbar_init(&bars[kPVDone0], 1);
+    mbar_init(&bars[kPVDone1], 1);
+    mbar_init(&bars[kQReady], 8);
     mbar_init(&bars[kBkReady], 4);
+    mbar_init(&bars[kMmaDone], 1);
     mbar_fence_init();
     // keys this CTA may see: up to the largest query position of its rows (and L)
     const int t_first = (int)(row0 / G);
@@ -182,6 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
+    // Per block b: U(b) into buffer b % 2 (once P.V of block b - 2 is done with it), S(b)
+    // over U(b) once the rotation group has built K(b), then P.V of block b - 1.
     if (lane == 0) {
       const uint32_t idU = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idS = tc::idesc_bf16(128, 128, 0, 0);
@@ -189,48 +204,62 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const uint32_t idPVr = tc::idesc_bf16(128, 16, 0, 1);
       const uint32_t aQ = smem_u32(sQ), aKF = smem_u32(sKF), aBk = smem_u32(sBk);
       bool ok = mbar_wait(&bars[kQReady], 0, a.status) && mbar_wait(&bars[kBkReady], 0, a.status);
-      int issued = 0;
+      // P.V of block c: A = P from its buffer (keys 0..63 at columns 0..31, keys 64..127 at 64..95)
+      auto issue_pv = [&](int c) {
+        const uint32_t buf = tm + kTmBuf + 128 * (c & 1);
+        const uint32_t st = smem_u32(smem + kOffStage + (c & 1) * kStageBytes);
+        const int nvp = min(kBlockPages, n_pages - c * kBlockPages);
+        for (int ks = 0; ks < nvp; ++ks)
+          tc::mma_ts(tm + kTmO, buf + (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4)),
+                     tc::smem_desc(st + kStV + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B), idPV, (c > 0 || ks > 0));
+        for (int ks = 0; ks < nvp; ++ks)
+          tc::mma_ts(tm + kTmOr, buf + (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4)),
+                     tc::smem_desc(st + kStVR + ks * kResTile, 4096, 256, tc::kSwizzle32B), idPVr, (c > 0 || ks > 0));
+        tc::commit(&bars[kPVDone0 + (c & 1)]);
+        tc::commit(&bars[kEmpty0 + (c & 1)]);
+      };
       for (int b = 0; b < n_blocks && ok; ++b) {
         const int stage = b & 1;
         const uint32_t st = smem_u32(smem + kOffStage + stage * kStageBytes);
-        const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
-        ok = mbar_wait(&bars[kFull0 + stage], (b >> 1) & 1, a.status);
-        if (ok && b > 0) ok = mbar_wait(&bars[kUFree], (b - 1) & 1, a.status);
+        const uint32_t buf = tm + kTmBuf + 128 * stage;
+        ok = mbar_wait(&bars[kFull0 + stage], (b >> 1) & 1, a.status) &&
+             (b < 2 || mbar_wait(&bars[kPVDone0 + stage], ((b >> 1) - 1) & 1, a.status));
         if (!ok) break;
         tc::fence_after();
-        tc::mma_ss(tm + kTmU, tc::smem_desc(st + kStKR, 16, 256, tc::kSwizzle32B),
-                   tc::smem_desc(aBk, 16, 256, tc::kSwizzle32B), idU, 0);
-        tc::commit(&bars[kUFull]);
+        tc::mma_ss(buf, tc::smem_desc(st + kStKR, 16, 256, tc::kSwizzle32B), tc::smem_desc(aBk, 16, 256, tc::kSwizzle32B),
+                   idU, 0);
+        tc::commit(&bars[kUFull0 + stage]);
         ok = mbar_wait(&bars[kKFReady], b & 1, a.status);
-        if (ok && b > 0) ok = mbar_wait(&bars[kPVDone], (b - 1) & 1, a.status);
         if (!ok) break;
         tc::fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc::mma_ss(tm + kTmS, tc::smem_desc(aQ + off, 16, 1024, tc::kSwizzle128B),
+          tc::mma_ss(buf, tc::smem_desc(aQ + off, 16, 1024, tc::kSwizzle128B),
                      tc::smem_desc(aKF + off, 16, 1024, tc::kSwizzle128B), idS, ks > 0);
         }
-        tc::commit(&bars[kSFull]);
+        tc::commit(&bars[kSFull0 + stage]);
         tc::commit(&bars[kKFFree]);
-        ok = mbar_wait(&bars[kPFull], b & 1, a.status);
-        if (!ok) break;
-        tc::fence_after();
-        for (int ks = 0; ks < nvp; ++ks)
-          tc::mma_ts(tm + kTmO, tm + kTmS + 8 * ks,
-                     tc::smem_desc(st + kStV + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B), idPV, (b > 0 || ks > 0));
-        for (int ks = 0; ks < nvp; ++ks)
-          tc::mma_ts(tm + kTmOr, tm + kTmS + 8 * ks,
-                     tc::smem_desc(st + kStVR + ks * kResTile, 4096, 256, tc::kSwizzle32B), idPVr, (b > 0 || ks > 0));
-        tc::commit(&bars[kPVDone]);
-        tc::commit(&bars[kEmpty0 + stage]);
-        issued = b + 1;
+        if (b > 0) {
+          ok = mbar_wait(&bars[kPFull0 + ((b - 1) & 1)], ((b - 1) >> 1) & 1, a.status);
+          if (!ok) break;
+          tc::fence_after();
+          issue_pv(b - 1);
+        }
+      }
+      if (ok && n_blocks > 0) {
+        ok = mbar_wait(&bars[kPFull0 + ((n_blocks - 1) & 1)], ((n_blocks - 1) >> 1) & 1, a.status);
+        if (ok) {
+          tc::fence_after();
+          issue_pv(n_blocks - 1);
+        }
       }
       // never leave with MMAs in flight
-      if (issued > 0) mbar_wait(&bars[kPVDone], (issued - 1) & 1, a.status);
+      tc::commit(&bars[kMmaDone]);
+      mbar_wait(&bars[kMmaDone], 0, a.status);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < kSoftWarp0) {
     // ------------------------------ RoPE group ------------------------------
     const int row = 32 * (warp & 3) + lane;  // key row of the block == TMEM lane
     const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -248,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int b = 0; b < n_blocks && ok; ++b) {
       const int stage = b & 1;
       uint8_t* st = smem + kOffStage + stage * kStageBytes;
+      const uint32_t ub = tl + kTmBuf + 128 * stage;
       const int j = b * kBlockKeys + row;
       // this key's rotation row: logical 32-byte unit u sits at unit u ^ (j % 8)
       uint4 rp[8][2];
@@ -260,16 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           rp[u][1] = rrow[(u ^ (j & 7)) * 2 + 1];
         }
       }
-      ok = mbar_wait(&bars[kFull0 + stage], (b >> 1) & 1, a.status) && mbar_wait(&bars[kUFull], b & 1, a.status);
-      if (ok && b > 0) ok = mbar_wait(&bars[kKFFree], (b - 1) & 1, a.status);
+      ok = mbar_wait(&bars[kFull0 + stage], (b >> 1) & 1, a.status) &&
+           mbar_wait(&bars[kUFull0 + stage], (b >> 1) & 1, a.status);
+      if (ok && b > 0) ok = mbar_wait(&bars[kKFFree], (b - 1) & 1, a.status);  // S(b - 1) is done with sKF
       if (!ok) break;
       tc::fence_after();
       const uint8_t* kt = st + kStK + p * kBaseTile;
 #pragma unroll
       for (int c = 0; c < 64; c += 16) {
         uint32_t ulo[16], uhi[16];
-        tc::ld16(tl + kTmU + c, ulo);
-        tc::ld16(tl + kTmU + 64 + c, uhi);
+        tc::ld16(ub + c, ulo);
+        tc::ld16(ub + 64 + c, uhi);
         uint4 kl[2], kh[2];
         kl[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c));
         kl[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 8));
@@ -300,8 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 72)) = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
       }
       tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kUFree]);
       // keys past the sequence: zero their value rows so that 0 * (never-written data) stays 0
       const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
       if (j >= L && p < nvp) {
@@ -321,23 +350,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   } else {
     // ------------------------------ softmax group ------------------------------
-    const int qr = 32 * (warp & 3) + lane;  // query row of the tile == TMEM lane
-    const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
+    // Two warps per TMEM lane quadrant: half sh holds the keys [64 sh, 64 sh + 64) of each
+    // block and the output columns d in [64 sh, 64 sh + 64); the two halves of a row meet
+    // through shared memory and a named barrier (one per quadrant).
+    const int q4 = warp & 3, sh = (warp - kSoftWarp0) >> 2;
+    const int qr = 32 * q4 + lane;  // query row of the tile == TMEM lane
+    const uint32_t tl = tm + ((uint32_t)(32 * q4) << 16);
+    const uint32_t pair_bar = 1 + q4, pair_threads = 64;
     const int64_t f = row0 + qr;
     const bool valid = f < n_rows;
     const int64_t tq = valid ? f / G : 0;
     const int gq = valid ? (int)(f % G) : 0;
     const int32_t pos = valid ? a.positions[(int64_t)agent * a.q_len + tq] : -1;
     const int64_t orow = (((int64_t)agent * a.q_len + tq) * a.hkv * G + (int64_t)h * G + gq) * kHeadDim;
-    {  // Q row into the K-major swizzled tile; B_v slice for the epilogue
+    {  // this half of the Q row into the K-major swizzled tile; this half of the B_v slice
       const uint4* src = reinterpret_cast<const uint4*>(a.q + orow);
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
+      for (int ch = 8 * sh; ch < 8 * sh + 8; ++ch) {
         const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(sQ + tc::sw128_off(128, qr, ch * 8)) = v;
       }
       const __nv_bfloat16* Bv = a.B_v + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim;
-      for (int i = qr; i < kRank * kHeadDim / 8; i += 128) {
+      for (int i = qr + 128 * sh; i < kRank * kHeadDim / 8; i += 256) {
         const int k = i / 16, ch = i % 16;
         *reinterpret_cast<uint4*>(sBv + (k * kHeadDim + ch * 8) * 2) =
             *reinterpret_cast<const uint4*>(Bv + (int64_t)k * a.hkv * kHeadDim + ch * 8);
@@ -346,19 +380,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kQReady]);
     }
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
     bool ok = true;
-    for (int b = 0; b < n_blocks && ok; ++b) {
-      ok = mbar_wait(&bars[kSFull], b & 1, a.status);
-      if (!ok) break;
+    // No early exit: both warps of a quadrant take every named barrier; after a wait that timed
+    // out (the status word says so) the loop runs on without waiting and its values are void.
+    for (int b = 0; b < n_blocks; ++b) {
+      const uint32_t buf = kTmBuf + 128 * (b & 1);
+      ok = ok && mbar_wait(&bars[kSFull0 + (b & 1)], (b >> 1) & 1, a.status);
       tc::fence_after();
-      const int kbase = b * kBlockKeys;
+      const int kbase = b * kBlockKeys + 64 * sh;
       float bm = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
+      for (int c = 0; c < 64; c += 32) {
         uint32_t v0[16], v1[16];
-        tc::ld16(tl + kTmS + c, v0);
-        tc::ld16(tl + kTmS + c + 16, v1);
+        tc::ld16(tl + buf + 64 * sh + c, v0);
+        tc::ld16(tl + buf + 64 * sh + c + 16, v1);
         tc::wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -367,16 +403,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           if (j < L && j <= pos) bm = fmaxf(bm, s);
         }
       }
+      // the row's block maximum: both halves (parity-alternating slots, so one barrier per block)
+      s_pmax[((b & 1) * 2 + sh) * 128 + qr] = bm;
+      named_sync(pair_bar, pair_threads);
+      bm = fmaxf(bm, s_pmax[((b & 1) * 2 + (sh ^ 1)) * 128 + qr]);
       const bool need = bm > m + 8.f;  // lazy rescale: only when the max grows by 2^8
       if (__any_sync(0xffffffffu, need)) {
         const float mn = need ? bm : m;
         const float alpha = (need && m != -INFINITY) ? exp2f(m - mn) : 1.f;
         if (b > 0) {
-          ok = mbar_wait(&bars[kPVDone], (b - 1) & 1, a.status);  // the accumulators are stable
+          // O (this half's columns; the first half also O_r) is stable once P.V of block b - 1 is done
+          ok = ok && mbar_wait(&bars[kPVDone0 + ((b - 1) & 1)], ((b - 1) >> 1) & 1, a.status);
           tc::fence_after();
 #pragma unroll
-          for (int c = 0; c < 128 + 16; c += 16) {
-            const uint32_t col = c < 128 ? kTmO + c : kTmOr;
+          for (int c = 0; c < 64 + 16; c += 16) {
+            if (c == 64 && sh == 1) break;
+            const uint32_t col = c < 64 ? kTmO + 64 * sh + c : kTmOr;
             uint32_t v[16];
             tc::ld16(tl + col, v);
             tc::wait_ld();
@@ -390,11 +432,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         m = mn;
       }
       const float mu = m == -INFINITY ? 0.f : m;
+      // P over this half's S columns: keys 64 sh + 2 i, 2 i + 1 at column 64 sh + i
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
+      for (int c = 0; c < 64; c += 32) {
         uint32_t v0[16], v1[16], pw[16];
-        tc::ld16(tl + kTmS + c, v0);
-        tc::ld16(tl + kTmS + c + 16, v1);
+        tc::ld16(tl + buf + 64 * sh + c, v0);
+        tc::ld16(tl + buf + 64 * sh + c + 16, v1);
         tc::wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -409,16 +452,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           }
           pw[i] = pack_bf16(pr[0], pr[1]);
         }
-        tc::st16(tl + kTmS + (c >> 1), pw);  // P over the columns of S already read
+        tc::st16(tl + buf + 64 * sh + (c >> 1), pw);  // over columns of S this thread already read
       }
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kPFull]);
+      if (lane == 0) mbar_arrive(&bars[kPFull0 + (b & 1)]);
     }
-    // epilogue
-    if (ok && n_blocks > 0) ok = mbar_wait(&bars[kPVDone], (n_blocks - 1) & 1, a.status);
+    // epilogue: the row sum of both halves, then this half's output columns
+    if (ok && n_blocks > 0) ok = mbar_wait(&bars[kPVDone0 + ((n_blocks - 1) & 1)], ((n_blocks - 1) >> 1) & 1, a.status);
     if (ok) ok = mbar_wait(&bars[kQReady], 0, a.status);  // every thread's part of the B_v slice is in place
+    named_sync(pair_bar, pair_threads);  // both halves are past their last use of s_pmax
+    s_pmax[sh * 128 + qr] = l;
+    named_sync(pair_bar, pair_threads);
+    l += s_pmax[(sh ^ 1) * 128 + qr];
     tc::fence_after();
     uint32_t orr[16];
     tc::ld16(tl + kTmOr, orr);
@@ -427,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const float inv = have ? 1.f / l : 0.f;
     const __nv_bfloat16* sbv = reinterpret_cast<const __nv_bfloat16*>(sBv);
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 16) {
+    for (int c = 64 * sh; c < 64 * sh + 64; c += 16) {
       uint32_t v[16];
       tc::ld16(tl + kTmO + c, v);
       tc::wait_ld();
