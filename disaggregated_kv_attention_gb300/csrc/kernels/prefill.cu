@@ -9,19 +9,20 @@
 //                 into a 2-stage ring with 1-D bulk async copies (one per run of
 //                 consecutive page ids)
 //          1      allocates 512 TMEM columns; one lane issues every MMA
-//          2..5   RoPE group, one key per thread: U = Kr . B_k^T arrives in TMEM;
-//                 K = bf16(Kb + RoPE_j(U)) is written to shared memory as the
-//                 128-key operand of the next score MMA
-//          6..13  softmax group, two warps per query row (half of the keys each):
-//                 S from TMEM, causal mask, online softmax; P (bf16) is written
-//                 back over S in TMEM
+//          2..9   RoPE group, two warps per key (half of the rotation pairs each):
+//                 U = Kr . B_k^T arrives in TMEM; K = bf16(Kb + RoPE_j(U)) is written
+//                 to shared memory as the 128-key operand of the next score MMA
+//          10..17 softmax group, two warps per query row (half of the keys each):
+//                 S from TMEM, causal mask, online softmax; P (bf16) to shared
+//                 memory as the A operand of the value products
 //   MMAs per block:  U[128x128]   = Kr[128x16] . B_k^T           (smem x smem)
 //                    S[128x128]   = Q[128x128] . K^T             (smem x smem)
-//                    O[128x128]  += P[128x128] . Vb[128x128]      (tmem x smem)
-//                    O_r[128x16] += P . Vr[128x16]                (tmem x smem)
-//   U, S and P of a block share one of two TMEM buffers (by block parity), so
-//   the next block's U, rotation and S run while this block's softmax does;
-//   the MMA warp issues, per block, U and S of block b, then P.V of block b - 1.
+//                    O[128x128]  += P[128x128] . Vb[128x128]      (smem x smem)
+//                    O_r[128x16] += P . Vr[128x16]                (smem x smem)
+//   U and S of a block share one of two TMEM buffers (by block parity), freed
+//   as soon as the softmax has read S, so the next blocks' U, rotation and S
+//   run while this block's softmax does; the MMA warp issues whichever product
+//   is ready first.
 //   epilogue: out = (O + O_r . B_v[:, hD:(h+1)D]) / l, B_v applied once per row.
 // Every wait is on an mbarrier with a bounded spin; a timeout sets the device
 // status word instead of hanging.
@@ -37,28 +38,42 @@ namespace {
 constexpr int kRows = 128;
 constexpr int kBlockPages = 8;
 constexpr int kBlockKeys = kBlockPages * kPage;
-constexpr int kSoftWarp0 = 6;  // warps 2..5 rotate keys, 6..13 run the softmax
-constexpr int kThreads = 14 * 32;
+constexpr int kRopeWarps = 8, kSoftWarp0 = 2 + kRopeWarps;  // warps 2..9 rotate keys, 10..17 run the softmax
+constexpr int kThreads = (kSoftWarp0 + 8) * 32;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int kOffPmax = 1024;                  // [2 parities][2 halves][128 rows] partial row maxima
-constexpr int kOffQ = 3072;                     // Q, K-major 128B-swizzled [2][128 rows][128 B]
-constexpr int kOffKF = kOffQ + 32768;           // full keys of one block, same layout
-constexpr int kOffStage = kOffKF + 32768;       // 2 stages
-constexpr int kStageBytes = 73728;
-constexpr int kStK = 0, kStV = 32768, kStKR = 65536, kStVR = 69632;  // 8 K tiles, 8 V tiles, 8 k_res, 8 v_res
-constexpr int kOffBk = kOffStage + 2 * kStageBytes;  // B_k^T, K-major 32B-swizzled [128 d][16 r]
+constexpr int kOffKF = 3072;                    // full keys of one block, K-major 128B-swizzled [2][128 rows][128 B]
+constexpr int kOffKStage = kOffKF + 32768;      // 2 stages of [8 K tiles | 8 k_res tiles]
+constexpr int kOffVStage = kOffKStage + 2 * 36864;  // 2 stages of [8 V tiles | 8 v_res tiles]
+constexpr int kStageBytes = 36864, kStRes = 32768;  // the residual tiles follow the base tiles
+constexpr int kOffP = kOffVStage + 2 * kStageBytes;  // P, K-major 128B-swizzled [2][128 rows][128 B]
+constexpr int kOffBk = kOffP + 32768;                // B_k^T, K-major 32B-swizzled [128 d][16 r]
 constexpr int kOffBv = kOffBk + 4096;                // B_v slice [16][128] bf16
 constexpr int kSmemBytes = kOffBv + 4096 + 1024;     // + slack for aligning the base
 static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have");
 
-// tensor memory columns: two buffers (U, then S, then P over S) by block parity, O, O_r
-constexpr uint32_t kTmBuf = 0, kTmO = 256, kTmOr = 384, kTmCols = 512;
+// tensor memory columns: two buffers (U, then S) by block parity, O, O_r
+// and Q (bf16 pairs: the A operand of the score product)
+constexpr uint32_t kTmBuf = 0, kTmO = 256, kTmOr = 384, kTmQ = 400, kTmCols = 512;
 
 // mbarrier indices
-enum { kFull0, kFull1, kEmpty0, kEmpty1, kUFull0, kUFull1, kKFReady, kKFFree, kSFull0, kSFull1, kPFull0, kPFull1,
-       kPVDone0, kPVDone1, kQReady, kBkReady, kMmaDone, kNumBars };
+enum { kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1, kUFull0, kUFull1, kKFReady, kKFFree,
+       kSFull0, kSFull1,
+       kSFree0, kSFree1, kPFull, kPVDone, kQReady, kBkReady, kMmaDone, kNumBars };
 static_assert(kNumBars * 8 <= 256, "barriers overlap the state that follows them");
+
+// Bytes of nvp page tiles whose last page keeps only `rows` rows.
+__device__ __forceinline__ uint32_t tile_bytes_pf(bool base, int nvp, int rows) {
+  const uint32_t tile = base ? kBaseTile : kResTile, rb = base ? 128u : 32u;
+  return rows < kPage ? (uint32_t)(nvp - 1) * tile + (base ? 2u : 1u) * (uint32_t)rows * rb : (uint32_t)nvp * tile;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 struct PrefillArgs {
   const uint8_t* k_base;
@@ -102,22 +117,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if ((uint32_t)adapter >= (uint32_t)a.n_adapters) adapter = 0;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[kFull0], 1);
-    mbar_init(&bars[kFull1], 1);
-    mbar_init(&bars[kEmpty0], 5);  // 4 RoPE warps + the MMA commit after the value products
-    mbar_init(&bars[kEmpty1], 5);
+    mbar_init(&bars[kKFull0], 1);
+    mbar_init(&bars[kKFull1], 1);
+    mbar_init(&bars[kKEmpty0], kRopeWarps + 1);  // the RoPE warps (K tiles) + the U commit (k_res tiles)
+    mbar_init(&bars[kKEmpty1], kRopeWarps + 1);
+    mbar_init(&bars[kVFull0], 1);
+    mbar_init(&bars[kVFull1], 1);
+    mbar_init(&bars[kVEmpty0], 1);  // the commit after the value products
+    mbar_init(&bars[kVEmpty1], 1);
     mbar_init(&bars[kUFull0], 1);
     mbar_init(&bars[kUFull1], 1);
-    mbar_init(&bars[kKFReady], 4);
+    mbar_init(&bars[kKFReady], kRopeWarps);
     mbar_init(&bars[kKFFree], 1);
     mbar_init(&bars[kSFull0], 1);
     mbar_init(&bars[kSFull1], 1);
-    mbar_init(&bars[kPFull0], 8);  // every softmax warp
-    mbar_init(&bars[kPFull1], 8);
-    mbar_init(&bars[kPVDone0], 1);
-    mbar_init(&bars[kPVDone1], 1);
+    mbar_init(&bars[kSFree0], 8);  // every softmax warp, once its last read of S is done
+    mbar_init(&bars[kSFree1], 8);
+    mbar_init(&bars[kPFull], 8);  // every softmax warp
+    mbar_init(&bars[kPVDone], 1);
     mbar_init(&bars[kQReady], 8);
-    mbar_init(&bars[kBkReady], 4);
+    mbar_init(&bars[kBkReady], kRopeWarps);
     mbar_init(&bars[kMmaDone], 1);
     mbar_fence_init();
     // keys this CTA may see: up to the largest query position of its rows (and L)
@@ -138,120 +157,211 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int32_t key_limit = s_meta[0];
   const int n_pages = (key_limit + kPage - 1) / kPage;
   const int n_blocks = (n_pages + kBlockPages - 1) / kBlockPages;
-  uint8_t* sQ = smem + kOffQ;
   uint8_t* sKF = smem + kOffKF;
+  uint8_t* sP = smem + kOffP;
   uint8_t* sBk = smem + kOffBk;
   uint8_t* sBv = smem + kOffBv;
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
+    // Two streams in block order, K one block ahead of V: a block's K and k_res tiles once the
+    // rotation group and the U product are done with that K stage (two blocks back), its V and
+    // v_res tiles once the value products of the previous block are done with the V stage.  Rows of the last
+    // page at or past the sequence end are zeroed in shared memory instead of copied, so that
+    // a zero probability never meets never-written (possibly NaN) value rows.
     const int64_t head_base = (int64_t)h * a.num_base_pages;
-    for (int b = 0; b < n_blocks; ++b) {
-      const int stage = b & 1;
-      if (b >= 2 && !mbar_wait(&bars[kEmpty0 + stage], ((b >> 1) - 1) & 1, a.status)) break;
-      const int pbase = b * kBlockPages;
-      const int nvp = min(kBlockPages, n_pages - pbase);
+    // page id of block b held by this lane (lanes 0..7 the base pages, 8..15 the residual
+    // pages; requested, not waited for)
+    auto lane_id = [&](int b) -> int32_t {
+      const int pbase = b * kBlockPages, nvp = min(kBlockPages, n_pages - pbase);
       int32_t id = 0;
-      if (lane < nvp) {
-        id = a.bpt[(int64_t)agent * a.pt_stride + pbase + lane];
-        if ((uint32_t)id >= (uint32_t)a.num_base_pages) {
-          flag_status(a.status, kDevBadPage);
-          id = 0;
-        }
-      } else if (lane >= 8 && lane - 8 < nvp) {
-        id = a.rpt[(int64_t)agent * a.pt_stride + pbase + lane - 8];
-        if ((uint32_t)id >= (uint32_t)a.num_res_pages) {
-          flag_status(a.status, kDevBadPage);
-          id = 0;
-        }
+      if (lane < nvp) id = a.bpt[(int64_t)agent * a.pt_stride + pbase + lane];
+      else if (lane >= 8 && lane - 8 < nvp) id = a.rpt[(int64_t)agent * a.pt_stride + pbase + lane - 8];
+      return id;
+    };
+    // the ids of a block to its copying lanes: lane 0 the base ids, lane 1 the residual ids
+    auto broadcast_ids = [&](int b, int32_t id, int32_t (&ids)[8]) {
+      const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
+      if (lane < nvp && (uint32_t)id >= (uint32_t)a.num_base_pages) {
+        flag_status(a.status, kDevBadPage);
+        id = 0;
+      } else if (lane >= 8 && lane - 8 < nvp && (uint32_t)id >= (uint32_t)a.num_res_pages) {
+        flag_status(a.status, kDevBadPage);
+        id = 0;
       }
-      int32_t ids[8];
-      const int src0 = lane < 2 ? 0 : 8;  // lanes 0, 1: base page ids; lanes 2, 3: residual page ids
+      const int src0 = lane == 1 ? 8 : 0;
 #pragma unroll
       for (int pg = 0; pg < 8; ++pg) ids[pg] = __shfl_sync(0xffffffffu, id, src0 + pg);
-      uint8_t* st = smem + kOffStage + stage * kStageBytes;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[kFull0 + stage], nvp * (2 * kBaseTile + 2 * kResTile));
-      __syncwarp();
-      if (lane < 4) {
-        const uint8_t* pool = lane == 0 ? a.k_base + head_base * kBaseTile
-                              : lane == 1 ? a.v_base + head_base * kBaseTile
-                              : lane == 2 ? a.k_res : a.v_res;
-        uint8_t* dst = st + (lane == 0 ? kStK : lane == 1 ? kStV : lane == 2 ? kStKR : kStVR);
-        const uint32_t tile = lane < 2 ? kBaseTile : kResTile;
-        int r0 = 0;
-        int32_t start = ids[0];
+    };
+    // one lane's copies of a block: whole pages by runs of consecutive ids, then the first
+    // `rows` rows of the last page when rows < 16
+    auto copy_pages = [&](const uint8_t* pool, uint8_t* dst, bool base, const int32_t (&ids)[8], int nvp, int rows,
+                          uint64_t* bar) {
+      const uint32_t tile = base ? kBaseTile : kResTile, rb = base ? 128u : 32u;
+      const int full = rows < kPage ? nvp - 1 : nvp;
+      int r0 = 0;
+      int32_t start = ids[0];
 #pragma unroll
-        for (int pg = 1; pg <= 8; ++pg) {
-          if (pg <= nvp) {
-            const bool end = pg == nvp || ids[pg < 8 ? pg : 7] != ids[pg - 1] + 1;
-            if (end) {
-              bulk_g2s(dst + r0 * tile, pool + (int64_t)start * tile, (pg - r0) * tile, &bars[kFull0 + stage]);
-              r0 = pg;
-              start = ids[pg < 8 ? pg : 7];
-            }
+      for (int pg = 1; pg <= 8; ++pg) {
+        if (pg <= full) {
+          const bool end = pg == full || ids[pg < 8 ? pg : 7] != ids[pg - 1] + 1;
+          if (end) {
+            bulk_g2s(dst + r0 * tile, pool + (int64_t)start * tile, (pg - r0) * tile, bar);
+            r0 = pg;
+            start = ids[pg < 8 ? pg : 7];
           }
         }
+      }
+      if (full < nvp && rows > 0) {
+        int32_t id = ids[0];
+#pragma unroll
+        for (int pg = 1; pg < 8; ++pg)
+          if (pg == full) id = ids[pg];
+        const uint8_t* src = pool + (int64_t)id * tile;
+        bulk_g2s(dst + full * tile, src, rows * rb, bar);
+        if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
+      }
+    };
+    // K copies of block b (ids in idsb), once its stage is free
+    auto copy_k = [&](int b, const int32_t (&idsb)[8]) {
+      const int stage = b & 1;
+      const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
+      uint8_t* st = smem + kOffKStage + stage * kStageBytes;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull0 + stage], nvp * (kBaseTile + kResTile));
+      __syncwarp();
+      if (lane == 0) copy_pages(a.k_base + head_base * kBaseTile, st, true, idsb, nvp, kPage, &bars[kKFull0 + stage]);
+      if (lane == 1) copy_pages(a.k_res, st + kStRes, false, idsb, nvp, kPage, &bars[kKFull0 + stage]);
+    };
+    // V copies of block b (ids in idsb), once its V stage is free
+    auto copy_v = [&](int b, const int32_t (&idsb)[8]) {
+      const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
+      const int rows = b * kBlockPages + nvp == n_pages ? min(kPage, max(0, L - (n_pages - 1) * kPage)) : kPage;
+      uint8_t* st = smem + kOffVStage + (b & 1) * kStageBytes;
+      uint64_t* vbar = &bars[kVFull0 + (b & 1)];
+      if (rows < kPage) {  // rows [rows, 16) of the last V and v_res tiles
+        uint8_t* tv = st + (nvp - 1) * kBaseTile;
+        uint8_t* tr = st + kStRes + (nvp - 1) * kResTile;
+        for (int o = rows * 128 + 16 * lane; o < 2048; o += 16 * 32) {
+          *reinterpret_cast<uint4*>(tv + o) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(tv + 2048 + o) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        for (int o = rows * 32 + 16 * lane; o < kResTile; o += 16 * 32)
+          *reinterpret_cast<uint4*>(tr + o) = make_uint4(0u, 0u, 0u, 0u);
+        tc::fence_proxy_async();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(vbar, tile_bytes_pf(true, nvp, rows) + tile_bytes_pf(false, nvp, rows));
+      __syncwarp();
+      if (lane == 0) copy_pages(a.v_base + head_base * kBaseTile, st, true, idsb, nvp, rows, vbar);
+      if (lane == 1) copy_pages(a.v_res, st + kStRes, false, idsb, nvp, rows, vbar);
+    };
+    // Two streams without waiting on each other (K ahead of V as far as its stages allow).  Each
+    // stream requests the page ids of its next block as soon as a block is out.
+    int32_t ids[8];
+    int32_t kid = n_blocks > 0 ? lane_id(0) : 0, vid = kid;
+    int kb = 0, vb = 0;  // next K block, next V block
+    uint32_t idle = 0;
+    bool ok = true;
+    while (ok && vb < n_blocks) {
+      bool did = false;
+      if (kb < n_blocks &&
+          __shfl_sync(0xffffffffu, kb < 2 || mbar_test(&bars[kKEmpty0 + (kb & 1)], ((kb >> 1) - 1) & 1), 0)) {
+        broadcast_ids(kb, kid, ids);
+        copy_k(kb, ids);
+        ++kb;
+        if (kb < n_blocks) kid = lane_id(kb);
+        did = true;
+      }
+      if (vb < kb &&
+          __shfl_sync(0xffffffffu, vb < 2 || mbar_test(&bars[kVEmpty0 + (vb & 1)], ((vb >> 1) - 1) & 1), 0)) {
+        broadcast_ids(vb, vid, ids);
+        copy_v(vb, ids);
+        ++vb;
+        if (vb < n_blocks) vid = lane_id(vb);
+        did = true;
+      }
+      if (did) {
+        idle = 0;
+      } else {
+        if (++idle > kWaitLimit) {
+          flag_status(a.status, kDevTimeout);
+          ok = false;
+        }
+        __nanosleep(100);
       }
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    // Per block b: U(b) into buffer b % 2 (once P.V of block b - 2 is done with it), S(b)
-    // over U(b) once the rotation group has built K(b), then P.V of block b - 1.
+    // Issues, whichever is ready first (scores first: the softmax waits on them and the value
+    // products of the previous block need only be done before the next P is written; then the
+    // value products, then U):
+    //   U(b)  into buffer b % 2 once block b's K stage is in and the softmax has read S(b - 2);
+    //   S(b)  over U(b) once the rotation group has built K(b);
+    //   P.V(b) once the softmax has written P(b) and block b's V stage is in.
     if (lane == 0) {
       const uint32_t idU = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idS = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idPV = tc::idesc_bf16(128, 128, 0, 1);
       const uint32_t idPVr = tc::idesc_bf16(128, 16, 0, 1);
-      const uint32_t aQ = smem_u32(sQ), aKF = smem_u32(sKF), aBk = smem_u32(sBk);
+      const uint32_t aKF = smem_u32(sKF), aBk = smem_u32(sBk), aP = smem_u32(sP);
       bool ok = mbar_wait(&bars[kQReady], 0, a.status) && mbar_wait(&bars[kBkReady], 0, a.status);
-      // P.V of block c: A = P from its buffer (keys 0..63 at columns 0..31, keys 64..127 at 64..95)
-      auto issue_pv = [&](int c) {
-        const uint32_t buf = tm + kTmBuf + 128 * (c & 1);
-        const uint32_t st = smem_u32(smem + kOffStage + (c & 1) * kStageBytes);
-        const int nvp = min(kBlockPages, n_pages - c * kBlockPages);
-        for (int ks = 0; ks < nvp; ++ks)
-          tc::mma_ts(tm + kTmO, buf + (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4)),
-                     tc::smem_desc(st + kStV + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B), idPV, (c > 0 || ks > 0));
-        for (int ks = 0; ks < nvp; ++ks)
-          tc::mma_ts(tm + kTmOr, buf + (ks < 4 ? 8 * ks : 64 + 8 * (ks - 4)),
-                     tc::smem_desc(st + kStVR + ks * kResTile, 4096, 256, tc::kSwizzle32B), idPVr, (c > 0 || ks > 0));
-        tc::commit(&bars[kPVDone0 + (c & 1)]);
-        tc::commit(&bars[kEmpty0 + (c & 1)]);
-      };
-      for (int b = 0; b < n_blocks && ok; ++b) {
-        const int stage = b & 1;
-        const uint32_t st = smem_u32(smem + kOffStage + stage * kStageBytes);
-        const uint32_t buf = tm + kTmBuf + 128 * stage;
-        ok = mbar_wait(&bars[kFull0 + stage], (b >> 1) & 1, a.status) &&
-             (b < 2 || mbar_wait(&bars[kPVDone0 + stage], ((b >> 1) - 1) & 1, a.status));
-        if (!ok) break;
-        tc::fence_after();
-        tc::mma_ss(buf, tc::smem_desc(st + kStKR, 16, 256, tc::kSwizzle32B), tc::smem_desc(aBk, 16, 256, tc::kSwizzle32B),
-                   idU, 0);
-        tc::commit(&bars[kUFull0 + stage]);
-        ok = mbar_wait(&bars[kKFReady], b & 1, a.status);
-        if (!ok) break;
-        tc::fence_after();
+      int iu = 0, is = 0, ip = 0;  // next U, S and P.V to issue
+      uint32_t idle = 0;
+      while (ok && ip < n_blocks) {
+        bool did = false;
+        if (is < iu && mbar_test(&bars[kKFReady], is & 1)) {
+          tc::fence_after();
+          const uint32_t buf = tm + kTmBuf + 128 * (is & 1);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          tc::mma_ss(buf, tc::smem_desc(aQ + off, 16, 1024, tc::kSwizzle128B),
-                     tc::smem_desc(aKF + off, 16, 1024, tc::kSwizzle128B), idS, ks > 0);
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            tc::mma_ts(buf, tm + kTmQ + 8 * ks, tc::smem_desc(aKF + off, 16, 1024, tc::kSwizzle128B), idS, ks > 0);
+          }
+          tc::commit(&bars[kSFull0 + (is & 1)]);
+          tc::commit(&bars[kKFFree]);
+          ++is;
+          did = true;
         }
-        tc::commit(&bars[kSFull0 + stage]);
-        tc::commit(&bars[kKFFree]);
-        if (b > 0) {
-          ok = mbar_wait(&bars[kPFull0 + ((b - 1) & 1)], ((b - 1) >> 1) & 1, a.status);
-          if (!ok) break;
+        if (ip < is && mbar_test(&bars[kPFull], ip & 1) && mbar_test(&bars[kVFull0 + (ip & 1)], (ip >> 1) & 1)) {
           tc::fence_after();
-          issue_pv(b - 1);
+          const uint32_t aV = smem_u32(smem + kOffVStage + (ip & 1) * kStageBytes);
+          const int nvp = min(kBlockPages, n_pages - ip * kBlockPages);
+          for (int ks = 0; ks < nvp; ++ks)  // 16 keys per step: 32 bytes of P's rows, one V tile
+            tc::mma_ss(tm + kTmO, tc::smem_desc(aP + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
+                       tc::smem_desc(aV + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B), idPV, (ip > 0 || ks > 0));
+          for (int ks = 0; ks < nvp; ++ks)
+            tc::mma_ss(tm + kTmOr, tc::smem_desc(aP + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
+                       tc::smem_desc(aV + kStRes + ks * kResTile, 4096, 256, tc::kSwizzle32B), idPVr, (ip > 0 || ks > 0));
+          tc::commit(&bars[kPVDone]);
+          tc::commit(&bars[kVEmpty0 + (ip & 1)]);
+          ++ip;
+          did = true;
         }
-      }
-      if (ok && n_blocks > 0) {
-        ok = mbar_wait(&bars[kPFull0 + ((n_blocks - 1) & 1)], ((n_blocks - 1) >> 1) & 1, a.status);
-        if (ok) {
+        if (iu < n_blocks && iu - is < 2 && mbar_test(&bars[kKFull0 + (iu & 1)], (iu >> 1) & 1) &&
+            (iu < 2 || mbar_test(&bars[kSFree0 + (iu & 1)], ((iu >> 1) - 1) & 1))) {
           tc::fence_after();
-          issue_pv(n_blocks - 1);
+          const uint32_t st = smem_u32(smem + kOffKStage + (iu & 1) * kStageBytes);
+          tc::mma_ss(tm + kTmBuf + 128 * (iu & 1), tc::smem_desc(st + kStRes, 16, 256, tc::kSwizzle32B),
+                     tc::smem_desc(aBk, 16, 256, tc::kSwizzle32B), idU, 0);
+          tc::commit(&bars[kUFull0 + (iu & 1)]);
+          tc::commit(&bars[kKEmpty0 + (iu & 1)]);
+          ++iu;
+          did = true;
+        }
+        if (did) {
+          idle = 0;
+        } else {
+          if (++idle > kWaitLimit) {
+            flag_status(a.status, kDevTimeout);
+            ok = false;
+          }
+          // sleep on the event due first
+          if (ip < is)
+            mbar_try_wait_for(&bars[kPFull], ip & 1, 200);
+          else if (is < iu)
+            mbar_try_wait_for(&bars[kKFReady], is & 1, 200);
+          else
+            mbar_try_wait_for(&bars[kKFull0 + (iu & 1)], (iu >> 1) & 1, 200);
         }
       }
       // never leave with MMAs in flight
@@ -261,12 +371,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     __syncwarp();
   } else if (warp < kSoftWarp0) {
     // ------------------------------ RoPE group ------------------------------
+    // Two warps per TMEM lane quadrant; half hf owns the rotation pairs (d, d + 64) with
+    // d in [32 hf, 32 hf + 32) of its 32 keys.
+    const int hf = (warp - 2) >> 2;
     const int row = 32 * (warp & 3) + lane;  // key row of the block == TMEM lane
     const uint32_t tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
-    {  // B_k^T: row d, 16 ranks
+    {  // B_k^T: row d, this half's 8 of the 16 ranks
       const __nv_bfloat16* B = a.B_k + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim + row;
 #pragma unroll
-      for (int k = 0; k < kRank; ++k)
+      for (int k = 8 * hf; k < 8 * hf + 8; ++k)
         *reinterpret_cast<__nv_bfloat16*>(sBk + tc::sw32_off(row, k)) = B[(int64_t)k * a.hkv * kHeadDim];
       tc::fence_proxy_async();
       __syncwarp();
@@ -276,28 +389,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     bool ok = true;
     for (int b = 0; b < n_blocks && ok; ++b) {
       const int stage = b & 1;
-      uint8_t* st = smem + kOffStage + stage * kStageBytes;
+      uint8_t* st = smem + kOffKStage + stage * kStageBytes;
       const uint32_t ub = tl + kTmBuf + 128 * stage;
       const int j = b * kBlockKeys + row;
-      // this key's rotation row: logical 32-byte unit u sits at unit u ^ (j % 8)
-      uint4 rp[8][2];
-      {
-        const int jr = j < a.rope_positions ? j : 0;
-        const uint4* rrow = reinterpret_cast<const uint4*>(a.rope + (int64_t)jr * kRopeRow);
+      const int jr = j < a.rope_positions ? j : 0;
+      // this key's rotation row: frequency groups 4 u .. 4 u + 3 are 32-byte unit u, stored at
+      // unit u ^ (j % 8); this half needs units 4 hf .. 4 hf + 3
+      const uint4* rrow = reinterpret_cast<const uint4*>(a.rope + (int64_t)jr * kRopeRow);
+      uint4 rp[4][2];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          rp[u][0] = rrow[(u ^ (j & 7)) * 2];
-          rp[u][1] = rrow[(u ^ (j & 7)) * 2 + 1];
-        }
+      for (int u = 0; u < 4; ++u) {
+        rp[u][0] = rrow[((4 * hf + u) ^ (j & 7)) * 2];
+        rp[u][1] = rrow[((4 * hf + u) ^ (j & 7)) * 2 + 1];
       }
-      ok = mbar_wait(&bars[kFull0 + stage], (b >> 1) & 1, a.status) &&
+      ok = mbar_wait(&bars[kKFull0 + stage], (b >> 1) & 1, a.status) &&
            mbar_wait(&bars[kUFull0 + stage], (b >> 1) & 1, a.status);
       if (ok && b > 0) ok = mbar_wait(&bars[kKFFree], (b - 1) & 1, a.status);  // S(b - 1) is done with sKF
       if (!ok) break;
       tc::fence_after();
-      const uint8_t* kt = st + kStK + p * kBaseTile;
+      const uint8_t* kt = st + p * kBaseTile;
 #pragma unroll
-      for (int c = 0; c < 64; c += 16) {
+      for (int c = 32 * hf; c < 32 * hf + 32; c += 16) {  // d in [c, c + 16) and [c + 64, c + 80)
         uint32_t ulo[16], uhi[16];
         tc::ld16(ub + c, ulo);
         tc::ld16(ub + 64 + c, uhi);
@@ -311,19 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const uint32_t* khw = reinterpret_cast<const uint32_t*>(kh);
         uint32_t olo[8], ohi[8];
 #pragma unroll
-        for (int i2 = 0; i2 < 8; ++i2) {  // elements d = c + 2*i2, c + 2*i2 + 1 (and + 64)
-          const int m = (c >> 1) + i2;     // frequency group
+        for (int i2 = 0; i2 < 8; ++i2) {  // frequency group c/2 + i2: elements d = c + 2 i2, + 1 (and + 64)
+          const int m = ((c - 32 * hf) >> 1) + i2;  // frequency group, counted from 16 hf
           const uint4 w = rp[m >> 2][(m & 3) >> 1];
           const uint32_t cw = (m & 1) ? w.z : w.x, sw = (m & 1) ? w.w : w.y;
+          // K = Kb + RoPE_j(U) in fp32, one bf16 rounding
           const float lo0 = __uint_as_float(ulo[2 * i2]), lo1 = __uint_as_float(ulo[2 * i2 + 1]);
           const float hi0 = __uint_as_float(uhi[2 * i2]), hi1 = __uint_as_float(uhi[2 * i2 + 1]);
           const float c0 = bf_lo(cw), c1 = bf_hi(cw), s0 = bf_lo(sw), s1 = bf_hi(sw);
-          const float kl0 = bf_lo(klw[i2]) + (lo0 * c0 - hi0 * s0);
-          const float kl1 = bf_hi(klw[i2]) + (lo1 * c1 - hi1 * s1);
-          const float kh0 = bf_lo(khw[i2]) + (hi0 * c0 + lo0 * s0);
-          const float kh1 = bf_hi(khw[i2]) + (hi1 * c1 + lo1 * s1);
-          olo[i2] = pack_bf16(kl0, kl1);
-          ohi[i2] = pack_bf16(kh0, kh1);
+          olo[i2] = pack_bf16(fmaf(lo0, c0, fmaf(-hi0, s0, bf_lo(klw[i2]))), fmaf(lo1, c1, fmaf(-hi1, s1, bf_hi(klw[i2]))));
+          ohi[i2] = pack_bf16(fmaf(hi0, c0, fmaf(lo0, s0, bf_lo(khw[i2]))), fmaf(hi1, c1, fmaf(lo1, s1, bf_hi(khw[i2]))));
         }
         *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c)) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
         *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 8)) = make_uint4(olo[4], olo[5], olo[6], olo[7]);
@@ -331,21 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 72)) = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
       }
       tc::fence_before();
-      // keys past the sequence: zero their value rows so that 0 * (never-written data) stays 0
-      const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
-      if (j >= L && p < nvp) {
-        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int ch = 0; ch < 16; ++ch)
-          *reinterpret_cast<uint4*>(st + kStV + p * kBaseTile + base_off(t, ch * 8)) = z;
-        *reinterpret_cast<uint4*>(st + kStVR + p * kResTile + res_off(t, 0)) = z;
-        *reinterpret_cast<uint4*>(st + kStVR + p * kResTile + res_off(t, 8)) = z;
-      }
       tc::fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[kKFReady]);
-        mbar_arrive(&bars[kEmpty0 + stage]);
+        mbar_arrive(&bars[kKEmpty0 + stage]);
       }
     }
   } else {
@@ -363,13 +462,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int gq = valid ? (int)(f % G) : 0;
     const int32_t pos = valid ? a.positions[(int64_t)agent * a.q_len + tq] : -1;
     const int64_t orow = (((int64_t)agent * a.q_len + tq) * a.hkv * G + (int64_t)h * G + gq) * kHeadDim;
-    {  // this half of the Q row into the K-major swizzled tile; this half of the B_v slice
+    {  // this half of the Q row into tensor memory (d = 64 sh .. 64 sh + 63 as bf16 pairs in
+       // columns 32 sh ..); this half of the B_v slice
       const uint4* src = reinterpret_cast<const uint4*>(a.q + orow);
+      uint32_t qw[32];
 #pragma unroll
-      for (int ch = 8 * sh; ch < 8 * sh + 8; ++ch) {
-        const uint4 v = valid ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sQ + tc::sw128_off(128, qr, ch * 8)) = v;
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = valid ? src[8 * sh + i] : make_uint4(0u, 0u, 0u, 0u);
+        qw[4 * i] = v.x;
+        qw[4 * i + 1] = v.y;
+        qw[4 * i + 2] = v.z;
+        qw[4 * i + 3] = v.w;
       }
+      tc::st16(tl + kTmQ + 32 * sh, qw);
+      tc::st16(tl + kTmQ + 32 * sh + 16, qw + 16);
+      tc::wait_st();
+      tc::fence_before();
       const __nv_bfloat16* Bv = a.B_v + (int64_t)adapter * kRank * a.hkv * kHeadDim + (int64_t)h * kHeadDim;
       for (int i = qr + 128 * sh; i < kRank * kHeadDim / 8; i += 256) {
         const int k = i / 16, ch = i % 16;
@@ -389,20 +497,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       ok = ok && mbar_wait(&bars[kSFull0 + (b & 1)], (b >> 1) & 1, a.status);
       tc::fence_after();
       const int kbase = b * kBlockKeys + 64 * sh;
+      // keys of this half all visible to this row: no per-key mask (every block below the diagonal)
+      const bool open = kbase + 64 <= L && kbase + 63 <= pos;
       float bm = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
-        uint32_t v0[16], v1[16];
-        tc::ld16(tl + buf + 64 * sh + c, v0);
-        tc::ld16(tl + buf + 64 * sh + c + 16, v1);
+        uint32_t v[32];
+        tc::ld16(tl + buf + 64 * sh + c, v);
+        tc::ld16(tl + buf + 64 * sh + c + 16, v + 16);
         tc::wait_ld();
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (open) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int j = kbase + c + i;
-          const float s = __uint_as_float(i < 16 ? v0[i] : v1[i - 16]) * a.scale_log2;
-          if (j < L && j <= pos) bm = fmaxf(bm, s);
+          for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(v[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int j = kbase + c + i;
+            if (j < L && j <= pos) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(v[i]));
+          }
         }
+        bm = fmaxf(bm, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
       }
+      bm *= a.scale_log2;  // the scale is positive, so it commutes with the maximum
       // the row's block maximum: both halves (parity-alternating slots, so one barrier per block)
       s_pmax[((b & 1) * 2 + sh) * 128 + qr] = bm;
       named_sync(pair_bar, pair_threads);
@@ -413,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const float alpha = (need && m != -INFINITY) ? exp2f(m - mn) : 1.f;
         if (b > 0) {
           // O (this half's columns; the first half also O_r) is stable once P.V of block b - 1 is done
-          ok = ok && mbar_wait(&bars[kPVDone0 + ((b - 1) & 1)], ((b - 1) >> 1) & 1, a.status);
+          ok = ok && mbar_wait(&bars[kPVDone], (b - 1) & 1, a.status);
           tc::fence_after();
 #pragma unroll
           for (int c = 0; c < 64 + 16; c += 16) {
@@ -432,12 +549,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         m = mn;
       }
       const float mu = m == -INFINITY ? 0.f : m;
-      // P over this half's S columns: keys 64 sh + 2 i, 2 i + 1 at column 64 sh + i
+      // P of this half's keys (64 sh + 2 i, 2 i + 1 in pw[i]): p = 2^(s * scale - mu) in one
+      // multiply-add, the row sum in four partial sums
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pw[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
-        uint32_t v0[16], v1[16], pw[16];
-        tc::ld16(tl + buf + 64 * sh + c, v0);
-        tc::ld16(tl + buf + 64 * sh + c + 16, v1);
+        uint32_t v[32];
+        tc::ld16(tl + buf + 64 * sh + c, v);
+        tc::ld16(tl + buf + 64 * sh + c + 16, v + 16);
         tc::wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -446,21 +566,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           for (int e = 0; e < 2; ++e) {
             const int ii = 2 * i + e;
             const int j = kbase + c + ii;
-            const float s = __uint_as_float(ii < 16 ? v0[ii] : v1[ii - 16]) * a.scale_log2;
-            pr[e] = (j < L && j <= pos) ? exp2f(s - mu) : 0.f;
-            l += pr[e];
+            const float x = ex2(fmaf(__uint_as_float(v[ii]), a.scale_log2, -mu));
+            pr[e] = (open || (j < L && j <= pos)) ? x : 0.f;
+            ls[ii & 3] += pr[e];
           }
-          pw[i] = pack_bf16(pr[0], pr[1]);
+          pw[(c >> 1) + i] = pack_bf16(pr[0], pr[1]);
         }
-        tc::st16(tl + buf + 64 * sh + (c >> 1), pw);  // over columns of S this thread already read
       }
-      tc::wait_st();
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // S of this block is read: its buffer may take U of block b + 2
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kPFull0 + (b & 1)]);
+      if (lane == 0) mbar_arrive(&bars[kSFree0 + (b & 1)]);
+      // P to shared memory once the value products of block b - 1 are done with the previous P
+      if (b > 0) ok = ok && mbar_wait(&bars[kPVDone], (b - 1) & 1, a.status);
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)
+        *reinterpret_cast<uint4*>(sP + tc::sw128_off(128, qr, 64 * sh + 8 * c8)) =
+            make_uint4(pw[4 * c8], pw[4 * c8 + 1], pw[4 * c8 + 2], pw[4 * c8 + 3]);
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[kPFull]);
     }
     // epilogue: the row sum of both halves, then this half's output columns
-    if (ok && n_blocks > 0) ok = mbar_wait(&bars[kPVDone0 + ((n_blocks - 1) & 1)], ((n_blocks - 1) >> 1) & 1, a.status);
+    if (ok && n_blocks > 0) ok = mbar_wait(&bars[kPVDone], (n_blocks - 1) & 1, a.status);
     if (ok) ok = mbar_wait(&bars[kQReady], 0, a.status);  // every thread's part of the B_v slice is in place
     named_sync(pair_bar, pair_threads);  // both halves are past their last use of s_pmax
     s_pmax[sh * 128 + qr] = l;
