@@ -5,13 +5,16 @@
 // up-projected residual keys, associativity of the value path, both
 // accumulators rescaled together), laid out for a dense contraction:
 //   grid   (tile of 128 (token, query-head) rows, agent, KV head)
-//   warps  0      producer: 128-key blocks (8 pages) of K, V, k_res, v_res tiles
-//                 into a 2-stage ring with 1-D bulk async copies (one per run of
-//                 consecutive page ids)
+//   warps  0      producer: 128-key blocks (8 pages) of K and k_res tiles into a
+//                 2-stage ring, V and v_res tiles into a 3-stage ring, with 1-D bulk
+//                 async copies of at most one page tile each (several small copies
+//                 land sooner than one large one); each K tile goes in as its two
+//                 64-column halves, so that a stage holds the block's 128 keys as one
+//                 K-major operand
 //          1      allocates 512 TMEM columns; one lane issues every MMA
 //          2..9   RoPE group, two warps per key (half of the rotation pairs each):
-//                 U = Kr . B_k^T arrives in TMEM; K = bf16(Kb + RoPE_j(U)) is written
-//                 to shared memory as the 128-key operand of the next score MMA
+//                 U = Kr . B_k^T arrives in TMEM; K = bf16(Kb + RoPE_j(U)) replaces
+//                 Kb in place in the stage, which the score MMA then reads
 //          10..17 softmax group, two warps per query row (half of the keys each):
 //                 S from TMEM, causal mask, online softmax; P (bf16) to shared
 //                 memory as the A operand of the value products
@@ -21,8 +24,9 @@
 //                    O_r[128x16] += P . Vr[128x16]                (smem x smem)
 //   U and S of a block share one of two TMEM buffers (by block parity), freed
 //   as soon as the softmax has read S, so the next blocks' U, rotation and S
-//   run while this block's softmax does; the MMA warp issues whichever product
-//   is ready first.
+//   run while this block's softmax does; a K stage is released by the commit of
+//   its score MMA, so the rotation of block b + 1 overlaps the score product of
+//   block b.  The MMA warp issues whichever product is ready first.
 //   epilogue: out = (O + O_r . B_v[:, hD:(h+1)D]) / l, B_v applied once per row.
 // Every wait is on an mbarrier with a bounded spin; a timeout sets the device
 // status word instead of hanging.
@@ -43,11 +47,14 @@ constexpr int kThreads = (kSoftWarp0 + 8) * 32;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int kOffPmax = 1024;                  // [2 parities][2 halves][128 rows] partial row maxima
-constexpr int kOffKF = 3072;                    // full keys of one block, K-major 128B-swizzled [2][128 rows][128 B]
-constexpr int kOffKStage = kOffKF + 32768;      // 2 stages of [8 K tiles | 8 k_res tiles]
-constexpr int kOffVStage = kOffKStage + 2 * 36864;  // 2 stages of [8 V tiles | 8 v_res tiles]
+constexpr int kKStages = 2, kVStages = 3;  // ring depths (at most 3 each)
+// K stages: [the block's keys, K-major 128B-swizzled [2 halves][128 rows][128 B] | 8 k_res tiles];
+// key 16 p + t of the block is row t of its page p, so half hh of page p's tile lands at
+// hh * 16384 + p * 2048 and the swizzle (on row % 8 == t % 8) carries over unchanged
+constexpr int kOffKStage = 3072;
+constexpr int kOffVStage = kOffKStage + kKStages * 36864;  // V stages of [8 V tiles | 8 v_res tiles]
 constexpr int kStageBytes = 36864, kStRes = 32768;  // the residual tiles follow the base tiles
-constexpr int kOffP = kOffVStage + 2 * kStageBytes;  // P, K-major 128B-swizzled [2][128 rows][128 B]
+constexpr int kOffP = kOffVStage + kVStages * kStageBytes;  // P, K-major 128B-swizzled [2][128 rows][128 B]
 constexpr int kOffBk = kOffP + 32768;                // B_k^T, K-major 32B-swizzled [128 d][16 r]
 constexpr int kOffBv = kOffBk + 4096;                // B_v slice [16][128] bf16
 constexpr int kSmemBytes = kOffBv + 4096 + 1024;     // + slack for aligning the base
@@ -58,8 +65,9 @@ static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have"
 constexpr uint32_t kTmBuf = 0, kTmO = 256, kTmOr = 384, kTmQ = 400, kTmCols = 512;
 
 // mbarrier indices
-enum { kKFull0, kKFull1, kKEmpty0, kKEmpty1, kVFull0, kVFull1, kVEmpty0, kVEmpty1, kUFull0, kUFull1, kKFReady, kKFFree,
-       kSFull0, kSFull1,
+enum { kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kVFull0, kVFull1, kVFull2, kVEmpty0, kVEmpty1, kVEmpty2,
+       kUFull0, kUFull1,
+       kKFReady0, kKFReady1, kKFReady2, kSFull0, kSFull1,
        kSFree0, kSFree1, kPFull, kPVDone, kQReady, kBkReady, kMmaDone, kNumBars };
 static_assert(kNumBars * 8 <= 256, "barriers overlap the state that follows them");
 
@@ -73,6 +81,32 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Two fp32 values in one 64-bit register for the packed fp32 instructions (add/fma .f32x2);
+// each lane rounds exactly as the scalar instruction does.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 struct PrefillArgs {
@@ -117,18 +151,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if ((uint32_t)adapter >= (uint32_t)a.n_adapters) adapter = 0;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[kKFull0], 1);
-    mbar_init(&bars[kKFull1], 1);
-    mbar_init(&bars[kKEmpty0], kRopeWarps + 1);  // the RoPE warps (K tiles) + the U commit (k_res tiles)
-    mbar_init(&bars[kKEmpty1], kRopeWarps + 1);
-    mbar_init(&bars[kVFull0], 1);
-    mbar_init(&bars[kVFull1], 1);
-    mbar_init(&bars[kVEmpty0], 1);  // the commit after the value products
-    mbar_init(&bars[kVEmpty1], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&bars[kKFull0 + i], 1);
+      mbar_init(&bars[kKEmpty0 + i], 1);            // the commit after the score MMA
+      mbar_init(&bars[kKFReady0 + i], kRopeWarps);  // every RoPE warp, once its keys are rotated
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&bars[kVFull0 + i], 1);
+      mbar_init(&bars[kVEmpty0 + i], 1);  // the commit after the value products
+    }
     mbar_init(&bars[kUFull0], 1);
     mbar_init(&bars[kUFull1], 1);
-    mbar_init(&bars[kKFReady], kRopeWarps);
-    mbar_init(&bars[kKFFree], 1);
     mbar_init(&bars[kSFull0], 1);
     mbar_init(&bars[kSFull1], 1);
     mbar_init(&bars[kSFree0], 8);  // every softmax warp, once its last read of S is done
@@ -157,17 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int32_t key_limit = s_meta[0];
   const int n_pages = (key_limit + kPage - 1) / kPage;
   const int n_blocks = (n_pages + kBlockPages - 1) / kBlockPages;
-  uint8_t* sKF = smem + kOffKF;
   uint8_t* sP = smem + kOffP;
   uint8_t* sBk = smem + kOffBk;
   uint8_t* sBv = smem + kOffBv;
 
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
-    // Two streams in block order, K one block ahead of V: a block's K and k_res tiles once the
-    // rotation group and the U product are done with that K stage (two blocks back), its V and
-    // v_res tiles once the value products of the previous block are done with the V stage.  Rows of the last
-    // page at or past the sequence end are zeroed in shared memory instead of copied, so that
+    // Two streams in block order, K ahead of V: a block's K and k_res tiles once the score
+    // product of the block kKStages back is done with that K stage, its V and v_res tiles once
+    // the value products of the block kVStages back are done with that V stage.  Rows of the
+    // last page at or past the sequence end are zeroed in shared memory instead of copied, so that
     // a zero probability never meets never-written (possibly NaN) value rows.
     const int64_t head_base = (int64_t)h * a.num_base_pages;
     // page id of block b held by this lane (lanes 0..7 the base pages, 8..15 the residual
@@ -179,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       else if (lane >= 8 && lane - 8 < nvp) id = a.rpt[(int64_t)agent * a.pt_stride + pbase + lane - 8];
       return id;
     };
-    // the ids of a block to its copying lanes: lane 0 the base ids, lane 1 the residual ids
-    auto broadcast_ids = [&](int b, int32_t id, int32_t (&ids)[8]) {
+    // the ids of a block to its copying lanes: lane 0 the base ids, lanes 1 and 16 the residual ids
+    auto broadcast_ids = [&](int b, int32_t& id, int32_t (&ids)[8]) {
       const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
       if (lane < nvp && (uint32_t)id >= (uint32_t)a.num_base_pages) {
         flag_status(a.status, kDevBadPage);
@@ -189,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         flag_status(a.status, kDevBadPage);
         id = 0;
       }
-      const int src0 = lane == 1 ? 8 : 0;
+      const int src0 = (lane == 1 || lane == 16) ? 8 : 0;
 #pragma unroll
       for (int pg = 0; pg < 8; ++pg) ids[pg] = __shfl_sync(0xffffffffu, id, src0 + pg);
     };
@@ -222,22 +254,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         if (base) bulk_g2s(dst + full * tile + 2048, src + 2048, rows * rb, bar);
       }
     };
-    // K copies of block b (ids in idsb), once its stage is free
-    auto copy_k = [&](int b, const int32_t (&idsb)[8]) {
-      const int stage = b & 1;
+    // K copies of block b (ids in idsb; `id` this lane's checked id), once its stage is free:
+    // lane 2 p + hh copies half hh of page p's K tile, lane 16 the k_res tiles
+    auto copy_k = [&](int b, const int32_t (&idsb)[8], int32_t id) {
+      const int stage = b % kKStages;
       const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
       uint8_t* st = smem + kOffKStage + stage * kStageBytes;
+      const int32_t pid = __shfl_sync(0xffffffffu, id, (lane >> 1) & 7);
       if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull0 + stage], nvp * (kBaseTile + kResTile));
       __syncwarp();
-      if (lane == 0) copy_pages(a.k_base + head_base * kBaseTile, st, true, idsb, nvp, kPage, &bars[kKFull0 + stage]);
-      if (lane == 1) copy_pages(a.k_res, st + kStRes, false, idsb, nvp, kPage, &bars[kKFull0 + stage]);
+      if (lane < 2 * nvp) {
+        const int hh = lane & 1;
+        bulk_g2s(st + hh * 16384 + (lane >> 1) * 2048, a.k_base + (head_base + pid) * kBaseTile + hh * 2048,
+                 kBaseTile / 2, &bars[kKFull0 + stage]);
+      }
+      if (lane == 16) copy_pages(a.k_res, st + kStRes, false, idsb, nvp, kPage, &bars[kKFull0 + stage]);
     };
-    // V copies of block b (ids in idsb), once its V stage is free
-    auto copy_v = [&](int b, const int32_t (&idsb)[8]) {
+    // V copies of block b (`id` this lane's checked id), once its V stage is free
+    auto copy_v = [&](int b, int32_t id) {
       const int nvp = min(kBlockPages, n_pages - b * kBlockPages);
       const int rows = b * kBlockPages + nvp == n_pages ? min(kPage, max(0, L - (n_pages - 1) * kPage)) : kPage;
-      uint8_t* st = smem + kOffVStage + (b & 1) * kStageBytes;
-      uint64_t* vbar = &bars[kVFull0 + (b & 1)];
+      uint8_t* st = smem + kOffVStage + (b % kVStages) * kStageBytes;
+      uint64_t* vbar = &bars[kVFull0 + b % kVStages];
       if (rows < kPage) {  // rows [rows, 16) of the last V and v_res tiles
         uint8_t* tv = st + (nvp - 1) * kBaseTile;
         uint8_t* tr = st + kStRes + (nvp - 1) * kResTile;
@@ -252,32 +290,54 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(vbar, tile_bytes_pf(true, nvp, rows) + tile_bytes_pf(false, nvp, rows));
       __syncwarp();
-      if (lane == 0) copy_pages(a.v_base + head_base * kBaseTile, st, true, idsb, nvp, rows, vbar);
-      if (lane == 1) copy_pages(a.v_res, st + kStRes, false, idsb, nvp, rows, vbar);
+      // one copy per page tile: lane pg the V tile of page pg, lane 8 + pg its v_res tile (the
+      // first `rows` rows of each half for the last page when rows < 16)
+      const int pg = lane & 7;
+      const int32_t pid = __shfl_sync(0xffffffffu, id, lane & 15);
+      const bool last = pg == nvp - 1 && rows < kPage;
+      if (lane < 8 && pg < nvp) {
+        const uint8_t* src = a.v_base + (head_base + pid) * kBaseTile;
+        if (!last) {
+          bulk_g2s(st + pg * kBaseTile, src, kBaseTile, vbar);
+        } else if (rows > 0) {
+          bulk_g2s(st + pg * kBaseTile, src, rows * 128, vbar);
+          bulk_g2s(st + pg * kBaseTile + 2048, src + 2048, rows * 128, vbar);
+        }
+      } else if (lane >= 8 && lane < 16 && pg < nvp && (!last || rows > 0)) {
+        bulk_g2s(st + kStRes + pg * kResTile, a.v_res + (int64_t)pid * kResTile, last ? rows * 32 : kResTile, vbar);
+      }
     };
     // Two streams without waiting on each other (K ahead of V as far as its stages allow).  Each
-    // stream requests the page ids of its next block as soon as a block is out.
+    // stream holds this lane's page ids of its next three blocks (kq0..2, vq0..2): an id load
+    // takes microseconds while every SM streams, so it is requested three copies ahead.
     int32_t ids[8];
-    int32_t kid = n_blocks > 0 ? lane_id(0) : 0, vid = kid;
+    int32_t kq0 = lane_id(0), kq1 = lane_id(1), kq2 = lane_id(2);
+    int32_t vq0 = kq0, vq1 = kq1, vq2 = kq2;
     int kb = 0, vb = 0;  // next K block, next V block
     uint32_t idle = 0;
     bool ok = true;
     while (ok && vb < n_blocks) {
       bool did = false;
       if (kb < n_blocks &&
-          __shfl_sync(0xffffffffu, kb < 2 || mbar_test(&bars[kKEmpty0 + (kb & 1)], ((kb >> 1) - 1) & 1), 0)) {
-        broadcast_ids(kb, kid, ids);
-        copy_k(kb, ids);
+          __shfl_sync(0xffffffffu, kb < kKStages || mbar_test(&bars[kKEmpty0 + kb % kKStages], (kb / kKStages - 1) & 1),
+                      0)) {
+        broadcast_ids(kb, kq0, ids);
+        copy_k(kb, ids, kq0);
         ++kb;
-        if (kb < n_blocks) kid = lane_id(kb);
+        kq0 = kq1;
+        kq1 = kq2;
+        kq2 = lane_id(kb + 2);  // 0 past the last block
         did = true;
       }
       if (vb < kb &&
-          __shfl_sync(0xffffffffu, vb < 2 || mbar_test(&bars[kVEmpty0 + (vb & 1)], ((vb >> 1) - 1) & 1), 0)) {
-        broadcast_ids(vb, vid, ids);
-        copy_v(vb, ids);
+          __shfl_sync(0xffffffffu, vb < kVStages || mbar_test(&bars[kVEmpty0 + vb % kVStages], (vb / kVStages - 1) & 1),
+                      0)) {
+        broadcast_ids(vb, vq0, ids);
+        copy_v(vb, vq0);
         ++vb;
-        if (vb < n_blocks) vid = lane_id(vb);
+        vq0 = vq1;
+        vq1 = vq2;
+        vq2 = lane_id(vb + 2);
         did = true;
       }
       if (did) {
@@ -296,35 +356,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // products of the previous block need only be done before the next P is written; then the
     // value products, then U):
     //   U(b)  into buffer b % 2 once block b's K stage is in and the softmax has read S(b - 2);
-    //   S(b)  over U(b) once the rotation group has built K(b);
+    //   S(b)  over U(b) once the rotation group has built K(b) in its stage (whose commit then
+    //         frees the stage for block b + 3);
     //   P.V(b) once the softmax has written P(b) and block b's V stage is in.
     if (lane == 0) {
       const uint32_t idU = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idS = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idPV = tc::idesc_bf16(128, 128, 0, 1);
       const uint32_t idPVr = tc::idesc_bf16(128, 16, 0, 1);
-      const uint32_t aKF = smem_u32(sKF), aBk = smem_u32(sBk), aP = smem_u32(sP);
+      const uint32_t aK = smem_u32(smem + kOffKStage), aBk = smem_u32(sBk), aP = smem_u32(sP);
       bool ok = mbar_wait(&bars[kQReady], 0, a.status) && mbar_wait(&bars[kBkReady], 0, a.status);
       int iu = 0, is = 0, ip = 0;  // next U, S and P.V to issue
       uint32_t idle = 0;
       while (ok && ip < n_blocks) {
         bool did = false;
-        if (is < iu && mbar_test(&bars[kKFReady], is & 1)) {
+        if (is < iu && mbar_test(&bars[kKFReady0 + is % kKStages], (is / kKStages) & 1)) {
           tc::fence_after();
           const uint32_t buf = tm + kTmBuf + 128 * (is & 1);
+          const uint32_t aKs = aK + (is % kKStages) * kStageBytes;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            tc::mma_ts(buf, tm + kTmQ + 8 * ks, tc::smem_desc(aKF + off, 16, 1024, tc::kSwizzle128B), idS, ks > 0);
+            tc::mma_ts(buf, tm + kTmQ + 8 * ks, tc::smem_desc(aKs + off, 16, 1024, tc::kSwizzle128B), idS, ks > 0);
           }
           tc::commit(&bars[kSFull0 + (is & 1)]);
-          tc::commit(&bars[kKFFree]);
+          tc::commit(&bars[kKEmpty0 + is % kKStages]);
           ++is;
           did = true;
         }
-        if (ip < is && mbar_test(&bars[kPFull], ip & 1) && mbar_test(&bars[kVFull0 + (ip & 1)], (ip >> 1) & 1)) {
+        if (ip < is && mbar_test(&bars[kPFull], ip & 1) && mbar_test(&bars[kVFull0 + ip % kVStages], (ip / kVStages) & 1)) {
           tc::fence_after();
-          const uint32_t aV = smem_u32(smem + kOffVStage + (ip & 1) * kStageBytes);
+          const uint32_t aV = smem_u32(smem + kOffVStage + (ip % kVStages) * kStageBytes);
           const int nvp = min(kBlockPages, n_pages - ip * kBlockPages);
           for (int ks = 0; ks < nvp; ++ks)  // 16 keys per step: 32 bytes of P's rows, one V tile
             tc::mma_ss(tm + kTmO, tc::smem_desc(aP + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
@@ -333,18 +395,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tc::mma_ss(tm + kTmOr, tc::smem_desc(aP + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
                        tc::smem_desc(aV + kStRes + ks * kResTile, 4096, 256, tc::kSwizzle32B), idPVr, (ip > 0 || ks > 0));
           tc::commit(&bars[kPVDone]);
-          tc::commit(&bars[kVEmpty0 + (ip & 1)]);
+          tc::commit(&bars[kVEmpty0 + ip % kVStages]);
           ++ip;
           did = true;
         }
-        if (iu < n_blocks && iu - is < 2 && mbar_test(&bars[kKFull0 + (iu & 1)], (iu >> 1) & 1) &&
+        if (iu < n_blocks && iu - is < 2 && mbar_test(&bars[kKFull0 + iu % kKStages], (iu / kKStages) & 1) &&
             (iu < 2 || mbar_test(&bars[kSFree0 + (iu & 1)], ((iu >> 1) - 1) & 1))) {
           tc::fence_after();
-          const uint32_t st = smem_u32(smem + kOffKStage + (iu & 1) * kStageBytes);
+          const uint32_t st = aK + (iu % kKStages) * kStageBytes;
           tc::mma_ss(tm + kTmBuf + 128 * (iu & 1), tc::smem_desc(st + kStRes, 16, 256, tc::kSwizzle32B),
                      tc::smem_desc(aBk, 16, 256, tc::kSwizzle32B), idU, 0);
           tc::commit(&bars[kUFull0 + (iu & 1)]);
-          tc::commit(&bars[kKEmpty0 + (iu & 1)]);
           ++iu;
           did = true;
         }
@@ -359,9 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           if (ip < is)
             mbar_try_wait_for(&bars[kPFull], ip & 1, 200);
           else if (is < iu)
-            mbar_try_wait_for(&bars[kKFReady], is & 1, 200);
+            mbar_try_wait_for(&bars[kKFReady0 + is % kKStages], (is / kKStages) & 1, 200);
           else
-            mbar_try_wait_for(&bars[kKFull0 + (iu & 1)], (iu >> 1) & 1, 200);
+            mbar_try_wait_for(&bars[kKFull0 + iu % kKStages], (iu / kKStages) & 1, 200);
         }
       }
       // never leave with MMAs in flight
@@ -385,12 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBkReady]);
     }
-    const int p = row >> 4, t = row & 15;
     bool ok = true;
     for (int b = 0; b < n_blocks && ok; ++b) {
-      const int stage = b & 1;
+      const int stage = b % kKStages;
       uint8_t* st = smem + kOffKStage + stage * kStageBytes;
-      const uint32_t ub = tl + kTmBuf + 128 * stage;
+      const uint32_t ub = tl + kTmBuf + 128 * (b & 1);
       const int j = b * kBlockKeys + row;
       const int jr = j < a.rope_positions ? j : 0;
       // this key's rotation row: frequency groups 4 u .. 4 u + 3 are 32-byte unit u, stored at
@@ -402,22 +462,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         rp[u][0] = rrow[((4 * hf + u) ^ (j & 7)) * 2];
         rp[u][1] = rrow[((4 * hf + u) ^ (j & 7)) * 2 + 1];
       }
-      ok = mbar_wait(&bars[kKFull0 + stage], (b >> 1) & 1, a.status) &&
-           mbar_wait(&bars[kUFull0 + stage], (b >> 1) & 1, a.status);
-      if (ok && b > 0) ok = mbar_wait(&bars[kKFFree], (b - 1) & 1, a.status);  // S(b - 1) is done with sKF
+      ok = mbar_wait(&bars[kKFull0 + stage], (b / kKStages) & 1, a.status) &&
+           mbar_wait(&bars[kUFull0 + (b & 1)], (b >> 1) & 1, a.status);
       if (!ok) break;
       tc::fence_after();
-      const uint8_t* kt = st + p * kBaseTile;
 #pragma unroll
       for (int c = 32 * hf; c < 32 * hf + 32; c += 16) {  // d in [c, c + 16) and [c + 64, c + 80)
         uint32_t ulo[16], uhi[16];
         tc::ld16(ub + c, ulo);
         tc::ld16(ub + 64 + c, uhi);
         uint4 kl[2], kh[2];
-        kl[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c));
-        kl[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 8));
-        kh[0] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 64));
-        kh[1] = *reinterpret_cast<const uint4*>(kt + base_off(t, c + 72));
+        kl[0] = *reinterpret_cast<const uint4*>(st + tc::sw128_off(128, row, c));
+        kl[1] = *reinterpret_cast<const uint4*>(st + tc::sw128_off(128, row, c + 8));
+        kh[0] = *reinterpret_cast<const uint4*>(st + tc::sw128_off(128, row, c + 64));
+        kh[1] = *reinterpret_cast<const uint4*>(st + tc::sw128_off(128, row, c + 72));
         tc::wait_ld();
         const uint32_t* klw = reinterpret_cast<const uint32_t*>(kl);
         const uint32_t* khw = reinterpret_cast<const uint32_t*>(kh);
@@ -434,17 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           olo[i2] = pack_bf16(fmaf(lo0, c0, fmaf(-hi0, s0, bf_lo(klw[i2]))), fmaf(lo1, c1, fmaf(-hi1, s1, bf_hi(klw[i2]))));
           ohi[i2] = pack_bf16(fmaf(hi0, c0, fmaf(lo0, s0, bf_lo(khw[i2]))), fmaf(hi1, c1, fmaf(lo1, s1, bf_hi(khw[i2]))));
         }
-        *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c)) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-        *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 8)) = make_uint4(olo[4], olo[5], olo[6], olo[7]);
-        *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 64)) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-        *reinterpret_cast<uint4*>(sKF + tc::sw128_off(128, row, c + 72)) = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+        // in place: this thread alone reads and writes these elements of its key row
+        *reinterpret_cast<uint4*>(st + tc::sw128_off(128, row, c)) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+        *reinterpret_cast<uint4*>(st + tc::sw128_off(128, row, c + 8)) = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+        *reinterpret_cast<uint4*>(st + tc::sw128_off(128, row, c + 64)) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+        *reinterpret_cast<uint4*>(st + tc::sw128_off(128, row, c + 72)) = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
       }
       tc::fence_before();
       tc::fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars[kKFReady]);
-        mbar_arrive(&bars[kKEmpty0 + stage]);
+        mbar_arrive(&bars[kKFReady0 + stage]);
       }
     }
   } else {
@@ -509,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (open) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(v[i]));
+          for (int i = 0; i < 32; i += 2)
+            mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -550,8 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       const float mu = m == -INFINITY ? 0.f : m;
       // P of this half's keys (64 sh + 2 i, 2 i + 1 in pw[i]): p = 2^(s * scale - mu) in one
-      // multiply-add, the row sum in four partial sums
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // multiply-add, the row sum in four partial sums (two packed pairs)
+      const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nmu2 = f2(-mu, -mu);
+      uint64_t ls2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
       uint32_t pw[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
@@ -559,21 +619,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         tc::ld16(tl + buf + 64 * sh + c, v);
         tc::ld16(tl + buf + 64 * sh + c + 16, v + 16);
         tc::wait_ld();
+        if (open) {  // every key of this half is visible to the row
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pr[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int ii = 2 * i + e;
-            const int j = kbase + c + ii;
-            const float x = ex2(fmaf(__uint_as_float(v[ii]), a.scale_log2, -mu));
-            pr[e] = (open || (j < L && j <= pos)) ? x : 0.f;
-            ls[ii & 3] += pr[e];
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2_split(f2_fma(f2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sc2, nmu2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            ls2[i & 1] = f2_add(ls2[i & 1], f2(p0, p1));
+            pw[(c >> 1) + i] = pack_bf16(p0, p1);
           }
-          pw[(c >> 1) + i] = pack_bf16(pr[0], pr[1]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float pr[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int j = kbase + c + 2 * i + e;
+              const float x = ex2(fmaf(__uint_as_float(v[2 * i + e]), a.scale_log2, -mu));
+              pr[e] = (j < L && j <= pos) ? x : 0.f;
+            }
+            ls2[i & 1] = f2_add(ls2[i & 1], f2(pr[0], pr[1]));
+            pw[(c >> 1) + i] = pack_bf16(pr[0], pr[1]);
+          }
         }
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      {
+        float l0, l1, l2, l3;
+        f2_split(ls2[0], l0, l1);
+        f2_split(ls2[1], l2, l3);
+        l += (l0 + l1) + (l2 + l3);
+      }
       // S of this block is read: its buffer may take U of block b + 2
       tc::fence_before();
       __syncwarp();
