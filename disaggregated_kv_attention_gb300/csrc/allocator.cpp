@@ -6,8 +6,11 @@
 // README ("Design vs APC" and "Methods": fork aliases the parent's frames in
 // O(pages) with refcounts, so freeing the parent keeps the trunk alive;
 // unaligned tail, pack path: the L mod P valid rows are copied into a private
-// page of the child).  Free-list order, id assignment and the error policy are
-// fixed choices documented in include/forkkv.h.
+// page of the child; "Methods", LCP commit: the committed branch keeps the
+// observed prefix, a mid-page boundary is split copy-on-write and the siblings
+// are aborted, which releases their own pages and only decrements the trunk's).
+// Free-list order, id assignment and the error policy are fixed choices
+// documented in include/forkkv.h.
 #include <cstdint>
 #include <new>
 #include <unordered_map>
@@ -221,6 +224,109 @@ int32_t forkkv_free(forkkv_alloc* a, int32_t seq) {
   for (int32_t p : s->res)
     if (--a->res_ref[p] == 0) a->res_free.push_back(p);
   a->seqs.erase(seq);
+  return FORKKV_OK;
+}
+
+int32_t forkkv_abort(forkkv_alloc* a, int32_t seq, int32_t* n_base_released, int32_t* n_res_released) {
+  if (!a) return FORKKV_ERR_INVALID_ARG;
+  const Seq* s = a->find(seq);
+  if (!s) return FORKKV_ERR_INVALID_ARG;
+  int32_t nb = 0, nr = 0;
+  for (int32_t p : s->base) nb += a->base_ref[p] == 1;
+  for (int32_t p : s->res) nr += a->res_ref[p] == 1;
+  const int32_t rc = forkkv_free(a, seq);
+  if (rc != FORKKV_OK) return rc;
+  if (n_base_released) *n_base_released = nb;
+  if (n_res_released) *n_res_released = nr;
+  return FORKKV_OK;
+}
+
+int32_t forkkv_commit(forkkv_alloc* a, int32_t seq, int32_t lcp_len, const int32_t* siblings, int32_t n_siblings,
+                      forkkv_cow_job* jobs, int32_t jobs_cap, int32_t* n_jobs) {
+  if (!a || !n_jobs || n_siblings < 0 || (n_siblings > 0 && !siblings) || jobs_cap < 0 || (jobs_cap > 0 && !jobs))
+    return FORKKV_ERR_INVALID_ARG;
+  Seq* s = a->find(seq);
+  if (!s || lcp_len < 0 || lcp_len > s->length) return FORKKV_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n_siblings; ++i) {
+    if (siblings[i] == seq || !a->find(siblings[i])) return FORKKV_ERR_INVALID_ARG;
+    for (int32_t k = 0; k < i; ++k)
+      if (siblings[k] == siblings[i]) return FORKKV_ERR_INVALID_ARG;
+  }
+  const int32_t P = a->page;
+  const int32_t keep = ceil_div(lcp_len, P), t = lcp_len % P;
+  const int32_t np = static_cast<int32_t>(s->base.size());
+  // Everything is decided before anything changes: the decrements that the sibling frees and the
+  // truncation will make (a page appears at most once in one sequence), the pages they release,
+  // and whether the boundary page is still shared afterwards.
+  std::unordered_map<int32_t, int32_t> dec_b, dec_r;
+  try {
+    for (int32_t i = 0; i < n_siblings; ++i) {
+      const Seq* o = a->find(siblings[i]);
+      for (int32_t p : o->base) dec_b[p]++;
+      for (int32_t p : o->res) dec_r[p]++;
+    }
+    for (int32_t j = keep; j < np; ++j) {
+      dec_b[s->base[j]]++;
+      dec_r[s->res[j]]++;
+    }
+  } catch (...) {
+    return FORKKV_ERR_INVALID_ARG;
+  }
+  int32_t free_b = static_cast<int32_t>(a->base_free.size()), free_r = static_cast<int32_t>(a->res_free.size());
+  for (const auto& e : dec_b) {
+    if (a->base_ref[e.first] < e.second) return FORKKV_ERR_REFCOUNT;
+    free_b += a->base_ref[e.first] == e.second;
+  }
+  for (const auto& e : dec_r) {
+    if (a->res_ref[e.first] < e.second) return FORKKV_ERR_REFCOUNT;
+    free_r += a->res_ref[e.first] == e.second;
+  }
+  auto after = [](const std::vector<int32_t>& ref, const std::unordered_map<int32_t, int32_t>& dec, int32_t p) {
+    auto it = dec.find(p);
+    return ref[p] - (it == dec.end() ? 0 : it->second);
+  };
+  const bool split_b = t != 0 && after(a->base_ref, dec_b, s->base[keep - 1]) > 1;
+  const bool split_r = t != 0 && after(a->res_ref, dec_r, s->res[keep - 1]) > 1;
+  if ((split_b ? 1 : 0) + (split_r ? 1 : 0) > jobs_cap) return FORKKV_ERR_INVALID_ARG;
+  if ((split_b && free_b < 1) || (split_r && free_r < 1)) return FORKKV_ERR_OUT_OF_PAGES;
+  // 1. abort the siblings, in the order given
+  for (int32_t i = 0; i < n_siblings; ++i)
+    if (forkkv_free(a, siblings[i]) != FORKKV_OK) return FORKKV_ERR_REFCOUNT;  // excluded by the checks above
+  s = a->find(seq);
+  // 2. truncate: pages past the committed prefix, base then residual, in logical order
+  for (int32_t j = keep; j < np; ++j)
+    if (--a->base_ref[s->base[j]] == 0) a->base_free.push_back(s->base[j]);
+  for (int32_t j = keep; j < np; ++j)
+    if (--a->res_ref[s->res[j]] == 0) a->res_free.push_back(s->res[j]);
+  s->base.resize(keep);
+  s->res.resize(keep);
+  // 3. a boundary page still shared is split: a private copy of its first t rows
+  int32_t k = 0;
+  if (split_b) {
+    const int32_t old = s->base[keep - 1], dst = a->pop(true);
+    a->base_ref[old]--;
+    s->base[keep - 1] = dst;
+    jobs[k++] = forkkv_cow_job{old, dst, t, FORKKV_JOB_BASE};
+  }
+  if (split_r) {
+    const int32_t old = s->res[keep - 1], dst = a->pop(false);
+    a->res_ref[old]--;
+    s->res[keep - 1] = dst;
+    jobs[k++] = forkkv_cow_job{old, dst, t, FORKKV_JOB_RES};
+  }
+  s->length = lcp_len;
+  *n_jobs = k;
+  return FORKKV_OK;
+}
+
+int32_t forkkv_lcp_len(const int32_t* spec, int32_t n_spec, const int32_t* observed, int32_t n_observed,
+                       int32_t* out) {
+  if (!out || n_spec < 0 || n_observed < 0 || (n_spec > 0 && !spec) || (n_observed > 0 && !observed))
+    return FORKKV_ERR_INVALID_ARG;
+  int32_t n = 0;
+  const int32_t m = n_spec < n_observed ? n_spec : n_observed;
+  while (n < m && spec[n] == observed[n]) ++n;
+  *out = n;
   return FORKKV_OK;
 }
 

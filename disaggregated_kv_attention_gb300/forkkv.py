@@ -88,6 +88,9 @@ _SIGNATURES = {
     "forkkv_fork": ([_vp, _i32, _i32, _u32, _P(_i32), _P(forkkv_cow_job), _i32, _P(_i32)], _i32),
     "forkkv_append": ([_vp, _i32, _i32, _P(forkkv_cow_job), _i32, _P(_i32)], _i32),
     "forkkv_free": ([_vp, _i32], _i32),
+    "forkkv_abort": ([_vp, _i32, _P(_i32), _P(_i32)], _i32),
+    "forkkv_commit": ([_vp, _i32, _i32, _vp, _i32, _P(forkkv_cow_job), _i32, _P(_i32)], _i32),
+    "forkkv_lcp_len": ([_vp, _i32, _vp, _i32, _P(_i32)], _i32),
     "forkkv_seq_len": ([_vp, _i32, _P(_i32)], _i32),
     "forkkv_page_tables": ([_vp, _vp, _i32, _i32, _vp, _vp, _vp], _i32),
     "forkkv_refcount": ([_vp, _i32, _i32, _P(_i32)], _i32),
@@ -179,6 +182,32 @@ def forkkv_append(alloc: int, seq: int, n_tokens: int) -> list:
 
 def forkkv_free(alloc: int, seq: int) -> None:
     _check(lib().forkkv_free(alloc, seq), "free")
+
+
+def forkkv_abort(alloc: int, seq: int) -> Tuple[int, int]:
+    """Free a speculative branch; returns (base pages, residual pages) released."""
+    nb, nr = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().forkkv_abort(alloc, seq, ctypes.byref(nb), ctypes.byref(nr)), "abort")
+    return nb.value, nr.value
+
+
+def forkkv_commit(alloc: int, seq: int, lcp_len: int, siblings: Sequence[int] = ()) -> list:
+    """LCP commit: abort the siblings, truncate seq to lcp_len, split a shared boundary page."""
+    sib = np.ascontiguousarray(np.asarray(list(siblings), dtype=np.int32))
+    n = ctypes.c_int32()
+    buf = (forkkv_cow_job * 2)()
+    _check(lib().forkkv_commit(alloc, seq, lcp_len, sib.ctypes.data if len(sib) else None, len(sib), buf, 2,
+                               ctypes.byref(n)), "commit")
+    return _jobs_out(buf, n.value)
+
+
+def forkkv_lcp_len(spec: Sequence[int], observed: Sequence[int]) -> int:
+    a = np.ascontiguousarray(np.asarray(list(spec), dtype=np.int32))
+    b = np.ascontiguousarray(np.asarray(list(observed), dtype=np.int32))
+    n = ctypes.c_int32()
+    _check(lib().forkkv_lcp_len(a.ctypes.data if len(a) else None, len(a), b.ctypes.data if len(b) else None, len(b),
+                                ctypes.byref(n)), "lcp_len")
+    return n.value
 
 
 def forkkv_seq_len(alloc: int, seq: int) -> int:

@@ -152,6 +152,36 @@ int32_t forkkv_append(forkkv_alloc* alloc, int32_t seq, int32_t n_tokens, forkkv
  * A child's references keep an aliased trunk alive after its parent is freed. */
 int32_t forkkv_free(forkkv_alloc* alloc, int32_t seq);
 
+/* Abort a speculative branch (ForkServe README, "Design vs APC" and "Methods":
+ * abort costs the residual, not the trunk): exactly forkkv_free, and the
+ * number of base and residual pages that went back to the free stacks (the
+ * branch's own pages; aliased trunk pages only lose a reference).  Either
+ * count pointer may be NULL. */
+int32_t forkkv_abort(forkkv_alloc* alloc, int32_t seq, int32_t* n_base_released, int32_t* n_res_released);
+
+/* LCP commit (ForkServe README, "Methods"): bind the observed token prefix of
+ * a branch, abort its siblings, split a mid-page boundary.  In this order:
+ *  1. each of siblings[0 .. n_siblings) is freed (forkkv_free, in the order
+ *     given; distinct, live, and not seq);
+ *  2. seq is truncated to lcp_len (0 <= lcp_len <= its length): its pages
+ *     from index ceil(lcp_len / 16) on lose a reference, base pages then
+ *     residual pages in logical order, pushed when they reach 0;
+ *  3. if lcp_len % 16 != 0 and the boundary page (index ceil(lcp_len/16) - 1)
+ *     is still shared (refcount > 1), it is replaced by a new private page and
+ *     a job {old, new, lcp_len % 16, kind} copies its committed rows: base
+ *     first, then residual (at most 2 jobs, host memory, jobs_cap entries).
+ * Siblings are aborted before the split so that a page they alone shared with
+ * seq is not copied.  All checks (ids, refcounts, free pages after steps 1-2,
+ * jobs_cap) come first: on an error nothing changes. */
+int32_t forkkv_commit(forkkv_alloc* alloc, int32_t seq, int32_t lcp_len, const int32_t* siblings,
+                      int32_t n_siblings, forkkv_cow_job* jobs, int32_t jobs_cap, int32_t* n_jobs);
+
+/* Length of the longest common prefix of two token id sequences (host
+ * memory): the number of tokens of a speculative branch that the observed
+ * sequence confirms, the lcp_len of forkkv_commit. */
+int32_t forkkv_lcp_len(const int32_t* spec, int32_t n_spec, const int32_t* observed, int32_t n_observed,
+                       int32_t* out);
+
 int32_t forkkv_seq_len(const forkkv_alloc* alloc, int32_t seq, int32_t* len_out);
 
 /* Page tables of n sequences, row-major [n][stride] (host memory), unused

@@ -8,7 +8,11 @@ Restates, as plain list manipulation:
   freeing the parent does not drop the trunk (the child's reference pins it);
 * ForkServe README, adaptive unaligned tail and "Status": the pack path clones
   the r = L mod P valid rows of the parent's partial last page into a private
-  page of the child (a row copy of n_valid rows, not P).
+  page of the child (a row copy of n_valid rows, not P);
+* ForkServe README, "Methods" (LCP commit; CoW tree: abort costs the residual,
+  not the trunk): a committed branch keeps the observed token prefix, its
+  siblings are aborted, and a boundary page in the middle of a shared page is
+  split copy-on-write.
 
 Policies the pages leave open (fixed here so page ids are deterministic, and
 mirrored bit for bit by the C++ allocator):
@@ -19,6 +23,10 @@ mirrored bit for bit by the C++ allocator):
   inherited prefix (the child's adapter gives it different xA rows); with it,
   full residual pages are aliased and a partial one is copied like the base tail;
 * append copies a partial last page first if it is shared (refcount > 1);
+* commit aborts the siblings first (each like free, in the order given), then
+  drops the branch's pages past the committed prefix (base then residual, in
+  logical order), then splits the boundary page of each pool only if it is
+  still shared, base before residual;
 * sequence ids count up from 0 and are never reused;
 * on any error nothing changes.
 """
@@ -180,6 +188,75 @@ class AllocatorModel:
                 self.res_free.append(p)
         del self.seqs[sid]
 
+    def abort(self, sid: int) -> Tuple[int, int]:
+        """Free a speculative branch; return how many base and residual pages went back to the pool."""
+        s = self._seq(sid)
+        nb = sum(1 for p in s.base if self.base_ref[p] == 1)
+        nr = sum(1 for p in s.res if self.res_ref[p] == 1)
+        self.free(sid)
+        return nb, nr
+
+    def _snapshot(self):
+        return (list(self.base_free), list(self.res_free), list(self.base_ref), list(self.res_ref),
+                {k: _Seq(v.length, list(v.base), list(v.res)) for k, v in self.seqs.items()})
+
+    def _restore(self, snap) -> None:
+        self.base_free, self.res_free, self.base_ref, self.res_ref, self.seqs = snap
+
+    def commit(self, sid: int, lcp_len: int, siblings: Sequence[int] = (),
+               jobs_cap: Optional[int] = None) -> List[Tuple[int, int, int, int]]:
+        """LCP commit: abort the siblings, keep the first lcp_len tokens of sid, split a shared boundary page."""
+        s = self._seq(sid)
+        if lcp_len < 0 or lcp_len > s.length:
+            raise AllocatorError(ERR_INVALID_ARG, "lcp_len out of range")
+        sibs = list(siblings)
+        if sid in sibs or len(set(sibs)) != len(sibs):
+            raise AllocatorError(ERR_INVALID_ARG, "bad sibling list")
+        for o in sibs:
+            self._seq(o)
+        snap = self._snapshot()
+        try:
+            for o in sibs:
+                self.free(o)
+            s = self.seqs[sid]
+            P = self.P
+            keep = _ceil_div(lcp_len, P)
+            t = lcp_len % P
+            for p in s.base[keep:]:
+                self.base_ref[p] -= 1
+                if self.base_ref[p] == 0:
+                    self.base_free.append(p)
+            for p in s.res[keep:]:
+                self.res_ref[p] -= 1
+                if self.res_ref[p] == 0:
+                    self.res_free.append(p)
+            del s.base[keep:]
+            del s.res[keep:]
+            split_b = bool(t) and self.base_ref[s.base[-1]] > 1
+            split_r = bool(t) and self.res_ref[s.res[-1]] > 1
+            if jobs_cap is not None and int(split_b) + int(split_r) > jobs_cap:
+                raise AllocatorError(ERR_INVALID_ARG, "job buffer too small")
+            if (split_b and not self.base_free) or (split_r and not self.res_free):
+                raise AllocatorError(ERR_OUT_OF_PAGES)
+            jobs = []
+            if split_b:
+                old = s.base[-1]
+                dst = self._pop(JOB_BASE)
+                self.base_ref[old] -= 1
+                s.base[-1] = dst
+                jobs.append((old, dst, t, JOB_BASE))
+            if split_r:
+                old = s.res[-1]
+                dst = self._pop(JOB_RES)
+                self.res_ref[old] -= 1
+                s.res[-1] = dst
+                jobs.append((old, dst, t, JOB_RES))
+            s.length = lcp_len
+            return jobs
+        except AllocatorError:
+            self._restore(snap)
+            raise
+
     def page_tables(self, sids: Sequence[int], stride: int):
         """Rows of base / residual page ids (padded with -1) and lengths."""
         bpt, rpt, lens = [], [], []
@@ -210,6 +287,14 @@ class AllocatorModel:
             "base_refsum": sum(self.base_ref),
             "res_refsum": sum(self.res_ref),
         }
+
+
+def lcp_len(spec: Sequence[int], observed: Sequence[int]) -> int:
+    """Tokens of a speculative branch confirmed by the observed sequence (longest common prefix)."""
+    n = 0
+    while n < len(spec) and n < len(observed) and spec[n] == observed[n]:
+        n += 1
+    return n
 
 
 def cow_copy_rows_model(src_page_rows, dst_page_rows, n_valid: int):

@@ -94,6 +94,18 @@ class _Pair:
     def _m_free(self, s):
         return self.m.free(s)
 
+    def _c_commit(self, s, n, sibs):
+        return fk.forkkv_commit(self.c, s, n, sibs)
+
+    def _m_commit(self, s, n, sibs):
+        return self.m.commit(s, n, sibs, jobs_cap=2)
+
+    def _c_abort(self, s):
+        return fk.forkkv_abort(self.c, s)
+
+    def _m_abort(self, s):
+        return self.m.abort(s)
+
     def check_state(self):
         st = fk.forkkv_stats_get(self.c)
         ms = self.m.stats()
@@ -153,6 +165,64 @@ def test_cpp_allocator_matches_model_on_random_operations():
     st = fk.forkkv_stats_get(pr.c)
     assert st["base_free"] == 200 and st["res_free"] == 260 and st["n_seqs"] == 0
     pr.close()
+
+
+def test_cpp_commit_and_abort_match_model():
+    """Speculative fan-outs committed at random common prefixes (some inside shared pages,
+    some with bad arguments) and aborted branches: same ids, jobs, tables and free stacks."""
+    rnd = random.Random(23)
+    pr = _Pair(160, 400)
+    live = []
+    seen = {"split": 0, "rejected": 0}
+    for step in range(3000):
+        x = rnd.random()
+        if x < 0.12 or not live:
+            sid = pr.op("create", rnd.randint(0, 70))
+            if sid is not None:
+                live.append(sid)
+        elif x < 0.42:
+            par = rnd.choice(live)
+            res = pr.op("fork", par, rnd.randint(0, pr.m.seqs[par].length), rnd.random() < 0.3)
+            if res is not None:
+                live.append(res[0])
+        elif x < 0.62:
+            pr.op("append", rnd.choice(live), rnd.randint(0, 30))
+        elif x < 0.84:
+            s = rnd.choice(live)
+            others = [o for o in live if o != s]
+            sibs = rnd.sample(others, min(len(others), rnd.randint(0, 3)))
+            if rnd.random() < 0.05 and sibs:
+                sibs.append(sibs[0])                  # a repeated sibling: rejected
+            if rnd.random() < 0.05:
+                sibs.append(s)                        # the branch itself: rejected
+            n = rnd.randint(-1, pr.m.seqs[s].length + 1)
+            jobs = pr.op("commit", s, n, sibs)
+            if jobs is None:
+                seen["rejected"] += 1
+            else:
+                seen["split"] += bool(jobs)
+                live = [o for o in live if o not in sibs]
+        else:
+            pr.op("abort", live.pop(rnd.randrange(len(live))))
+        if step % 40 == 0:
+            pr.check_state()
+    pr.check_state()
+    assert seen["split"] > 20 and seen["rejected"] > 20, seen
+    for s in live:
+        pr.op("abort", s)
+    st = fk.forkkv_stats_get(pr.c)
+    assert st["base_free"] == 160 and st["res_free"] == 400 and st["n_seqs"] == 0
+    pr.close()
+
+
+def test_lcp_len_matches_model():
+    from oracle.allocator import lcp_len
+    rnd = random.Random(3)
+    for _ in range(300):
+        n = rnd.randint(0, 12)
+        a = [rnd.randint(0, 3) for _ in range(n)]
+        b = a[:rnd.randint(0, n)] + [rnd.randint(0, 3) for _ in range(rnd.randint(0, 5))]
+        assert fk.forkkv_lcp_len(a, b) == lcp_len(a, b)
 
 
 def test_invalid_arguments_rejected():

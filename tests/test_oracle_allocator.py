@@ -14,7 +14,7 @@ import pytest
 
 from oracle import accounting as acc
 from oracle.allocator import (AllocatorError, AllocatorModel, ERR_INVALID_ARG, ERR_OUT_OF_PAGES,
-                              JOB_BASE, JOB_RES)
+                              JOB_BASE, JOB_RES, lcp_len)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 P = 16
@@ -220,3 +220,103 @@ def test_errors_change_nothing():
     with pytest.raises(AllocatorError) as e:
         m.free(99)
     assert e.value.code == ERR_INVALID_ARG
+
+
+def test_commit_worked_example():
+    """LCP commit (ForkServe README, "Methods"), worked by hand with the LIFO policy: two
+    speculative branches of a 40-token root; branch b1 grows to 50 tokens; the observed tokens
+    confirm only its first 20, inside the trunk's shared page 1, so that page is split."""
+    m = AllocatorModel(16, 16, P)
+    root = m.seq_create(40)                    # base [0, 1, 2], res [0, 1, 2]
+    b1, _ = m.fork(root, 40)                   # base [0, 1, 3] (tail copy), res [3, 4, 5]
+    b2, _ = m.fork(root, 40)                   # base [0, 1, 4], res [6, 7, 8]
+    assert m.append(b1, 10) == []              # base [0, 1, 3, 5], res [3, 4, 5, 9]
+    jobs = m.commit(b1, 20, siblings=[b2])
+    # b2 frees base 4 and res 6, 7, 8; truncation frees base 3, 5 and res 5, 9; base page 1 is
+    # still shared with the root, so b1 gets the last freed base page (5) with 20 % 16 = 4 rows
+    assert jobs == [(1, 5, 4, JOB_BASE)]
+    assert m.seqs[b1].base == [0, 5] and m.seqs[b1].res == [3, 4] and m.seqs[b1].length == 20
+    assert b2 not in m.seqs
+    assert m.base_free[-2:] == [4, 3] and m.res_free[-5:] == [6, 7, 8, 5, 9]
+    assert m.base_ref[0] == 2 and m.base_ref[1] == 1 and m.base_ref[2] == 1
+    # abort of the root now releases its own pages only: base 1 and 2 (page 0 is still b1's)
+    # and its three residual pages
+    assert m.abort(root) == (2, 3)
+    assert m.base_ref[0] == 1
+
+
+def test_commit_aborts_siblings_before_splitting():
+    """A boundary page shared only with an aborted sibling is not copied."""
+    m = AllocatorModel(16, 16, P)
+    t = m.seq_create(32)                       # base [0, 1]
+    a, _ = m.fork(t, 32)                       # aliases [0, 1]
+    b, _ = m.fork(t, 32)
+    m.free(t)                                  # trunk pages now shared by a and b only
+    assert m.commit(a, 20, siblings=[b]) == []  # page 1 back to refcount 1: no split
+    assert m.seqs[a].base == [0, 1] and m.base_ref[1] == 1
+    c, _ = m.fork(a, 16)
+    # truncation to 8 tokens releases page 1 (pushed on the free stack), then page 0, shared
+    # with c, is split into the page on top of the stack: page 1 again
+    assert m.commit(a, 8) == [(0, 1, 8, JOB_BASE)]
+    assert m.seqs[a].base == [1] and m.seqs[c].base == [0] and m.base_ref[0] == 1
+
+
+def test_commit_page_aligned_and_full_length():
+    m = AllocatorModel(16, 16, P)
+    r = m.seq_create(48)
+    assert m.commit(r, 48) == [] and m.seqs[r].base == [0, 1, 2]
+    assert m.commit(r, 32) == [] and m.seqs[r].base == [0, 1] and m.base_free[-1] == 2
+    assert m.commit(r, 0) == [] and m.seqs[r].base == [] and m.seqs[r].length == 0
+    assert m.append(r, 17) == [] and len(m.seqs[r].base) == 2
+
+
+def test_abort_costs_the_residual_not_the_trunk():
+    """ForkServe README, "Design vs APC": abort releases the branch's own pages; the trunk,
+    aliased by the other branches, only loses a reference."""
+    m = AllocatorModel(64, 64, P)
+    root = m.seq_create(64)                    # 4 trunk pages
+    kids = []
+    for _ in range(4):
+        c, _ = m.fork(root, 64)
+        m.append(c, 20)                        # 2 own base pages, 4 + 2 own residual pages
+        kids.append(c)
+    live_before = m.stats()["base_live"]
+    assert m.abort(kids[0]) == (2, 6)
+    assert m.stats()["base_live"] == live_before - 2
+    assert all(m.base_ref[p] == 4 for p in m.seqs[root].base)
+
+
+def test_commit_errors_change_nothing():
+    m = AllocatorModel(3, 12, P)
+    a = m.seq_create(48)                       # base [0, 1, 2]: the base pool is empty
+    c, _ = m.fork(a, 48)                       # aligned: aliases all three
+    before = m._snapshot()
+
+    def same():
+        after = m._snapshot()
+        return (after[0], after[1], after[2], after[3]) == (before[0], before[1], before[2], before[3]) and \
+            {k: (v.length, v.base, v.res) for k, v in after[4].items()} == \
+            {k: (v.length, v.base, v.res) for k, v in before[4].items()}
+
+    for args, code in [((a, 49, []), ERR_INVALID_ARG), ((a, 20, [a]), ERR_INVALID_ARG),
+                       ((a, 20, [c, c]), ERR_INVALID_ARG), ((a, 20, [99]), ERR_INVALID_ARG),
+                       ((a, -1, []), ERR_INVALID_ARG)]:
+        with pytest.raises(AllocatorError) as e:
+            m.commit(*args)
+        assert e.value.code == code and same()
+    # truncating a to 20 tokens drops its reference to page 2 (c still holds it, nothing is
+    # freed), and page 1, shared with c, needs a copy: no free base page
+    with pytest.raises(AllocatorError) as e:
+        m.commit(a, 20)
+    assert e.value.code == ERR_OUT_OF_PAGES and same()
+    # with c aborted first nothing is shared any more: no copy, page 2 freed
+    assert m.commit(a, 20, siblings=[c]) == []
+    assert m.base_free == [2] and m.seqs[a].base == [0, 1]
+
+
+def test_lcp_len_pins():
+    assert lcp_len([], [1, 2]) == 0
+    assert lcp_len([5, 6, 7], [5, 6, 7]) == 3
+    assert lcp_len([5, 6, 7, 8], [5, 6, 9]) == 2
+    assert lcp_len([1], [2]) == 0
+    assert lcp_len([3, 3, 3], [3, 3, 3, 3, 3]) == 3
