@@ -11,8 +11,12 @@ One step = one decode step of all 32 layers: per layer, the new token's rows
 are scattered into the pools (forkkv_write_rows) and ResidualAttention decode
 runs (forkkv_residual_attn_decode: split-KV kernel + combine kernel).  The
 writes of a step and the decodes of a step are each captured in a CUDA graph;
-the timed region replays them K times.  tokens/s counts one (agent, layer)
-attention as one token, i.e. A * layers / step time.
+the timed region replays them K times, with CUDA events around each step's
+decodes (the roofline's launch time).  tokens/s counts one (agent, layer)
+attention as one token, i.e. A * layers / step time.  The same step through
+the library's one-graph call (forkkv_step_graph_launch, every layer's write
+and decode in one CUDA graph) is timed too ("step_graph"), and the e2e figure
+runs through it with host copies in and out.
 
 --impl reference times the fp64 CPU oracle instead (the only reference this
 method has), on bounded samples of the same workload.
@@ -366,7 +370,22 @@ def main() -> int:
     ms_step = total_ms / args.steps
     value = world * A * layers / (ms_step / 1000)
 
-    # end to end through the public API: pinned host inputs in, result out, every step
+    # the same step through the public one-graph API (forkkv_step_graph_*: every layer's row
+    # write and decode in one CUDA graph), device-timed over the same number of steps
+    rows = [(slot_b, slot_r, kb_new[l], vb_new[l], kr_new[l], vr_new[l]) for l in range(layers)]
+    sg = fk.forkkv_step_graph_create(params, rows)
+    for _ in range(args.warmup):
+        fk.forkkv_step_graph_launch(sg, stream)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        fk.forkkv_step_graph_launch(sg, stream)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    sg_ms = g0.elapsed_time(g1) / args.steps
+
+    # end to end through the public API: pinned host inputs in, the one-graph step, result out,
+    # every step
     q_h = q_all.cpu().pin_memory()
     kbh, vbh = kb_new.cpu().pin_memory(), vb_new.cpu().pin_memory()
     krh, vrh = kr_new.cpu().pin_memory(), vr_new.cpu().pin_memory()
@@ -382,8 +401,7 @@ def main() -> int:
     def e2e_step():
         for d, h in h2d:
             d.copy_(h, non_blocking=True)
-        g_w.replay()
-        g_d.replay()
+        fk.forkkv_step_graph_launch(sg, stream)
         out_h.copy_(out_all, non_blocking=True)
         stream.synchronize()
 
@@ -402,6 +420,7 @@ def main() -> int:
     e2e_value = world * A * layers / e2e_s
 
     torch.cuda.synchronize()
+    fk.forkkv_step_graph_destroy(sg)
     st = fk.forkkv_get_device_status()
     if st:
         raise RuntimeError(f"device status {st} after the timed region")
@@ -419,10 +438,13 @@ def main() -> int:
                      "alg_bytes_per_launch": fig["bytes"], "launch_us": call_us},
         "decode_call_us": call_us,
         "model_step_tokens_per_s": world * A / (ms_step / 1000),
+        "step_graph": {"ms_per_step": sg_ms, "tokens_per_s": world * A * layers / (sg_ms / 1000),
+                       "model_step_tokens_per_s": world * A / (sg_ms / 1000),
+                       "api": "forkkv_step_graph_launch: one CUDA graph per model step (all layers)"},
         "achieved_tflops": fig["flops"] / (call_us * 1e-6) / 1e12,
         "alg_flops_per_call": fig["flops"],
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d_bytes,
-                "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps, "api": "forkkv_step_graph_launch"},
         "gpu_launches": args.steps * layers * 3,
         "clocks": clk,
     }

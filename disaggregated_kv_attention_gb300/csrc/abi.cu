@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "../../include/forkkv.h"
 #include "internal.h"
@@ -224,6 +225,72 @@ int32_t forkkv_residual_attn_prefill_chunk(const forkkv_attn_params* p, void* st
     rope = p->workspace;
   }
   return cuda_status(fkv::launch_prefill(*p, rope, st, as_stream(stream)));
+}
+
+}  // extern "C"
+
+struct forkkv_step_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" {
+
+int32_t forkkv_step_graph_create(const forkkv_attn_params* params, const forkkv_step_rows* rows, int32_t n_layers,
+                                 forkkv_step_graph** out) {
+  if (!params || !out || n_layers < 1) return FORKKV_ERR_INVALID_ARG;
+  if (!fkv::device_status_ptr()) return FORKKV_ERR_CUDA;  // resolved outside the capture
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return FORKKV_ERR_CUDA;
+  int32_t rc = FORKKV_OK;
+  cudaGraph_t graph = nullptr;
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return FORKKV_ERR_CUDA;
+  }
+  for (int32_t l = 0; l < n_layers && rc == FORKKV_OK; ++l) {
+    const forkkv_attn_params& p = params[l];
+    if (rows && rows[l].n_rows > 0) {
+      const forkkv_step_rows& r = rows[l];
+      rc = forkkv_write_rows(&p.pools, p.layer, r.n_rows, r.slot_base, r.slot_res, r.k_base_rows, r.v_base_rows,
+                             r.k_res_rows, r.v_res_rows, s);
+    }
+    if (rc == FORKKV_OK) rc = forkkv_residual_attn_decode(&p, s);
+  }
+  const cudaError_t e = cudaStreamEndCapture(s, &graph);  // always: leaves the stream out of capture
+  cudaStreamDestroy(s);
+  if (rc == FORKKV_OK && e != cudaSuccess) rc = FORKKV_ERR_CUDA;
+  cudaGraphExec_t exec = nullptr;
+  if (rc == FORKKV_OK && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) rc = FORKKV_ERR_CUDA;
+  forkkv_step_graph* g = nullptr;
+  if (rc == FORKKV_OK) {
+    g = new (std::nothrow) forkkv_step_graph();
+    if (!g) rc = FORKKV_ERR_INVALID_ARG;
+  }
+  if (rc != FORKKV_OK) {
+    if (exec) cudaGraphExecDestroy(exec);
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();  // clear a capture error so later calls start clean
+    return rc;
+  }
+  g->graph = graph;
+  g->exec = exec;
+  *out = g;
+  return FORKKV_OK;
+}
+
+int32_t forkkv_step_graph_launch(forkkv_step_graph* graph, void* stream) {
+  if (!graph || !graph->exec) return FORKKV_ERR_INVALID_ARG;
+  return cuda_status(cudaGraphLaunch(graph->exec, as_stream(stream)));
+}
+
+int32_t forkkv_step_graph_destroy(forkkv_step_graph* graph) {
+  if (!graph) return FORKKV_OK;
+  cudaError_t e = cudaSuccess;
+  if (graph->exec) e = cudaGraphExecDestroy(graph->exec);
+  if (graph->graph && e == cudaSuccess) e = cudaGraphDestroy(graph->graph);
+  delete graph;
+  return cuda_status(e);
 }
 
 int32_t forkkv_get_device_status(uint32_t* status, void* stream) {

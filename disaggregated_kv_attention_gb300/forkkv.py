@@ -102,6 +102,9 @@ _SIGNATURES = {
     "forkkv_plan_build": ([_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _P(forkkv_plan_info)], _i32),
     "forkkv_decode_workspace_size": ([_P(forkkv_attn_params), _P(ctypes.c_size_t)], _i32),
     "forkkv_residual_attn_decode": ([_P(forkkv_attn_params), _vp], _i32),
+    "forkkv_step_graph_create": ([_P(forkkv_attn_params), _vp, _i32, _P(_vp)], _i32),
+    "forkkv_step_graph_launch": ([_vp, _vp], _i32),
+    "forkkv_step_graph_destroy": ([_vp], _i32),
     "forkkv_prefill_workspace_size": ([_P(forkkv_attn_params), _P(ctypes.c_size_t)], _i32),
     "forkkv_residual_attn_prefill_chunk": ([_P(forkkv_attn_params), _vp], _i32),
     "forkkv_get_device_status": ([_P(_u32), _vp], _i32),
@@ -357,6 +360,38 @@ def workspace_for(p: forkkv_attn_params, prefill: bool = False, device="cuda") -
 
 def forkkv_residual_attn_decode(p: forkkv_attn_params, stream=None) -> None:
     _check(lib().forkkv_residual_attn_decode(ctypes.byref(p), _stream(stream)), "residual_attn_decode")
+
+
+class forkkv_step_rows(ctypes.Structure):
+    _fields_ = [("n_rows", _i32), ("slot_base", _vp), ("slot_res", _vp), ("k_base_rows", _vp),
+                ("v_base_rows", _vp), ("k_res_rows", _vp), ("v_res_rows", _vp)]
+
+
+def forkkv_step_graph_create(params: Sequence[forkkv_attn_params], rows=None) -> int:
+    """One decode step of len(params) layers as one CUDA graph.  rows: None, or per layer a tuple
+    (slot_base, slot_res, k_base_rows, v_base_rows, k_res_rows, v_res_rows) of device tensors (or None)."""
+    n = len(params)
+    parr = (forkkv_attn_params * n)(*params)
+    rarr = None
+    if rows is not None:
+        rarr = (forkkv_step_rows * n)()
+        for l, (sb, sr, kb, vb, kr, vr) in enumerate(rows):
+            rarr[l].n_rows = int((sb if sb is not None else sr).numel())
+            rarr[l].slot_base, rarr[l].slot_res = _ptr(sb), _ptr(sr)
+            rarr[l].k_base_rows, rarr[l].v_base_rows = _ptr(kb), _ptr(vb)
+            rarr[l].k_res_rows, rarr[l].v_res_rows = _ptr(kr), _ptr(vr)
+    out = _vp()
+    _check(lib().forkkv_step_graph_create(parr, ctypes.cast(rarr, _vp) if rarr is not None else None, n,
+                                          ctypes.byref(out)), "step_graph_create")
+    return out.value
+
+
+def forkkv_step_graph_launch(graph: int, stream=None) -> None:
+    _check(lib().forkkv_step_graph_launch(graph, _stream(stream)), "step_graph_launch")
+
+
+def forkkv_step_graph_destroy(graph: int) -> None:
+    _check(lib().forkkv_step_graph_destroy(graph), "step_graph_destroy")
 
 
 def forkkv_residual_attn_prefill_chunk(p: forkkv_attn_params, stream=None) -> None:

@@ -342,6 +342,43 @@ int32_t forkkv_residual_attn_prefill_chunk(const forkkv_attn_params* p, void* st
 #define FORKKV_STATIC_SCRATCH_BYTES (8u << 20)
 int32_t forkkv_residual_attn_decode_static(const forkkv_attn_params* p, void* stream);
 
+/* ==== one model decode step as one CUDA graph ==============================
+ * ForkKV L2 section 5 reports decode throughput per model step (decode batch
+ * across all layers); one step of an n_layers model is, per layer l in order,
+ * the write of that step's new rows (forkkv_write_rows with rows[l], skipped
+ * when rows is NULL or rows[l].n_rows == 0) and forkkv_residual_attn_decode
+ * (params[l]).  forkkv_step_graph_create captures that sequence once, on a
+ * private stream, into a CUDA graph; forkkv_step_graph_launch replays it on
+ * `stream` with one launch call.
+ *   - Everything is validated as the per-layer calls validate it; any error
+ *     ends the capture and returns that status with *out unchanged.
+ *   - The graph records addresses, sizes and the decode geometry (n_agents,
+ *     max_seq_len, the plan and its CTA count): between launches the caller
+ *     may change the contents of every buffer (q, new rows, slots, page
+ *     tables, seq_lens, positions) but not where they are nor the geometry;
+ *     a step that needs a longer max_seq_len or a new plan (a sequence that
+ *     enters a new page) needs a new graph.
+ *   - The graph owns only its CUDA graph objects; every buffer stays the
+ *     caller's and must outlive it.  Release it with forkkv_step_graph_destroy.
+ *   - Make one ordinary call of forkkv_write_rows and forkkv_residual_attn_decode
+ *     on the device first (it resolves kernel attributes and the status word). */
+typedef struct {
+  int32_t n_rows;            /* new rows of this layer (one per agent in a decode step) */
+  const int32_t* slot_base;  /* [n_rows] device, or NULL (no base rows) */
+  const int32_t* slot_res;   /* [n_rows] device, or NULL (no residual rows) */
+  const void* k_base_rows;   /* [n_rows][Hkv][128] bf16 device */
+  const void* v_base_rows;
+  const void* k_res_rows;    /* [n_rows][16] bf16 device */
+  const void* v_res_rows;
+} forkkv_step_rows;
+
+typedef struct forkkv_step_graph forkkv_step_graph;
+
+int32_t forkkv_step_graph_create(const forkkv_attn_params* params, const forkkv_step_rows* rows, int32_t n_layers,
+                                 forkkv_step_graph** out);
+int32_t forkkv_step_graph_launch(forkkv_step_graph* graph, void* stream);
+int32_t forkkv_step_graph_destroy(forkkv_step_graph* graph);
+
 /* Read and clear the device status word of the current device (OR of
  * FORKKV_DEV_* bits set by kernels since the last read).  Synchronises
  * `stream`. */

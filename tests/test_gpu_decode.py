@@ -202,3 +202,69 @@ def test_group_larger_than_eight_is_unsupported():
     with pytest.raises(fk.ForkKVError) as e:
         fk.forkkv_decode_workspace_size(p)
     assert e.value.code == -5
+
+
+def test_step_graph_matches_per_layer_calls():
+    """One model decode step (new rows written, then attention, for every layer) captured as
+    one CUDA graph gives the same bytes as the per-layer calls, again after the inputs'
+    contents change between launches; layer 0 matches the oracle."""
+    w = wl.generate(wl.CONFIGS["tiny_decode"])
+    layers = 3
+    dev = torch.device("cuda", 0)
+    P = place(w, device=dev, n_layers=layers)
+    A = w.cfg.n_agents
+    lens = [int(x) for x in w.seq_lens]
+    g = torch.Generator().manual_seed(9)
+    q_all = torch.stack([P.q.cpu()] + [torch.randn(P.q.shape, generator=g).to(torch.bfloat16)
+                                       for _ in range(layers - 1)]).to(dev)
+    out_graph = torch.full_like(q_all, float("nan"))
+    out_ref = torch.full_like(q_all, float("nan"))
+    rows_l = []
+    kb = torch.stack([w.agent_base(a)[0][lens[a] - 1] for a in range(A)]).to(dev)
+    vb = torch.stack([w.agent_base(a)[1][lens[a] - 1] for a in range(A)]).to(dev)
+    kr = torch.stack([w.k_res[a][lens[a] - 1] for a in range(A)]).to(dev)
+    vr = torch.stack([w.v_res[a][lens[a] - 1] for a in range(A)]).to(dev)
+    sb = torch.tensor([int(P.bpt_np[a, (lens[a] - 1) // 16]) * 16 + (lens[a] - 1) % 16 for a in range(A)],
+                      dtype=torch.int32, device=dev)
+    sr = torch.tensor([int(P.rpt_np[a, (lens[a] - 1) // 16]) * 16 + (lens[a] - 1) % 16 for a in range(A)],
+                      dtype=torch.int32, device=dev)
+    for _ in range(layers):
+        rows_l.append((sb, sr, kb, vb, kr, vr))
+    rope = fk.rope_table(w.cfg.rope_theta, P.max_seq_len, device=dev)
+    plan, info = fk.forkkv_plan_build(P.bpt_np, w.seq_lens.numpy(), w.cfg.n_kv_heads)
+    plan_d = torch.from_numpy(plan).to(dev)
+
+    def mk(out):
+        ps = [fk.attn_params(P.pools, l, q_all[l], out[l], P.bpt, P.rpt, P.seq_lens, P.positions, P.max_seq_len,
+                             P.B_k, P.B_v, rope=rope, plan=plan_d, plan_info=info) for l in range(layers)]
+        return ps
+
+    p_ref, p_graph = mk(out_ref), mk(out_graph)
+    ws = fk.workspace_for(p_ref[0], device=dev)
+    for p in p_ref + p_graph:
+        fk.set_workspace(p, ws)
+
+    def eager():
+        for l in range(layers):
+            fk.forkkv_write_rows(P.pools, l, sb, sr, kb, vb, kr, vr)
+            fk.forkkv_residual_attn_decode(p_ref[l])
+
+    eager()
+    torch.cuda.synchronize()
+    graph = fk.forkkv_step_graph_create(p_graph, rows_l)
+    try:
+        for step in range(2):
+            fk.forkkv_step_graph_launch(graph)
+            torch.cuda.synchronize()
+            assert fk.forkkv_get_device_status() == 0
+            assert torch.equal(out_graph.view(torch.int16), out_ref.view(torch.int16)), step
+            q_all.mul_(-0.5)  # new contents, same addresses
+            eager()
+            torch.cuda.synchronize()
+    finally:
+        fk.forkkv_step_graph_destroy(graph)
+    q_all.mul_(1.0 / 0.25)  # back to the layer-0 query of the workload (two halvings, exact in bf16)
+    eager()
+    torch.cuda.synchronize()
+    m, ok = compare(out_ref[0], oracle(w, range(A)))
+    assert ok, m
