@@ -214,6 +214,67 @@ def bench_prefill(args, cfg) -> int:
     return 0
 
 
+def bench_fill(args, cfg) -> int:
+    """Residual fill of a fan-out: every agent's xA rows of every shared-prefix token, one call
+    (forkkv_residual_fill), for the decode configuration's agents and prefix (hidden size of the
+    model named by the configuration).  Four copies of x are cycled so the inputs exceed L2."""
+    import torch
+    from disaggregated_kv_attention_gb300 import build as _build
+    from disaggregated_kv_attention_gb300 import forkkv as fk
+    _build.build()
+    n_ag = cfg.n_agents
+    n_tok = cfg.nodes[0].tokens[0]  # the root's (shared prefix's) tokens
+    hidden = cfg.hidden
+    dev = torch.device("cuda", 0)
+    g = torch.Generator().manual_seed(1000 + cfg.index)
+    reps = 4
+    xs = [torch.randn(n_tok, hidden, generator=g).to(torch.bfloat16).to(dev) for _ in range(reps)]
+    A = (0.02 * torch.randn(n_ag, 2, 16, hidden, generator=g)).to(torch.bfloat16).to(dev)
+    n_res = n_ag * ((n_tok + 15) // 16)
+    pools = fk.Pools(8, n_res, cfg.n_kv_heads, n_layers=1, device=dev, fill=0)
+    t = torch.arange(n_tok)
+    slots = torch.stack([((t // 16) * n_ag + a) * 16 + t % 16 for a in range(n_ag)]).to(torch.int32).to(dev)
+    fk.forkkv_residual_fill(pools, 0, xs[0], A, slots)
+    torch.cuda.synchronize()
+    if fk.forkkv_get_device_status():
+        raise RuntimeError("device status set by the residual fill")
+    for k in range(args.warmup):
+        fk.forkkv_residual_fill(pools, 0, xs[k % reps], A, slots)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    time.sleep(0.3)
+    for k in range(args.steps):
+        ev[2 * k].record(stream)
+        fk.forkkv_residual_fill(pools, 0, xs[k % reps], A, slots)
+        ev[2 * k + 1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    us = [1000 * ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(args.steps)]
+    t_us = statistics.mean(us)
+    alg_bytes = n_tok * hidden * 2 + A.numel() * 2 + n_ag * n_tok * 2 * 16 * 2 + slots.numel() * 4
+    flops = 2 * n_tok * hidden * 32 * n_ag
+    hbm, tf, tf_sus, src = _peaks()
+    gbs = alg_bytes / (t_us * 1e-6) / 1e9
+    tfs = flops / (t_us * 1e-6) / 1e12
+    hbm_bound = alg_bytes / (hbm * 1e9) >= flops / (tf * 1e12)
+    print(json.dumps({
+        "metric": "Residual fill GB/s (% of HBM peak), 1 GPU", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_us / 1000, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} fan-out fill: {n_ag} agents x {n_tok} prefix tokens, hidden {hidden}, "
+                               f"rank 16 (k and v), x cycled over {reps} copies (inputs > L2)"},
+        "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": gbs if hbm_bound else tfs,
+                     "peak": hbm if hbm_bound else tf, "unit": "GB/s" if hbm_bound else "TFLOP/s",
+                     "frac": (gbs / hbm) if hbm_bound else (tfs / tf), "traffic": _traffic("residual_fill_kernel"),
+                     "peak_source": f"{src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops burst'})",
+                     "alg_bytes_per_launch": alg_bytes, "alg_flops_per_launch": flops},
+        "achieved_tflops": tfs, "tensor_frac": tfs / tf, "hbm_frac": gbs / hbm,
+        "gpu_launches": args.steps, "clocks": clk}))
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -223,6 +284,7 @@ def main() -> int:
     ap.add_argument("--config", default="llama3_8b_decode")
     ap.add_argument("--layers", type=int, default=0, help="pool sets (0 = the model's layer count)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fill", action="store_true", help="time the residual fill of the configuration's fan-out")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -232,6 +294,8 @@ def main() -> int:
 
     from disaggregated_kv_attention_gb300 import workload as wl
     cfg = wl.CONFIGS[args.config]
+    if args.fill:
+        return bench_fill(args, cfg)
     if cfg.q_len != 1:
         return bench_prefill(args, cfg)
     layers = args.layers or cfg.model_layers

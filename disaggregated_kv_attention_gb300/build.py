@@ -28,6 +28,7 @@ SOURCES = [
     "kernels/rows.cu",
     "kernels/decode.cu",
     "kernels/prefill.cu",
+    "kernels/fill.cu",
     "decode_static.cu",
 ]
 

@@ -130,6 +130,39 @@ int32_t forkkv_write_rows(const forkkv_pool_desc* pools, int32_t layer, int32_t 
                                             k_res_rows, v_res_rows, st, as_stream(stream)));
 }
 
+int32_t forkkv_residual_fill(const forkkv_pool_desc* pools, int32_t layer, const void* x, int32_t n_tok,
+                             int32_t hidden, const void* A, int32_t n_agents, const int32_t* slot_res, void* stream) {
+  int32_t rc = check_pools(pools);
+  if (rc) return rc;
+  if (layer < 0 || layer >= pools->n_layers || n_tok < 0 || n_agents < 0 || n_agents > (1 << 20))
+    return FORKKV_ERR_INVALID_ARG;
+  if (n_tok == 0 || n_agents == 0) return FORKKV_OK;
+  if (!x || !A || !slot_res || !aligned(x, 16) || !aligned(A, 16) || hidden < 8 || hidden % 8 != 0)
+    return FORKKV_ERR_INVALID_ARG;
+  uint32_t* st = fkv::device_status_ptr();
+  if (!st) return FORKKV_ERR_CUDA;
+  return cuda_status(
+      fkv::launch_residual_fill(*pools, layer, x, n_tok, hidden, A, n_agents, slot_res, st, as_stream(stream)));
+}
+
+int32_t forkkv_append_rows(const forkkv_pool_desc* pools, int32_t layer, int32_t n_rows, const int32_t* slot_base,
+                           const int32_t* slot_res, const void* k_base_rows, const void* v_base_rows, const void* x,
+                           int32_t hidden, const void* A, int32_t n_adapters, const int32_t* adapter_ids,
+                           void* stream) {
+  int32_t rc = check_pools(pools);
+  if (rc) return rc;
+  if (layer < 0 || layer >= pools->n_layers || n_rows < 0) return FORKKV_ERR_INVALID_ARG;
+  if (slot_base && (!k_base_rows || !v_base_rows || !aligned(k_base_rows, 16) || !aligned(v_base_rows, 16)))
+    return FORKKV_ERR_INVALID_ARG;
+  if (slot_res && (!x || !A || !aligned(x, 16) || !aligned(A, 16) || hidden < 8 || hidden % 8 != 0 ||
+                   n_adapters < 1))
+    return FORKKV_ERR_INVALID_ARG;
+  uint32_t* st = fkv::device_status_ptr();
+  if (!st) return FORKKV_ERR_CUDA;
+  return cuda_status(fkv::launch_append_rows(*pools, layer, n_rows, slot_base, slot_res, k_base_rows, v_base_rows, x,
+                                             hidden, A, n_adapters, adapter_ids, st, as_stream(stream)));
+}
+
 int32_t forkkv_cow_copy_rows(const forkkv_pool_desc* pools, const forkkv_cow_job* jobs, int32_t n_jobs,
                              void* stream) {
   int32_t rc = check_pools(pools);

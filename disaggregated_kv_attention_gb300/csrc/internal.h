@@ -22,6 +22,14 @@ cudaError_t launch_write_rows(const forkkv_pool_desc& pools, int32_t layer, int3
                               const void* vr, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_cow_copy(const forkkv_pool_desc& pools, const CowJobBatch& batch, cudaStream_t stream);
 cudaError_t launch_rope_table(const uint32_t* turns_hi_lo, int32_t n_positions, void* table, cudaStream_t stream);
+cudaError_t launch_residual_fill(const forkkv_pool_desc& pools, int32_t layer, const void* x, int32_t n_tok,
+                                 int32_t hidden, const void* A, int32_t n_ag, const int32_t* slot_res,
+                                 uint32_t* status, cudaStream_t stream);
+cudaError_t launch_append_rows(const forkkv_pool_desc& pools, int32_t layer, int32_t n_rows, const int32_t* slot_base,
+                               const int32_t* slot_res, const void* kb, const void* vb, const void* x, int32_t hidden,
+                               const void* A, int32_t n_adapters, const int32_t* adapter_ids, uint32_t* status,
+                               cudaStream_t stream);
+int32_t fill_columns_per_cta(int32_t n_tok, int32_t n_ag, int32_t sm_count);
 
 // Decode: partial-result workspace geometry.
 struct DecodeGeometry {

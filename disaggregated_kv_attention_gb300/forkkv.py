@@ -96,6 +96,9 @@ _SIGNATURES = {
     "forkkv_refcount": ([_vp, _i32, _i32, _P(_i32)], _i32),
     "forkkv_stats_get": ([_vp, _P(forkkv_stats)], _i32),
     "forkkv_write_rows": ([_P(forkkv_pool_desc), _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "forkkv_residual_fill": ([_P(forkkv_pool_desc), _i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp], _i32),
+    "forkkv_append_rows": ([_P(forkkv_pool_desc), _i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp],
+                           _i32),
     "forkkv_cow_copy_rows": ([_P(forkkv_pool_desc), _P(forkkv_cow_job), _i32, _vp], _i32),
     "forkkv_rope_table_bytes": ([_i32, _P(ctypes.c_size_t)], _i32),
     "forkkv_rope_table_build": ([ctypes.c_double, _i32, _vp, _vp], _i32),
@@ -270,6 +273,27 @@ def forkkv_write_rows(pools: Pools, layer: int, slot_base: Optional[torch.Tensor
     _check(lib().forkkv_write_rows(ctypes.byref(pools.desc), layer, n, _ptr(slot_base), _ptr(slot_res),
                                    _ptr(k_base_rows), _ptr(v_base_rows), _ptr(k_res_rows), _ptr(v_res_rows),
                                    _stream(stream)), "write_rows")
+
+
+def forkkv_residual_fill(pools: Pools, layer: int, x: torch.Tensor, A: torch.Tensor, slot_res: torch.Tensor,
+                         stream=None) -> None:
+    """x [n_tok, hidden], A [n_agents, 2, 16, hidden] bf16, slot_res [n_agents, n_tok] int32 (device)."""
+    n_tok, hidden = x.shape
+    n_ag = A.shape[0]
+    _check(lib().forkkv_residual_fill(ctypes.byref(pools.desc), layer, _ptr(x), n_tok, hidden, _ptr(A), n_ag,
+                                      _ptr(slot_res), _stream(stream)), "residual_fill")
+
+
+def forkkv_append_rows(pools: Pools, layer: int, slot_base: Optional[torch.Tensor], slot_res: Optional[torch.Tensor],
+                       k_base_rows=None, v_base_rows=None, x=None, A=None, adapter_ids=None, stream=None) -> None:
+    """New tokens' base rows and residual rows from their hidden states x [n, hidden] with adapters
+    A [n_adapters, 2, 16, hidden] (adapter_ids [n] or None: row index)."""
+    n = int((slot_base if slot_base is not None else slot_res).numel())
+    hidden = 0 if x is None else x.shape[1]
+    n_ad = 0 if A is None else A.shape[0]
+    _check(lib().forkkv_append_rows(ctypes.byref(pools.desc), layer, n, _ptr(slot_base), _ptr(slot_res),
+                                    _ptr(k_base_rows), _ptr(v_base_rows), _ptr(x), hidden, _ptr(A), n_ad,
+                                    _ptr(adapter_ids), _stream(stream)), "append_rows")
 
 
 def forkkv_cow_copy_rows(pools: Pools, jobs: Sequence[Tuple[int, int, int, int]], stream=None) -> None:

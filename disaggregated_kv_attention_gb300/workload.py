@@ -54,6 +54,7 @@ class WorkloadConfig:
     rank: int = RANK
     page_size: int = PAGE_SIZE
     description: str = ""
+    hidden: int = 4096          # model hidden size (inputs of the k/v projections; the residual fill's K)
 
     @property
     def group(self) -> int:
@@ -98,17 +99,21 @@ CONFIGS: Dict[str, WorkloadConfig] = {
             description="32q/8kv, 4 agents on a 512-token prefix + 64 private tokens each, 1 query/agent"),
         WorkloadConfig(
             "llama3_8b_decode", 1, 32, 8, 500000.0, 32, 1, _fan(8192, 8, (256, 1024)),
-            description="32q/8kv, 8 agents on an 8192-token prefix (refcount 8) + U[256,1024] private tokens, 1 query/agent"),
+            description="32q/8kv, 8 agents on an 8192-token prefix (refcount 8) + U[256,1024] private tokens, 1 query/agent",
+            hidden=4096),
         WorkloadConfig(
             "qwen25_7b_mapreduce_decode", 2, 28, 4, 1000000.0, 28, 1, _fan(32768, 32, (64, 4096)),
-            description="28q/4kv, 32 agents on a 32768-token prefix + U[64,4096] private tokens, 1 query/agent"),
+            description="28q/4kv, 32 agents on a 32768-token prefix + U[64,4096] private tokens, 1 query/agent",
+            hidden=3584),
         WorkloadConfig(
             "qwen25_14b_prefill", 3, 40, 8, 1000000.0, 48, 2048, _fan(16384, 8, (2048, 2048)),
-            description="40q/8kv, 8 agents each prefilling a causal 2048-token chunk on a 16384-token prefix"),
+            description="40q/8kv, 8 agents each prefilling a causal 2048-token chunk on a 16384-token prefix",
+            hidden=5120),
         WorkloadConfig(
             "llama3_70b_stress_decode", 4, 64, 8, 500000.0, 80, 1,
             _two_level(131072, 4, 8192, 16, (1, 4096)),
-            description="64q/8kv, 64 agents: 131072-token root -> 4 trunks of 8192 -> 16 agents each with U[1,4096] private tokens"),
+            description="64q/8kv, 64 agents: 131072-token root -> 4 trunks of 8192 -> 16 agents each with U[1,4096] private tokens",
+            hidden=8192),
     ]
 }
 

@@ -217,6 +217,40 @@ int32_t forkkv_write_rows(const forkkv_pool_desc* pools, int32_t layer, int32_t 
                           const void* k_base_rows, const void* v_base_rows,
                           const void* k_res_rows, const void* v_res_rows, void* stream);
 
+/* Residual rows of agents forked from a prefix (ForkKV L2 section 3, Figure 6:
+ * a child allocates only residual pages and fills them with its own xA rows;
+ * section 2 Q2: a LoRA projection is xW + xA B).  For each agent a < n_agents
+ * and token t < n_tok:
+ *   k_res = x[t] . A[a][0][r]  and  v_res = x[t] . A[a][1][r]  for r < 16,
+ * accumulated in fp32 and rounded to bf16 (nearest even), written to the
+ * residual slot slot_res[a * n_tok + t] (page = slot / 16, row = slot % 16) of
+ * layer `layer`; slot < 0 skips the pair.
+ *   x        [n_tok][hidden] bf16, device, 16-byte aligned (the prefix tokens'
+ *            inputs of the k and v projections);
+ *   A        [n_agents][2][16][hidden] bf16, device, 16-byte aligned (agent a's
+ *            LoRA down-projections of the k and v projections, as stored by
+ *            PEFT: lora_A.weight is [rank][in_features]);
+ *   hidden   a multiple of 8 (>= 8).
+ * One launch: the agents are stacked along N of one tensor-core contraction, so
+ * x is read once for all of them.  Caller-owned buffers; INVALID_ARG for a bad
+ * size, pointer or alignment; a slot past the pool sets FORKKV_DEV_BAD_PAGE. */
+int32_t forkkv_residual_fill(const forkkv_pool_desc* pools, int32_t layer, const void* x, int32_t n_tok,
+                             int32_t hidden, const void* A, int32_t n_agents, const int32_t* slot_res, void* stream);
+
+/* Decode-step append, fused (one launch): for each new token i < n_rows, its
+ * base rows as forkkv_write_rows writes them (slot_base, k_base_rows,
+ * v_base_rows; skipped when slot_base is NULL) and its residual rows computed
+ * from its hidden state: k_res = x[i] . A[ad][0][r], v_res = x[i] . A[ad][1][r]
+ * with ad = adapter_ids[i] (NULL: ad = i), fp32 accumulation, bf16 (nearest
+ * even), written at slot_res[i] (skipped when slot_res is NULL).
+ *   x [n_rows][hidden], A [n_adapters][2][16][hidden] bf16, device, 16-byte
+ *   aligned, hidden a multiple of 8; an adapter id outside [0, n_adapters)
+ *   sets FORKKV_DEV_BAD_ARG and uses adapter 0. */
+int32_t forkkv_append_rows(const forkkv_pool_desc* pools, int32_t layer, int32_t n_rows, const int32_t* slot_base,
+                           const int32_t* slot_res, const void* k_base_rows, const void* v_base_rows, const void* x,
+                           int32_t hidden, const void* A, int32_t n_adapters, const int32_t* adapter_ids,
+                           void* stream);
+
 /* Execute copy-on-write jobs on every layer (ForkServe "Status": the pack path
  * copies n_valid rows of a page, not the page).  `jobs` is HOST memory; the
  * jobs travel in the kernel's parameters, so no device buffer is needed.
