@@ -170,9 +170,12 @@ int32_t forkkv_cow_copy_rows(const forkkv_pool_desc* pools, const forkkv_cow_job
   if (n_jobs < 0 || (n_jobs > 0 && !jobs)) return FORKKV_ERR_INVALID_ARG;
   for (int32_t i = 0; i < n_jobs; ++i) {
     const forkkv_cow_job& j = jobs[i];
-    if (j.kind != FORKKV_JOB_BASE && j.kind != FORKKV_JOB_RES) return FORKKV_ERR_INVALID_ARG;
+    if (j.kind != FORKKV_JOB_BASE && j.kind != FORKKV_JOB_RES && j.kind != FORKKV_JOB_BASE_ZERO &&
+        j.kind != FORKKV_JOB_RES_ZERO)
+      return FORKKV_ERR_INVALID_ARG;
     if (j.n_valid < 0 || j.n_valid > FORKKV_PAGE_SIZE) return FORKKV_ERR_INVALID_ARG;
-    const int32_t lim = j.kind == FORKKV_JOB_BASE ? pools->num_base_pages : pools->num_res_pages;
+    const bool base = j.kind == FORKKV_JOB_BASE || j.kind == FORKKV_JOB_BASE_ZERO;
+    const int32_t lim = base ? pools->num_base_pages : pools->num_res_pages;
     if (j.src_page < 0 || j.src_page >= lim || j.dst_page < 0 || j.dst_page >= lim) return FORKKV_ERR_BAD_PAGE;
   }
   for (int32_t i = 0; i < n_jobs; i += fkv::kMaxCowJobsPerLaunch) {

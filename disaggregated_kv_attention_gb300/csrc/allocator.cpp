@@ -5,12 +5,20 @@
 // pages read-only and allocates only its residual pages) and the ForkServe
 // README ("Design vs APC" and "Methods": fork aliases the parent's frames in
 // O(pages) with refcounts, so freeing the parent keeps the trunk alive;
-// unaligned tail, pack path: the L mod P valid rows are copied into a private
-// page of the child; "Methods", LCP commit: the committed branch keeps the
-// observed prefix, a mid-page boundary is split copy-on-write and the siblings
-// are aborted, which releases their own pages and only decrements the trunk's).
-// Free-list order, id assignment and the error policy are fixed choices
-// documented in include/forkkv.h.
+// unaligned tail: the pack path copies the L mod P valid rows into a private
+// page of each child, the freeze path keeps one read-only tail page shared by
+// the children, whose own tokens start on a fresh page (pages_freeze =
+// 1 + k ceil(l / P)), which needs a fork-aware slot map: each child's slots
+// skip the rest of the frozen page; "Methods", LCP commit: the committed branch
+// keeps the observed prefix, a mid-page boundary is split copy-on-write and the
+// siblings are aborted, which releases their own pages and only decrements the
+// trunk's).  Free-list order, id assignment and the error policy are fixed
+// choices documented in include/forkkv.h.
+//
+// Slots: a sequence's keys live in slots 0, 1, ... (slot s is row s % 16 of
+// its page s / 16).  Token p sits in slot p, except in a sequence with a hole
+// [hole_start, hole_start + hole_len) (made by a freeze fork), where tokens at
+// or past hole_start sit hole_len slots further on.  Pages cover the slots.
 #include <cstdint>
 #include <new>
 #include <unordered_map>
@@ -21,9 +29,14 @@
 namespace {
 
 struct Seq {
-  int32_t length = 0;
+  int32_t length = 0;      // tokens
+  int32_t hole_start = 0;  // first slot of the hole (0 with no hole)
+  int32_t hole_len = 0;    // slots in the hole (0: none)
   std::vector<int32_t> base;
   std::vector<int32_t> res;
+  int32_t slots() const { return length + hole_len; }
+  // slots taken by the first n tokens
+  int32_t slots_of(int32_t n) const { return hole_len && n > hole_start ? n + hole_len : n; }
 };
 
 inline int32_t ceil_div(int64_t a, int64_t b) { return static_cast<int32_t>((a + b - 1) / b); }
@@ -34,16 +47,36 @@ struct forkkv_alloc {
   int32_t page = FORKKV_PAGE_SIZE;
   std::vector<int32_t> base_free, res_free;  // LIFO stacks
   std::vector<int32_t> base_ref, res_ref;
+  // a page frozen by freeze forks: its rows [0, frozen) are read by the children; only its
+  // owner (the sequence it was the partial tail of, while it holds it) may write the rest
+  std::vector<int32_t> base_frozen, res_frozen;
+  std::vector<int32_t> base_owner, res_owner;
   std::unordered_map<int32_t, Seq> seqs;
   int32_t next_id = 0;
 
   int32_t pop(bool base) {
     auto& st = base ? base_free : res_free;
-    auto& rf = base ? base_ref : res_ref;
     int32_t p = st.back();
     st.pop_back();
-    rf[p] = 1;
+    (base ? base_ref : res_ref)[p] = 1;
+    (base ? base_frozen : res_frozen)[p] = 0;
+    (base ? base_owner : res_owner)[p] = -1;
     return p;
+  }
+  // seq drops its reference to page p
+  void release(bool base, int32_t p, int32_t seq) {
+    auto& own = base ? base_owner : res_owner;
+    if (own[p] == seq) own[p] = -1;
+    if (--(base ? base_ref : res_ref)[p] == 0) {
+      (base ? base_free : res_free).push_back(p);
+      (base ? base_frozen : res_frozen)[p] = 0;
+      own[p] = -1;
+    }
+  }
+  // seq may write rows >= row of its shared page p in place (its own frozen tail, past every
+  // child's frozen rows)
+  bool writes_in_place(bool base, int32_t p, int32_t seq, int32_t row) const {
+    return (base ? base_owner : res_owner)[p] == seq && row >= (base ? base_frozen : res_frozen)[p];
   }
   Seq* find(int32_t id) {
     auto it = seqs.find(id);
@@ -70,6 +103,10 @@ int32_t forkkv_alloc_create(int32_t num_base_pages, int32_t num_res_pages, int32
     for (int32_t i = 0; i < num_res_pages; ++i) a->res_free[i] = num_res_pages - 1 - i;
     a->base_ref.assign(num_base_pages, 0);
     a->res_ref.assign(num_res_pages, 0);
+    a->base_frozen.assign(num_base_pages, 0);
+    a->res_frozen.assign(num_res_pages, 0);
+    a->base_owner.assign(num_base_pages, -1);
+    a->res_owner.assign(num_res_pages, -1);
   } catch (...) {
     delete a;
     return FORKKV_ERR_INVALID_ARG;
@@ -109,16 +146,29 @@ int32_t forkkv_seq_create(forkkv_alloc* a, int32_t n_tokens, int32_t* seq_out) {
 int32_t forkkv_fork(forkkv_alloc* a, int32_t parent, int32_t prefix_len, uint32_t flags,
                     int32_t* child_out, forkkv_cow_job* jobs, int32_t jobs_cap, int32_t* n_jobs) {
   if (!a || !child_out || !n_jobs || jobs_cap < 0 || (jobs_cap > 0 && !jobs)) return FORKKV_ERR_INVALID_ARG;
-  if (flags & ~FORKKV_FORK_SHARE_RES) return FORKKV_ERR_INVALID_ARG;
+  if (flags & ~(FORKKV_FORK_SHARE_RES | FORKKV_FORK_FREEZE_TAIL)) return FORKKV_ERR_INVALID_ARG;
   const Seq* par = a->find(parent);
   if (!par || prefix_len < 0 || prefix_len > par->length) return FORKKV_ERR_INVALID_ARG;
   const bool share_res = (flags & FORKKV_FORK_SHARE_RES) != 0;
   const int32_t P = a->page;
-  const int32_t nf = prefix_len / P, t = prefix_len % P;
+  const bool inherit = par->hole_len && prefix_len > par->hole_start;  // the prefix spans the parent's hole
+  const int32_t slot_end = par->slots_of(prefix_len);
+  const int32_t nf = slot_end / P, t = slot_end % P;
   const int32_t npg = nf + (t ? 1 : 0);
-  const int32_t need_base = t ? 1 : 0;
-  const int32_t need_res = share_res ? (t ? 1 : 0) : npg;
-  const int32_t nj = (t ? 1 : 0) * (share_res ? 2 : 1);
+  // freeze: only for an unaligned tail, and only if the child would not hold two holes
+  const bool freeze = (flags & FORKKV_FORK_FREEZE_TAIL) && t && !inherit;
+  // rows of the parent's tail page the parent has written (the rest may never have been)
+  const int32_t written = freeze ? (par->slots() - nf * P < P ? par->slots() - nf * P : P) : P;
+  int32_t need_base, need_res, nj;
+  if (freeze) {
+    need_base = 0;
+    need_res = share_res ? 0 : npg;
+    nj = (written < P ? 1 : 0) + (share_res ? (written < P ? 1 : 0) : 1);
+  } else {
+    need_base = t ? 1 : 0;
+    need_res = share_res ? (t ? 1 : 0) : npg;
+    nj = (t ? 1 : 0) * (share_res ? 2 : 1);
+  }
   if (nj > jobs_cap) return FORKKV_ERR_INVALID_ARG;
   if (need_base > static_cast<int32_t>(a->base_free.size()) || need_res > static_cast<int32_t>(a->res_free.size()))
     return FORKKV_ERR_OUT_OF_PAGES;
@@ -131,27 +181,58 @@ int32_t forkkv_fork(forkkv_alloc* a, int32_t parent, int32_t prefix_len, uint32_
     a->seqs.emplace(id, Seq());  // may throw (and invalidate nothing else) before any change
     par = a->find(parent);       // re-find: emplace may rehash
     int32_t k = 0;
+    if (inherit) {
+      c.hole_start = par->hole_start;
+      c.hole_len = par->hole_len;
+    }
     for (int32_t i = 0; i < nf; ++i) {
       c.base.push_back(par->base[i]);
       a->base_ref[par->base[i]]++;
     }
-    if (t) {
-      const int32_t dst = a->pop(true);
-      jobs[k++] = forkkv_cow_job{par->base[nf], dst, t, FORKKV_JOB_BASE};
-      c.base.push_back(dst);
-    }
-    if (share_res) {
-      for (int32_t i = 0; i < nf; ++i) {
-        c.res.push_back(par->res[i]);
-        a->res_ref[par->res[i]]++;
-      }
-      if (t) {
-        const int32_t dst = a->pop(false);
-        jobs[k++] = forkkv_cow_job{par->res[nf], dst, t, FORKKV_JOB_RES};
-        c.res.push_back(dst);
+    if (freeze) {
+      // the parent's tail page, read-only for the child: rows [0, t) are the prefix's; the
+      // child's slots [slot_end, (nf + 1) P) are a hole, its own tokens start on a fresh page
+      const int32_t tp = par->base[nf];
+      c.base.push_back(tp);
+      a->base_ref[tp]++;
+      if (a->base_frozen[tp] < t) a->base_frozen[tp] = t;
+      if (a->base_owner[tp] < 0 && par->slots() < (nf + 1) * P) a->base_owner[tp] = parent;
+      if (written < P) jobs[k++] = forkkv_cow_job{tp, tp, written, FORKKV_JOB_BASE_ZERO};
+      c.hole_start = slot_end;
+      c.hole_len = P - t;
+      if (share_res) {
+        for (int32_t i = 0; i <= nf; ++i) {
+          c.res.push_back(par->res[i]);
+          a->res_ref[par->res[i]]++;
+        }
+        const int32_t rp = par->res[nf];
+        if (a->res_frozen[rp] < t) a->res_frozen[rp] = t;
+        if (a->res_owner[rp] < 0 && par->slots() < (nf + 1) * P) a->res_owner[rp] = parent;
+        if (written < P) jobs[k++] = forkkv_cow_job{rp, rp, written, FORKKV_JOB_RES_ZERO};
+      } else {
+        for (int32_t i = 0; i < npg; ++i) c.res.push_back(a->pop(false));
+        // the child's own residual rows of the hole are never written
+        jobs[k++] = forkkv_cow_job{c.res[nf], c.res[nf], t, FORKKV_JOB_RES_ZERO};
       }
     } else {
-      for (int32_t i = 0; i < npg; ++i) c.res.push_back(a->pop(false));
+      if (t) {
+        const int32_t dst = a->pop(true);
+        jobs[k++] = forkkv_cow_job{par->base[nf], dst, t, FORKKV_JOB_BASE};
+        c.base.push_back(dst);
+      }
+      if (share_res) {
+        for (int32_t i = 0; i < nf; ++i) {
+          c.res.push_back(par->res[i]);
+          a->res_ref[par->res[i]]++;
+        }
+        if (t) {
+          const int32_t dst = a->pop(false);
+          jobs[k++] = forkkv_cow_job{par->res[nf], dst, t, FORKKV_JOB_RES};
+          c.res.push_back(dst);
+        }
+      } else {
+        for (int32_t i = 0; i < npg; ++i) c.res.push_back(a->pop(false));
+      }
     }
     a->seqs[id] = std::move(c);
     a->next_id++;
@@ -169,12 +250,15 @@ int32_t forkkv_append(forkkv_alloc* a, int32_t seq, int32_t n_tokens, forkkv_cow
   Seq* s = a->find(seq);
   if (!s) return FORKKV_ERR_INVALID_ARG;
   const int32_t P = a->page;
-  const int64_t L = s->length;
-  if (L + n_tokens > INT32_MAX) return FORKKV_ERR_INVALID_ARG;
-  const int32_t grow = ceil_div(L + n_tokens, P) - ceil_div(L, P);
-  const int32_t tail = static_cast<int32_t>(L % P);
-  const bool cow_base = n_tokens > 0 && tail && a->base_ref[s->base.back()] > 1;
-  const bool cow_res = n_tokens > 0 && tail && a->res_ref[s->res.back()] > 1;
+  const int64_t S = s->slots();
+  if (S + n_tokens > INT32_MAX) return FORKKV_ERR_INVALID_ARG;
+  const int32_t grow = ceil_div(S + n_tokens, P) - ceil_div(S, P);
+  const int32_t tail = static_cast<int32_t>(S % P);
+  // a shared partial last page is copied first, unless it is this sequence's frozen tail
+  const bool cow_base = n_tokens > 0 && tail && a->base_ref[s->base.back()] > 1 &&
+                        !a->writes_in_place(true, s->base.back(), seq, tail);
+  const bool cow_res = n_tokens > 0 && tail && a->res_ref[s->res.back()] > 1 &&
+                       !a->writes_in_place(false, s->res.back(), seq, tail);
   const int32_t nj = (cow_base ? 1 : 0) + (cow_res ? 1 : 0);
   if (nj > jobs_cap) return FORKKV_ERR_INVALID_ARG;
   if (grow + (cow_base ? 1 : 0) > static_cast<int32_t>(a->base_free.size()) ||
@@ -190,7 +274,7 @@ int32_t forkkv_append(forkkv_alloc* a, int32_t seq, int32_t n_tokens, forkkv_cow
   if (cow_base) {
     const int32_t old = s->base.back();
     const int32_t dst = a->pop(true);
-    a->base_ref[old]--;
+    a->release(true, old, seq);
     s->base.back() = dst;
     jobs[k++] = forkkv_cow_job{old, dst, tail, FORKKV_JOB_BASE};
   }
@@ -198,12 +282,12 @@ int32_t forkkv_append(forkkv_alloc* a, int32_t seq, int32_t n_tokens, forkkv_cow
   if (cow_res) {
     const int32_t old = s->res.back();
     const int32_t dst = a->pop(false);
-    a->res_ref[old]--;
+    a->release(false, old, seq);
     s->res.back() = dst;
     jobs[k++] = forkkv_cow_job{old, dst, tail, FORKKV_JOB_RES};
   }
   for (int32_t i = 0; i < grow; ++i) s->res.push_back(a->pop(false));
-  s->length = static_cast<int32_t>(L + n_tokens);
+  s->length = static_cast<int32_t>(s->length + n_tokens);
   *n_jobs = k;
   return FORKKV_OK;
 }
@@ -219,10 +303,8 @@ int32_t forkkv_free(forkkv_alloc* a, int32_t seq) {
   // pushes never exceed the pool size, so reserve once to keep push_back from throwing
   a->base_free.reserve(a->base_ref.size());
   a->res_free.reserve(a->res_ref.size());
-  for (int32_t p : s->base)
-    if (--a->base_ref[p] == 0) a->base_free.push_back(p);
-  for (int32_t p : s->res)
-    if (--a->res_ref[p] == 0) a->res_free.push_back(p);
+  for (int32_t p : s->base) a->release(true, p, seq);
+  for (int32_t p : s->res) a->release(false, p, seq);
   a->seqs.erase(seq);
   return FORKKV_OK;
 }
@@ -253,7 +335,8 @@ int32_t forkkv_commit(forkkv_alloc* a, int32_t seq, int32_t lcp_len, const int32
       if (siblings[k] == siblings[i]) return FORKKV_ERR_INVALID_ARG;
   }
   const int32_t P = a->page;
-  const int32_t keep = ceil_div(lcp_len, P), t = lcp_len % P;
+  const int32_t new_slots = s->slots_of(lcp_len);  // the hole goes too if the prefix ends at or before it
+  const int32_t keep = ceil_div(new_slots, P), t = new_slots % P;
   const int32_t np = static_cast<int32_t>(s->base.size());
   // Everything is decided before anything changes: the decrements that the sibling frees and the
   // truncation will make (a page appears at most once in one sequence), the pages they release,
@@ -285,8 +368,12 @@ int32_t forkkv_commit(forkkv_alloc* a, int32_t seq, int32_t lcp_len, const int32
     auto it = dec.find(p);
     return ref[p] - (it == dec.end() ? 0 : it->second);
   };
-  const bool split_b = t != 0 && after(a->base_ref, dec_b, s->base[keep - 1]) > 1;
-  const bool split_r = t != 0 && after(a->res_ref, dec_r, s->res[keep - 1]) > 1;
+  // a boundary page still shared is split unless it is this sequence's own frozen tail and the
+  // rows it will write lie past every child's frozen rows (a sibling that owned it is gone by then)
+  const bool split_b = t != 0 && after(a->base_ref, dec_b, s->base[keep - 1]) > 1 &&
+                       !a->writes_in_place(true, s->base[keep - 1], seq, t);
+  const bool split_r = t != 0 && after(a->res_ref, dec_r, s->res[keep - 1]) > 1 &&
+                       !a->writes_in_place(false, s->res[keep - 1], seq, t);
   if ((split_b ? 1 : 0) + (split_r ? 1 : 0) > jobs_cap) return FORKKV_ERR_INVALID_ARG;
   if ((split_b && free_b < 1) || (split_r && free_r < 1)) return FORKKV_ERR_OUT_OF_PAGES;
   // 1. abort the siblings, in the order given
@@ -294,26 +381,27 @@ int32_t forkkv_commit(forkkv_alloc* a, int32_t seq, int32_t lcp_len, const int32
     if (forkkv_free(a, siblings[i]) != FORKKV_OK) return FORKKV_ERR_REFCOUNT;  // excluded by the checks above
   s = a->find(seq);
   // 2. truncate: pages past the committed prefix, base then residual, in logical order
-  for (int32_t j = keep; j < np; ++j)
-    if (--a->base_ref[s->base[j]] == 0) a->base_free.push_back(s->base[j]);
-  for (int32_t j = keep; j < np; ++j)
-    if (--a->res_ref[s->res[j]] == 0) a->res_free.push_back(s->res[j]);
+  a->base_free.reserve(a->base_ref.size());
+  a->res_free.reserve(a->res_ref.size());
+  for (int32_t j = keep; j < np; ++j) a->release(true, s->base[j], seq);
+  for (int32_t j = keep; j < np; ++j) a->release(false, s->res[j], seq);
   s->base.resize(keep);
   s->res.resize(keep);
   // 3. a boundary page still shared is split: a private copy of its first t rows
   int32_t k = 0;
   if (split_b) {
     const int32_t old = s->base[keep - 1], dst = a->pop(true);
-    a->base_ref[old]--;
+    a->release(true, old, seq);
     s->base[keep - 1] = dst;
     jobs[k++] = forkkv_cow_job{old, dst, t, FORKKV_JOB_BASE};
   }
   if (split_r) {
     const int32_t old = s->res[keep - 1], dst = a->pop(false);
-    a->res_ref[old]--;
+    a->release(false, old, seq);
     s->res[keep - 1] = dst;
     jobs[k++] = forkkv_cow_job{old, dst, t, FORKKV_JOB_RES};
   }
+  if (s->hole_len && lcp_len <= s->hole_start) s->hole_start = s->hole_len = 0;
   s->length = lcp_len;
   *n_jobs = k;
   return FORKKV_OK;
@@ -354,7 +442,19 @@ int32_t forkkv_page_tables(const forkkv_alloc* a, const int32_t* seqs, int32_t n
       b[j] = j < np ? s->base[j] : -1;
       r[j] = j < np ? s->res[j] : -1;
     }
-    seq_lens[i] = s->length;
+    seq_lens[i] = s->slots();
+  }
+  return FORKKV_OK;
+}
+
+int32_t forkkv_slot_maps(const forkkv_alloc* a, const int32_t* seqs, int32_t n, int32_t* holes) {
+  if (!a || n < 0 || (n > 0 && (!seqs || !holes))) return FORKKV_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i)
+    if (!a->find(seqs[i])) return FORKKV_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    const Seq* s = a->find(seqs[i]);
+    holes[2 * i] = s->hole_start;
+    holes[2 * i + 1] = s->hole_len;
   }
   return FORKKV_OK;
 }

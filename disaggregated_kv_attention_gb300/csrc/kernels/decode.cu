@@ -111,6 +111,7 @@ struct DecodeArgs {
   int32_t pt_stride;
   const int32_t* seq_lens;
   const int32_t* positions;
+  const int32_t* holes;  // [n_agents][2] slot map (first hole slot, hole length), or null
   const __nv_bfloat16* B_k;  // [n_adapters][16][Hkv*128]
   const int32_t* adapter_ids;
   int32_t n_adapters;
@@ -130,13 +131,16 @@ struct DecodeArgs {
 // producer warp describes each unit of its CTA, in order, in a ring of two descriptors in
 // shared memory (kUnitInts int32 each, one field per lane when built) that the other warps
 // read at the start of the unit.
-constexpr int kUnitInts = 24;
+constexpr int kUnitInts = 26;
 enum {
   kUfP0, kUfP1, kUfNa, kUfH, kUfSlot, kUfEnd,  // page range, agents, KV head, first slot, end of list
-  kUfAgent = 6, kUfL = 10, kUfPos = 14, kUfAdapter = 18  // per agent (4 each): index, keys, position, adapter
+  kUfAgent = 6, kUfL = 10, kUfPos = 14, kUfAdapter = 18,  // per agent (4 each): index, keys, position, adapter,
+  kUfHole = 22                                           // hole (16 * first slot + length, 0: none)
 };
 constexpr int kOffUnits = 1408;  // 2 x kUnitInts int32 in the header of shared memory
-static_assert(kOffUnits + 2 * kUnitInts * 4 <= 2048, "unit ring overlaps the operand tiles");
+constexpr int kOffHoles = 1664;  // the softmax warps' copies of the unit's hole codes
+static_assert(kOffUnits + 2 * kUnitInts * 4 <= kOffHoles && kOffHoles + 4 * kMaxGroup * 4 <= 2048,
+              "unit ring and hole codes overlap each other or the operand tiles");
 
 // The first unit of this CTA: plan record blockIdx.x, or unit code blockIdx.x (-1: none).
 __device__ __forceinline__ int32_t first_unit(const DecodeArgs& a) {
@@ -226,6 +230,16 @@ __device__ __forceinline__ int32_t unit_field(const DecodeArgs& a, int32_t r, in
     case kUfL: return x < na ? __ldg(a.seq_lens + agx) : 0;  // clipped and checked at publication
     case kUfPos: return __ldg(a.positions + agx);
     case kUfAdapter: return a.adapter_ids ? __ldg(a.adapter_ids + agx) : agx;
+    case kUfHole: {
+      if (!a.holes) return 0;
+      const int32_t hs = __ldg(a.holes + 2 * agx), hn = __ldg(a.holes + 2 * agx + 1);
+      if (hn == 0) return 0;
+      if (hn < 0 || hn >= kPage || hs < 0 || hs > (1 << 26)) {
+        flag_status(a.status, kDevBadArg);
+        return 0;
+      }
+      return hs * kPage + hn;
+    }
     default: return 0;
   }
 }
@@ -359,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   float* s_mref = reinterpret_cast<float*>(smem + 768);     // [4 warps][4 agents][8] reference maxima
   int32_t* s_lp = reinterpret_cast<int32_t*>(smem + 1280);  // [4 warps][4 agents][2] length, position
   int32_t* s_units = reinterpret_cast<int32_t*>(smem + kOffUnits);  // [2][kUnitInts] unit descriptors
+  int32_t* s_lh = reinterpret_cast<int32_t*>(smem + kOffHoles);      // [4 warps][4 agents] hole codes
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
@@ -696,9 +711,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     for (int k = 0; ok; ++k) {
       if (!unit_wait(k)) break;
       const int32_t p0 = unit_at(k, kUfP0), p1 = unit_at(k, kUfP1), na = unit_at(k, kUfNa);
+      // The key in slot j sits at position j, or j - hole length past the agent's hole.  Agents
+      // that share a page past a hole have the same hole (it came with the pages), and a slot in
+      // the page of a hole is at its own index for every agent that sees it, so the first
+      // agent's hole gives the rotation position of every visible key of the item.
+      const int32_t hc0 = unit_at(k, kUfHole);
       const bool end = unit_at(k, kUfEnd) != 0;
       unit_release(k);
       if (end) break;
+      const int32_t hend = (hc0 >> 4) + (hc0 & 15), hn0 = hc0 & 15;
       const int N = blocks_of(p0, p1) * na;
       for (int n = 0; n < N && ok; ++n) {
         const int b = n / na, ai = n - b * na;
@@ -708,16 +729,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const int j = pbase * kPage + row;
         if (ai == 0) {
           // chunk c = 32 hf + 16 cc holds frequency groups m = c/2 .. c/2 + 7: 32-byte units
-          // c/8 and c/8 + 1 of the row, stored at unit u ^ (j % 8)
-          const int jr = j < a.rope_positions ? j : 0;
+          // c/8 and c/8 + 1 of the row of position jr, stored at unit u ^ (jr % 8)
+          const int kp = (hn0 != 0 && j >= hend) ? j - hn0 : j;
+          const int jr = kp < a.rope_positions ? kp : 0;
           const uint4* rrow = reinterpret_cast<const uint4*>(a.rope + (int64_t)jr * kRopeRow);
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
             for (int uu = 0; uu < 2; ++uu) {
               const int un = 4 * hf + 2 * cc + uu;
-              rp[cc][2 * uu] = __ldg(rrow + (un ^ (j & 7)) * 2);
-              rp[cc][2 * uu + 1] = __ldg(rrow + (un ^ (j & 7)) * 2 + 1);
+              rp[cc][2 * uu] = __ldg(rrow + (un ^ (jr & 7)) * 2);
+              rp[cc][2 * uu + 1] = __ldg(rrow + (un ^ (jr & 7)) * 2 + 1);
             }
           ok = mbar_wait(&bars[kKFull0 + stage], (g >> 1) & 1, a.status);
           if (!ok) break;
@@ -855,6 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const uint32_t tl = tm + ((uint32_t)(32 * sw_) << 16);
     float* mref = s_mref + sw_ * (kMaxGroup * 8);  // this warp's copy (all four evolve identically)
     int32_t* lp = s_lp + sw_ * (kMaxGroup * 2);    // this warp's copy of each agent's (length, position)
+    int32_t* lh = s_lh + sw_ * kMaxGroup;          // and of each agent's hole code
     // query head whose warp-wide reductions this lane ends up holding, and the lanes that publish them
     const int gl = kG == 8 ? lane >> 2 : lane >> 3;
     const bool publisher = kG == 8 ? (lane & 3) == 0 : (lane & 7) == 0;
@@ -870,6 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (lane < kMaxGroup) {
         lp[2 * lane] = unit_at(k, kUfL + lane);  // 0 past the unit's agents
         lp[2 * lane + 1] = unit_at(k, kUfPos + lane);
+        lh[lane] = unit_at(k, kUfHole + lane);
       }
       unit_release(k);
       if (end) break;
@@ -879,8 +903,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const int g = gb + b, m = gn + n;  // global block and step
         const int pbase = p0 + b * kBlockPages;
         const int j = pbase * kPage + row;
-        const int32_t L = lp[2 * ai], pos = lp[2 * ai + 1];
-        const bool vis = j < L && j <= pos && j < p1 * kPage;
+        const int32_t L = lp[2 * ai], pos = lp[2 * ai + 1], hc = lh[ai];
+        // slot j: hidden in the agent's hole; past it, its key position is j - hole length
+        const int32_t hs = hc >> 4, hn = hc & 15;
+        const bool in_hole = hn != 0 && j >= hs && j < hs + hn;
+        const int32_t kp = (hn != 0 && j >= hs + hn) ? j - hn : j;
+        const bool vis = j < L && !in_hole && kp <= pos && j < p1 * kPage;
         const int sr = m % kSRing;
         ok = mbar_wait(&bars[kSFull0 + sr], (m / kSRing) & 1, a.status);
         if (!ok) break;
@@ -1191,6 +1219,7 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   a.pt_stride = p.pt_stride;
   a.seq_lens = p.seq_lens;
   a.positions = p.positions;
+  a.holes = p.holes;
   a.B_k = static_cast<const __nv_bfloat16*>(p.B_k);
   a.adapter_ids = p.adapter_ids;
   a.n_adapters = p.n_adapters;

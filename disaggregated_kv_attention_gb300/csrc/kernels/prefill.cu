@@ -122,6 +122,7 @@ struct PrefillArgs {
   int32_t pt_stride, max_seq_len;
   const int32_t* seq_lens;
   const int32_t* positions;  // [A][q_len]
+  const int32_t* holes;      // [A][2] slot map (first hole slot, hole length), or null
   const __nv_bfloat16* B_k;
   const __nv_bfloat16* B_v;
   const int32_t* adapter_ids;
@@ -149,6 +150,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int32_t L = min(a.seq_lens[agent], a.max_seq_len);
   int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
   if ((uint32_t)adapter >= (uint32_t)a.n_adapters) adapter = 0;
+  // the agent's slot map: the key in slot j is hidden in [hs, hs + hn) and sits at position
+  // j - hn past it (kpos); token position p sits in slot p, or p + hn from hs on
+  int32_t hs = a.holes ? a.holes[2 * agent] : 0, hn = a.holes ? a.holes[2 * agent + 1] : 0;
+  if (hn < 0 || hn >= kPage || hs < 0) {
+    if (threadIdx.x == 0) flag_status(a.status, kDevBadArg);
+    hs = hn = 0;
+  }
+  auto kpos = [&](int j) { return (hn != 0 && j >= hs + hn) ? j - hn : j; };
+  // key positions grow with the slot, so "position <= p" is "slot <= slot of p" (hole aside)
+  auto slot_of = [&](int32_t p) { return (hn != 0 && p >= hs) ? p + hn : p; };
+  const int32_t hlo = hn != 0 ? hs : 0, hhi = hn != 0 ? hs + hn : 0;  // hidden slots [hlo, hhi)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kKStages; ++i) {
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (a.seq_lens[agent] < 1 || a.seq_lens[agent] > a.max_seq_len) flag_status(a.status, kDevBadArg);
     if ((uint32_t)(a.adapter_ids ? a.adapter_ids[agent] : agent) >= (uint32_t)a.n_adapters)
       flag_status(a.status, kDevBadArg);
-    s_meta[0] = max(0, min(pmax + 1, L));
+    s_meta[0] = max(0, min(slot_of(pmax) + 1, L));
   }
   if (warp == 1) tc::alloc(s_tmem, kTmCols);
   tc::fence_before();
@@ -452,15 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       uint8_t* st = smem + kOffKStage + stage * kStageBytes;
       const uint32_t ub = tl + kTmBuf + 128 * (b & 1);
       const int j = b * kBlockKeys + row;
-      const int jr = j < a.rope_positions ? j : 0;
-      // this key's rotation row: frequency groups 4 u .. 4 u + 3 are 32-byte unit u, stored at
-      // unit u ^ (j % 8); this half needs units 4 hf .. 4 hf + 3
+      const int jr = kpos(j) < a.rope_positions ? kpos(j) : 0;
+      // this key's rotation row (position jr): frequency groups 4 u .. 4 u + 3 are 32-byte unit u,
+      // stored at unit u ^ (jr % 8); this half needs units 4 hf .. 4 hf + 3
       const uint4* rrow = reinterpret_cast<const uint4*>(a.rope + (int64_t)jr * kRopeRow);
       uint4 rp[4][2];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        rp[u][0] = rrow[((4 * hf + u) ^ (j & 7)) * 2];
-        rp[u][1] = rrow[((4 * hf + u) ^ (j & 7)) * 2 + 1];
+        rp[u][0] = rrow[((4 * hf + u) ^ (jr & 7)) * 2];
+        rp[u][1] = rrow[((4 * hf + u) ^ (jr & 7)) * 2 + 1];
       }
       ok = mbar_wait(&bars[kKFull0 + stage], (b / kKStages) & 1, a.status) &&
            mbar_wait(&bars[kUFull0 + (b & 1)], (b >> 1) & 1, a.status);
@@ -519,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int64_t tq = valid ? f / G : 0;
     const int gq = valid ? (int)(f % G) : 0;
     const int32_t pos = valid ? a.positions[(int64_t)agent * a.q_len + tq] : -1;
+    const int32_t lim = min(L, slot_of(pos) + 1);  // slots below lim (outside the hole) are visible
     const int64_t orow = (((int64_t)agent * a.q_len + tq) * a.hkv * G + (int64_t)h * G + gq) * kHeadDim;
     {  // this half of the Q row into tensor memory (d = 64 sh .. 64 sh + 63 as bf16 pairs in
        // columns 32 sh ..); this half of the B_v slice
@@ -556,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tc::fence_after();
       const int kbase = b * kBlockKeys + 64 * sh;
       // keys of this half all visible to this row: no per-key mask (every block below the diagonal)
-      const bool open = kbase + 64 <= L && kbase + 63 <= pos;
+      const bool open = kbase + 64 <= lim && !(kbase < hhi && kbase + 64 > hlo);
       float bm = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
@@ -573,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int j = kbase + c + i;
-            if (j < L && j <= pos) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(v[i]));
+            if (j < lim && (j < hlo || j >= hhi)) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(v[i]));
           }
         }
         bm = fmaxf(bm, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
@@ -636,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             for (int e = 0; e < 2; ++e) {
               const int j = kbase + c + 2 * i + e;
               const float x = ex2(fmaf(__uint_as_float(v[2 * i + e]), a.scale_log2, -mu));
-              pr[e] = (j < L && j <= pos) ? x : 0.f;
+              pr[e] = (j < lim && (j < hlo || j >= hhi)) ? x : 0.f;
             }
             ls2[i & 1] = f2_add(ls2[i & 1], f2(pr[0], pr[1]));
             pw[(c >> 1) + i] = pack_bf16(pr[0], pr[1]);
@@ -746,6 +759,7 @@ cudaError_t launch_prefill(const forkkv_attn_params& p, const void* rope_table, 
   a.max_seq_len = p.max_seq_len;
   a.seq_lens = p.seq_lens;
   a.positions = p.positions;
+  a.holes = p.holes;
   a.B_k = static_cast<const __nv_bfloat16*>(p.B_k);
   a.B_v = static_cast<const __nv_bfloat16*>(p.B_v);
   a.adapter_ids = p.adapter_ids;

@@ -82,10 +82,33 @@ struct CowArgs {
 
 // blockIdx.x = job, blockIdx.y = layer.  A base row t occupies the two 128-byte
 // segments at t*128 and 2048 + t*128 of each (head, page) tile (the swizzle only
-// permutes chunks inside a segment), a residual row the 32 bytes at t*32.
+// permutes chunks inside a segment), a residual row the 32 bytes at t*32.  Zero
+// jobs clear rows n_valid..15 of their page (the unwritten rows of a frozen tail).
 __global__ void __launch_bounds__(256) cow_copy_kernel(const CowArgs a, const __grid_constant__ CowJobBatch b) {
   const forkkv_cow_job job = b.jobs[blockIdx.x];
   const int64_t layer = blockIdx.y;
+  if (job.kind == FORKKV_JOB_BASE_ZERO || job.kind == FORKKV_JOB_RES_ZERO) {
+    const int32_t rows = kPage - job.n_valid;
+    if (job.kind == FORKKV_JOB_BASE_ZERO) {
+      const int32_t per_tile = rows * 16;  // 16-byte chunks of the cleared rows
+      for (int32_t i = threadIdx.x; i < a.hkv * 2 * per_tile; i += blockDim.x) {
+        const int32_t tile = i / per_tile, c = i % per_tile;
+        const int32_t h = tile >> 1, kv = tile & 1;
+        const int32_t t = job.n_valid + (c >> 4), part = (c >> 3) & 1, w = c & 7;
+        uint8_t* pool = (kv ? a.v_base : a.k_base) + layer * a.base_layer_bytes;
+        *reinterpret_cast<uint4*>(pool + ((int64_t)h * a.num_base_pages + job.dst_page) * kBaseTile + part * 2048 +
+                                  t * 128 + w * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else {
+      for (int32_t i = threadIdx.x; i < 2 * rows * 2; i += blockDim.x) {
+        const int32_t kv = i / (rows * 2), c = i % (rows * 2);
+        uint8_t* pool = (kv ? a.v_res : a.k_res) + layer * a.res_layer_bytes;
+        *reinterpret_cast<uint4*>(pool + (int64_t)job.dst_page * kResTile + (job.n_valid + (c >> 1)) * 32 +
+                                  (c & 1) * 16) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
   if (job.kind == FORKKV_JOB_BASE) {
     const int32_t per_tile = job.n_valid * 16;  // 16-byte chunks of the valid rows
     const int32_t total = a.hkv * 2 * per_tile;

@@ -29,7 +29,10 @@ PLAN_ITEM_INTS = 16
 PLAN_UNIT_INTS = 16
 JOB_BASE = 0
 JOB_RES = 1
+JOB_BASE_ZERO = 2
+JOB_RES_ZERO = 3
 FORK_SHARE_RES = 1
+FORK_FREEZE_TAIL = 2
 DEV_BAD_PAGE, DEV_TIMEOUT, DEV_BAD_ARG = 1, 2, 4
 
 
@@ -74,6 +77,7 @@ class forkkv_attn_params(ctypes.Structure):
         ("plan", ctypes.c_void_p), ("plan_items", ctypes.c_int32), ("plan_slots", ctypes.c_int32),
         ("plan_ctas", ctypes.c_int32),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("holes", ctypes.c_void_p),
     ]
 
 
@@ -92,6 +96,7 @@ _SIGNATURES = {
     "forkkv_commit": ([_vp, _i32, _i32, _vp, _i32, _P(forkkv_cow_job), _i32, _P(_i32)], _i32),
     "forkkv_lcp_len": ([_vp, _i32, _vp, _i32, _P(_i32)], _i32),
     "forkkv_seq_len": ([_vp, _i32, _P(_i32)], _i32),
+    "forkkv_slot_maps": ([_vp, _vp, _i32, _vp], _i32),
     "forkkv_page_tables": ([_vp, _vp, _i32, _i32, _vp, _vp, _vp], _i32),
     "forkkv_refcount": ([_vp, _i32, _i32, _P(_i32)], _i32),
     "forkkv_stats_get": ([_vp, _P(forkkv_stats)], _i32),
@@ -234,6 +239,15 @@ def forkkv_page_tables(alloc: int, seqs: Sequence[int], stride: int):
     return bpt, rpt, lens
 
 
+def forkkv_slot_maps(alloc: int, seqs: Sequence[int]) -> np.ndarray:
+    """[n, 2] int32: each sequence's hole (first slot, length), (0, 0) without one."""
+    n = len(seqs)
+    s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+    holes = np.zeros((n, 2), np.int32)
+    _check(lib().forkkv_slot_maps(alloc, s.ctypes.data, n, holes.ctypes.data), "slot_maps")
+    return holes
+
+
 def forkkv_refcount(alloc: int, kind: int, page: int) -> int:
     out = ctypes.c_int32()
     _check(lib().forkkv_refcount(alloc, kind, page, ctypes.byref(out)), "refcount")
@@ -334,7 +348,8 @@ def attn_params(pools: Pools, layer: int, q: torch.Tensor, out: torch.Tensor, bp
                 seq_lens: torch.Tensor, positions: torch.Tensor, max_seq_len: int, B_k: torch.Tensor,
                 B_v: torch.Tensor, adapter_ids: Optional[torch.Tensor] = None, rope: Optional[torch.Tensor] = None,
                 rope_theta: float = 0.0, sm_scale: float = 0.0, plan: Optional[torch.Tensor] = None,
-                plan_info: Optional[forkkv_plan_info] = None) -> forkkv_attn_params:
+                plan_info: Optional[forkkv_plan_info] = None,
+                holes: Optional[torch.Tensor] = None) -> forkkv_attn_params:
     """Fill a forkkv_attn_params from tensors (q/out [A, q_len, Hq, 128], tables [A, stride])."""
     A, q_len, Hq, D = q.shape
     p = forkkv_attn_params()
@@ -352,6 +367,7 @@ def attn_params(pools: Pools, layer: int, q: torch.Tensor, out: torch.Tensor, bp
     p.rope_table_positions = 0 if rope is None else rope.shape[0]
     p.rope_theta = rope_theta
     p.sm_scale = sm_scale
+    p.holes = _ptr(holes)
     if plan is not None:
         p.plan, p.plan_items, p.plan_slots = plan.data_ptr(), plan_info.n_items, plan_info.n_slots
         p.plan_ctas = plan_info.n_ctas

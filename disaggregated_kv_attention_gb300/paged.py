@@ -17,6 +17,15 @@ from . import forkkv as fk
 from . import workload as wl
 
 
+def token_slots(hole, start: int, n: int) -> np.ndarray:
+    """Slots of tokens [start, start + n) of a sequence whose slot map is `hole` = (first hole slot,
+    hole length), as include/forkkv.h defines them: token p sits in slot p, or p + hole length when the
+    sequence has a hole and p is at or past its first slot."""
+    p = np.arange(start, start + n, dtype=np.int64)
+    hs, hn = int(hole[0]), int(hole[1])
+    return np.where((hn > 0) & (p >= hs), p + hn, p)
+
+
 def _slots(bpt_row: np.ndarray, start: int, n: int) -> np.ndarray:
     j = np.arange(start, start + n)
     return (bpt_row[j // 16].astype(np.int64) * 16 + (j % 16)).astype(np.int32)

@@ -98,9 +98,15 @@ typedef struct forkkv_alloc forkkv_alloc;
 
 #define FORKKV_JOB_BASE 0  /* copy rows of a base page (all layers, all KV heads, K and V) */
 #define FORKKV_JOB_RES 1   /* copy rows of a residual page (all layers, k_res and v_res)  */
+#define FORKKV_JOB_BASE_ZERO 2 /* zero rows n_valid..15 of base page dst_page (all layers, heads, K and V) */
+#define FORKKV_JOB_RES_ZERO 3  /* zero rows n_valid..15 of residual page dst_page (all layers)             */
 
 /* One copy-on-write job: rows [0, n_valid) of page src_page are copied into
- * page dst_page; rows n_valid..15 of dst_page are left untouched. */
+ * page dst_page; rows n_valid..15 of dst_page are left untouched.  A zero job
+ * (kind *_ZERO, src_page == dst_page) instead sets rows n_valid..15 of
+ * dst_page to zero: rows of a frozen tail page that no token has been written
+ * to, which the children's slot maps skip (so that a zero probability never
+ * meets a never-written value row). */
 typedef struct {
   int32_t src_page;
   int32_t dst_page;
@@ -108,7 +114,8 @@ typedef struct {
   int32_t kind; /* FORKKV_JOB_BASE or FORKKV_JOB_RES */
 } forkkv_cow_job;
 
-#define FORKKV_FORK_SHARE_RES 1u /* child aliases the parent's residual pages too */
+#define FORKKV_FORK_SHARE_RES 1u   /* child aliases the parent's residual pages too */
+#define FORKKV_FORK_FREEZE_TAIL 2u /* unaligned prefix: share the tail page read-only, no copy */
 
 typedef struct {
   int32_t n_seqs;
@@ -142,9 +149,31 @@ int32_t forkkv_seq_create(forkkv_alloc* alloc, int32_t n_tokens, int32_t* seq_ou
 int32_t forkkv_fork(forkkv_alloc* alloc, int32_t parent, int32_t prefix_len, uint32_t flags,
                     int32_t* child_out, forkkv_cow_job* jobs, int32_t jobs_cap, int32_t* n_jobs);
 
-/* Grow a sequence by n_tokens >= 0.  A partial last page that is shared
+/* Freeze-tail fork (FORKKV_FORK_FREEZE_TAIL; ForkServe README, adaptive
+ * unaligned tail: pages_freeze = 1 + k ceil(l / P), one read-only tail page
+ * shared by the k children instead of a copy in each; "it needs a fork-aware
+ * slot map").  With the flag and prefix_len % 16 = t != 0 the child also
+ * aliases the parent's partial tail page (refcount + 1, no copy); the child's
+ * slots [prefix_len, next multiple of 16) become a hole that its slot map
+ * skips, so its own tokens start on a fresh page, and its residual pages are
+ * new (or, with FORKKV_FORK_SHARE_RES, the parent's residual tail page is
+ * shared the same way).  The parent keeps writing its later tokens into the
+ * same page in place (the children read only its first t rows).  Zero jobs
+ * (FORKKV_JOB_*_ZERO) clear the rows of that page no token has been written
+ * to yet, and the hole rows of the child's own residual page: run a fork's jobs
+ * before writing new rows.  A sequence holds at most one hole: a freeze fork
+ * whose prefix spans the parent's hole is a pack fork (the child inherits the
+ * parent's hole).  Without an unaligned tail the flag changes nothing.
+ *
+ * Slots: a sequence's keys occupy slots 0, 1, ... (slot s is row s % 16 of its
+ * page s / 16); token p is in slot p, or p + hole_len if the sequence has a
+ * hole and p >= hole_start.  Page tables and lengths count slots.
+ *
+ * Grow a sequence by n_tokens >= 0.  A partial last page that is shared
  * (refcount > 1) is first replaced by a private copy (one job per pool, at
- * most 2), then ceil-new-length pages are added in logical order. */
+ * most 2) unless it is this sequence's frozen tail page past every child's
+ * frozen rows (written in place), then pages covering the new slots are added
+ * in logical order. */
 int32_t forkkv_append(forkkv_alloc* alloc, int32_t seq, int32_t n_tokens, forkkv_cow_job* jobs,
                       int32_t jobs_cap, int32_t* n_jobs);
 
@@ -185,10 +214,16 @@ int32_t forkkv_lcp_len(const int32_t* spec, int32_t n_spec, const int32_t* obser
 int32_t forkkv_seq_len(const forkkv_alloc* alloc, int32_t seq, int32_t* len_out);
 
 /* Page tables of n sequences, row-major [n][stride] (host memory), unused
- * entries set to -1, and their lengths.  INVALID_ARG if a sequence has more
- * than stride pages. */
+ * entries set to -1, and their lengths in slots (tokens + hole length, the
+ * seq_lens the attention calls take).  INVALID_ARG if a sequence has more than
+ * stride pages. */
 int32_t forkkv_page_tables(const forkkv_alloc* alloc, const int32_t* seqs, int32_t n, int32_t stride,
                            int32_t* bpt, int32_t* rpt, int32_t* seq_lens);
+
+/* Slot maps of n sequences (host memory): holes[2 i] = first slot of sequence
+ * i's hole, holes[2 i + 1] = its length (0, 0 without a hole); the holes array
+ * of the attention calls. */
+int32_t forkkv_slot_maps(const forkkv_alloc* alloc, const int32_t* seqs, int32_t n, int32_t* holes);
 
 int32_t forkkv_refcount(const forkkv_alloc* alloc, int32_t kind, int32_t page, int32_t* out);
 int32_t forkkv_stats_get(const forkkv_alloc* alloc, forkkv_stats* out);
@@ -316,8 +351,11 @@ typedef struct {
   const int32_t* bpt;      /* [A][pt_stride] base page ids (device) */
   const int32_t* rpt;      /* [A][pt_stride] residual page ids (device) */
   int32_t pt_stride;
-  const int32_t* seq_lens; /* [A] keys of each agent, including the query tokens' own rows */
-  const int32_t* positions;/* [A][q_len] absolute query positions; key j visible iff j <= position */
+  const int32_t* seq_lens; /* [A] key slots of each agent (forkkv_page_tables), including the query
+                              tokens' own rows */
+  const int32_t* positions;/* [A][q_len] absolute query positions; the key in slot s is visible iff
+                              s < seq_len, s is not in the agent's hole and its position (s, or
+                              s - hole_len past the hole) <= the query position */
   int32_t max_seq_len;     /* host-known bound on every seq_len */
   const void* B_k;         /* bf16 [n_adapters][16][num_kv_heads * 128] */
   const void* B_v;         /* bf16 [n_adapters][16][num_kv_heads * 128] */
@@ -333,6 +371,8 @@ typedef struct {
   int32_t plan_ctas;
   void* workspace;         /* device scratch, >= the *_workspace_size bytes, 256-byte aligned */
   size_t workspace_bytes;
+  const int32_t* holes;    /* [A][2] device: each agent's slot map (first hole slot, hole length;
+                              forkkv_slot_maps), or NULL when no agent has a hole */
 } forkkv_attn_params;
 
 /* Scratch bytes forkkv_residual_attn_decode needs for these params. */

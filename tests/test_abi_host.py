@@ -76,11 +76,11 @@ class _Pair:
     def _m_create(self, n):
         return self.m.seq_create(n)
 
-    def _c_fork(self, p, n, share):
-        return fk.forkkv_fork(self.c, p, n, fk.FORK_SHARE_RES if share else 0)
+    def _c_fork(self, p, n, share, freeze=False):
+        return fk.forkkv_fork(self.c, p, n, (fk.FORK_SHARE_RES if share else 0) | (fk.FORK_FREEZE_TAIL if freeze else 0))
 
-    def _m_fork(self, p, n, share):
-        return self.m.fork(p, n, share_res=share)
+    def _m_fork(self, p, n, share, freeze=False):
+        return self.m.fork(p, n, share_res=share, freeze=freeze)
 
     def _c_append(self, s, n):
         return fk.forkkv_append(self.c, s, n)
@@ -119,6 +119,7 @@ class _Pair:
             assert np.array_equal(b, np.array(mb, np.int32))
             assert np.array_equal(r, np.array(mr, np.int32))
             assert np.array_equal(l, np.array(ml, np.int32))
+            assert np.array_equal(fk.forkkv_slot_maps(self.c, sids), np.array(self.m.slot_maps(sids), np.int32))
         for p in range(0, len(self.m.base_ref), 7):
             assert fk.forkkv_refcount(self.c, fk.JOB_BASE, p) == self.m.base_ref[p]
 
@@ -150,7 +151,8 @@ def test_cpp_allocator_matches_model_on_random_operations():
                 live.append(sid)
         elif x < 0.5:
             par = rnd.choice(live)
-            res = pr.op("fork", par, rnd.randint(0, pr.m.seqs[par].length + 2), rnd.random() < 0.3)
+            res = pr.op("fork", par, rnd.randint(0, pr.m.seqs[par].length + 2), rnd.random() < 0.3,
+                        rnd.random() < 0.4)
             if res is not None:
                 live.append(res[0])
         elif x < 0.8:
@@ -182,7 +184,7 @@ def test_cpp_commit_and_abort_match_model():
                 live.append(sid)
         elif x < 0.42:
             par = rnd.choice(live)
-            res = pr.op("fork", par, rnd.randint(0, pr.m.seqs[par].length), rnd.random() < 0.3)
+            res = pr.op("fork", par, rnd.randint(0, pr.m.seqs[par].length), rnd.random() < 0.3, rnd.random() < 0.4)
             if res is not None:
                 live.append(res[0])
         elif x < 0.62:
@@ -319,3 +321,26 @@ def test_plan_covers_every_page_once(shape, target):
             assert (ag, pg) in cover
         assert sorted(slots[off[ag]:off[ag + 1]]) == sorted(s for s, o in slot_owner.items() if o == ag)
     assert off[A] == info.n_slots
+
+
+
+def test_cpp_freeze_fanout_matches_model():
+    """Same-batch fan-outs of unaligned trunks with the freeze flag, the parent writing on, children
+    appending, committing and aborting: ids, jobs (copies and zero jobs), tables, slot maps."""
+    for L, k, ell in [(2050, 4, 48), (40, 6, 3), (16, 3, 20), (1000, 8, 200)]:
+        pr = _Pair(4000, 8000)
+        root = pr.op("create", L)
+        kids = []
+        for i in range(k):
+            c, jobs = pr.op("fork", root, L, i % 2 == 1, True)
+            kids.append(c)
+            pr.op("append", c, ell)
+            pr.op("append", root, 1)
+        pr.check_state()
+        pr.op("commit", kids[0], L - 1, kids[1:3])
+        if k > 3:
+            pr.op("abort", kids[3])
+        pr.check_state()
+        pr.op("free", root)
+        pr.check_state()
+        pr.close()

@@ -14,7 +14,7 @@ import pytest
 
 from oracle import accounting as acc
 from oracle.allocator import (AllocatorError, AllocatorModel, ERR_INVALID_ARG, ERR_OUT_OF_PAGES,
-                              JOB_BASE, JOB_RES, lcp_len)
+                              JOB_BASE, JOB_BASE_ZERO, JOB_RES, JOB_RES_ZERO, lcp_len)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 P = 16
@@ -142,7 +142,8 @@ def _check_invariants(m: AllocatorModel):
     assert st["base_live"] + st["base_free"] == len(m.base_ref)
     assert st["res_live"] + st["res_free"] == len(m.res_ref)
     for s in m.seqs.values():
-        assert len(s.base) == len(s.res) == math.ceil(s.length / P)
+        assert len(s.base) == len(s.res) == math.ceil(s.slots() / P)
+        assert s.hole_len == 0 or (0 < s.hole_len < P and (s.hole_start + s.hole_len) % P == 0)
 
 
 def test_random_operations_keep_invariants():
@@ -158,7 +159,8 @@ def test_random_operations_keep_invariants():
                 live.append(m.seq_create(rnd.randint(0, 70)))
             elif op < 0.5:
                 par = rnd.choice(live)
-                c, _ = m.fork(par, rnd.randint(0, m.seqs[par].length), share_res=rnd.random() < 0.3)
+                c, _ = m.fork(par, rnd.randint(0, m.seqs[par].length), share_res=rnd.random() < 0.3,
+                              freeze=rnd.random() < 0.4)
                 live.append(c)
             elif op < 0.8:
                 m.append(rnd.choice(live), rnd.randint(0, 40))
@@ -320,3 +322,47 @@ def test_lcp_len_pins():
     assert lcp_len([5, 6, 7, 8], [5, 6, 9]) == 2
     assert lcp_len([1], [2]) == 0
     assert lcp_len([3, 3, 3], [3, 3, 3, 3, 3]) == 3
+
+
+def test_freeze_fork_worked_example():
+    """Freeze-tail fork (ForkServe README, adaptive unaligned tail), worked by hand."""
+    m = AllocatorModel(64, 64, P)
+    root = m.seq_create(40)                    # base [0, 1, 2] (page 2 holds 8 rows), res [0, 1, 2]
+    c1, jobs = m.fork(root, 40, freeze=True)   # aliases page 2 too; hole = slots 40..47
+    # rows 8..15 of page 2 hold no token yet: zeroed; the child's own residual page 5 likewise
+    assert jobs == [(2, 2, 8, JOB_BASE_ZERO), (5, 5, 8, JOB_RES_ZERO)]
+    assert m.seqs[c1].base == [0, 1, 2] and m.seqs[c1].res == [3, 4, 5]
+    assert m.slot_maps([c1]) == [(40, 8)] and m.page_tables([c1], 3)[2] == [48]
+    c2, jobs = m.fork(root, 40, freeze=True)
+    assert jobs == [(2, 2, 8, JOB_BASE_ZERO), (8, 8, 8, JOB_RES_ZERO)]
+    assert m.base_ref[2] == 3 and m.stats()["base_live"] == 3  # no tail copies
+    assert m.append(c1, 5) == [] and m.seqs[c1].base == [0, 1, 2, 3]  # own tokens start on a new page
+    # the parent keeps writing its frozen tail in place (the children read only rows 0..7)
+    assert m.append(root, 4) == [] and m.seqs[root].base == [0, 1, 2]
+    c3, jobs = m.fork(root, 44, freeze=True)   # rows 12..15 are still empty
+    assert jobs[0] == (2, 2, 12, JOB_BASE_ZERO) and m.slot_maps([c3]) == [(44, 4)]
+    assert m.append(root, 1) == [] and m.seqs[root].base == [0, 1, 2]
+    # a child that commits back into the shared page no longer has a hole and gets its own copy
+    assert m.commit(c2, 36) == [(2, 4, 4, JOB_BASE)]
+    assert m.slot_maps([c2]) == [(0, 0)] and m.page_tables([c2], 3)[2] == [36]
+    # a freeze fork of a child whose prefix spans its hole is a pack fork that inherits the hole
+    g, jobs = m.fork(c1, 42, freeze=True)
+    assert m.slot_maps([g]) == [(40, 8)] and jobs == [(3, jobs[0][1], 2, JOB_BASE)]
+    # freeing the parent hands the frozen page to nobody: a later append by a child copies nothing
+    m.free(root)                               # page 2 stays with c1, c3 and g
+    assert m.base_ref[2] == 3 and m.owner[JOB_BASE][2] == -1
+
+
+@pytest.mark.parametrize("L,k,ell", [(2050, 4, 48), (2047, 8, 100), (40, 3, 16), (4096, 4, 7)])
+def test_freeze_page_count_matches_formula(L, k, ell):
+    """pages_freeze = 1 + k ceil(l / P) pages beyond the trunk's full pages (ForkServe README)."""
+    m = AllocatorModel(100000, 100000, P)
+    root = m.seq_create(L)
+    for _ in range(k):
+        c, _ = m.fork(root, L, freeze=True)
+        m.append(c, ell)
+    full = L // P
+    if L % P:
+        assert m.stats()["base_live"] == full + acc.pages_freeze_children(L, k, ell, P)
+    else:
+        assert m.stats()["base_live"] == full + k * math.ceil(ell / P)
