@@ -300,53 +300,29 @@ __device__ __forceinline__ void copy_tiles(const uint8_t* pool, bool base, int32
   }
 }
 
-// Reduce eight values per lane over the 32 lanes of a warp (max or sum), transposed so
-// that nine shuffles suffice: lane l ends with the reduction of value l / 4.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce8(const float* v_in, int lane) {
-  float v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) v[i] = v_in[i];
-  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {  // lanes with bit 4 set keep values 4..7
-    const bool hi = lane & 16;
-    const float keep = hi ? v[i + 4] : v[i], give = hi ? v[i] : v[i + 4];
-    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, give, 16));
+// Wait for a phase completed by a tensor-core commit (the waiter orders its tensor-memory
+// accesses with tcgen05.fence::after_thread_sync, so no memory acquire is needed).
+__device__ __forceinline__ bool mbar_wait_tc(uint64_t* bar, uint32_t parity, uint32_t* status) {
+#pragma unroll 1
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
   }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {  // bit 3: values 2..3 of the four left
-    const bool hi = lane & 8;
-    const float keep = hi ? v[i + 2] : v[i], give = hi ? v[i] : v[i + 2];
-    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, give, 8));
-  }
-  {
-    const bool hi = lane & 4;
-    const float keep = hi ? v[1] : v[0], give = hi ? v[0] : v[1];
-    v[0] = op(keep, __shfl_xor_sync(0xffffffffu, give, 4));
-  }
-  v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 2));
-  v[0] = op(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
-  return v[0];
+  flag_status(status, kDevTimeout);
+  return false;
 }
 
-// Reduce four values per lane over a warp (max or sum), transposed: six shuffles, and lane l
-// ends with the reduction of value (l / 8) % 4.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce4(const float* v_in, int lane) {
-  auto op = [](float x, float y) { return kMax ? fmaxf(x, y) : x + y; };
-  float v[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {  // lanes with bit 4 set keep values 2..3
-    const bool hi = lane & 16;
-    const float keep = hi ? v_in[i + 2] : v_in[i], give = hi ? v_in[i] : v_in[i + 2];
-    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, give, 16));
-  }
-  const bool hi = lane & 8;
-  float r = op(hi ? v[1] : v[0], __shfl_xor_sync(0xffffffffu, hi ? v[0] : v[1], 8));
-  r = op(r, __shfl_xor_sync(0xffffffffu, r, 4));
-  r = op(r, __shfl_xor_sync(0xffffffffu, r, 2));
-  r = op(r, __shfl_xor_sync(0xffffffffu, r, 1));
+// Maximum over the 32 lanes of a warp.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
   return r;
 }
 
@@ -745,28 +721,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           if (!ok) break;
         }
         // U of this step, read out at once (as bf16 pairs) so that its buffer frees early
-        ok = mbar_wait(&bars[kUFull0 + (m & 1)], (m >> 1) & 1, a.status);
+        ok = mbar_wait_tc(&bars[kUFull0 + (m & 1)], (m >> 1) & 1, a.status);
         if (!ok) break;
         tc::fence_after();
         uint32_t ul[2][8], uh[2][8];  // [chunk][pair]: U columns (c + 2 i, c + 2 i + 1) and + 64
+        {
+          uint32_t lo[2][16], hi[2][16];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 32 * hf + 16 * cc;
-          uint32_t lo[16], hi[16];
-          tc::ld16(tl + kTmU + 128 * (m & 1) + c, lo);
-          tc::ld16(tl + kTmU + 128 * (m & 1) + 64 + c, hi);
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 32 * hf + 16 * cc;
+            tc::ld16(tl + kTmU + 128 * (m & 1) + c, lo[cc]);
+            tc::ld16(tl + kTmU + 128 * (m & 1) + 64 + c, hi[cc]);
+          }
           tc::wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            ul[cc][i] = pack_bf16(__uint_as_float(lo[2 * i]), __uint_as_float(lo[2 * i + 1]));
-            uh[cc][i] = pack_bf16(__uint_as_float(hi[2 * i]), __uint_as_float(hi[2 * i + 1]));
-          }
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              ul[cc][i] = pack_bf16(__uint_as_float(lo[cc][2 * i]), __uint_as_float(lo[cc][2 * i + 1]));
+              uh[cc][i] = pack_bf16(__uint_as_float(hi[cc][2 * i]), __uint_as_float(hi[cc][2 * i + 1]));
+            }
         }
         tc::fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kUFree0 + (m & 1)]);
         const int kr = m & 1;
-        if (m >= kKfRing && !mbar_wait(&bars[kKFFree0 + kr], ((m >> 1) - 1) & 1, a.status)) {
+        if (m >= kKfRing && !mbar_wait_tc(&bars[kKFFree0 + kr], ((m >> 1) - 1) & 1, a.status)) {
           ok = false;
           break;
         }
@@ -878,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     float* mref = s_mref + sw_ * (kMaxGroup * 8);  // this warp's copy (all four evolve identically)
     int32_t* lp = s_lp + sw_ * (kMaxGroup * 2);    // this warp's copy of each agent's (length, position)
     int32_t* lh = s_lh + sw_ * kMaxGroup;          // and of each agent's hole code
-    // query head whose warp-wide reductions this lane ends up holding, and the lanes that publish them
+    // query head whose reference maximum this lane publishes after a rescale, and the publishing lanes
     const int gl = kG == 8 ? lane >> 2 : lane >> 3;
     const bool publisher = kG == 8 ? (lane & 3) == 0 : (lane & 7) == 0;
     int gb = 0, gn = 0;
@@ -910,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const int32_t kp = (hn != 0 && j >= hs + hn) ? j - hn : j;
         const bool vis = j < L && !in_hole && kp <= pos && j < p1 * kPage;
         const int sr = m % kSRing;
-        ok = mbar_wait(&bars[kSFull0 + sr], (m / kSRing) & 1, a.status);
+        ok = mbar_wait_tc(&bars[kSFull0 + sr], (m / kSRing) & 1, a.status);
         if (!ok) break;
         tc::fence_after();
         uint32_t sv[kG];
@@ -923,11 +903,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         float sc[kG];
 #pragma unroll
         for (int q = 0; q < kG; ++q) sc[q] = (vis && q < G) ? __uint_as_float(sv[q]) * a.scale_log2 : -INFINITY;
-        float wmax;  // max over the warp's keys of query head gl
-        if constexpr (kG == 8) wmax = warp_reduce8<true>(sc, lane);
-        else wmax = warp_reduce4<true>(sc, lane);
         float* red = s_red + (m & 1) * 32;
-        if (publisher) red[sw_ * kG + gl] = wmax;
+#pragma unroll
+        for (int q = 0; q < kG; ++q) {  // max over the warp's keys of each query head
+          const float wq = warp_max(sc[q]);
+          if (lane == q) red[sw_ * kG + q] = wq;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kRed0 + (m & 1)]);
         // while the other warps' maxima come in: probabilities against the current reference
