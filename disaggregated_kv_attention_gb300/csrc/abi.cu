@@ -329,6 +329,13 @@ int32_t forkkv_step_graph_destroy(forkkv_step_graph* graph) {
   return cuda_status(e);
 }
 
+int32_t forkkv_wait_selftest(uint32_t polls, void* stream) {
+  if (polls < 1 || polls > (1u << 20)) return FORKKV_ERR_INVALID_ARG;
+  uint32_t* st = fkv::device_status_ptr();
+  if (!st) return FORKKV_ERR_CUDA;
+  return cuda_status(fkv::launch_wait_selftest(polls, st, as_stream(stream)));
+}
+
 int32_t forkkv_get_device_status(uint32_t* status, void* stream) {
   if (!status) return FORKKV_ERR_INVALID_ARG;
   uint32_t* st = fkv::device_status_ptr();

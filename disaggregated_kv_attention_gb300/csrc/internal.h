@@ -22,6 +22,7 @@ cudaError_t launch_write_rows(const forkkv_pool_desc& pools, int32_t layer, int3
                               const void* vr, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_cow_copy(const forkkv_pool_desc& pools, const CowJobBatch& batch, cudaStream_t stream);
 cudaError_t launch_rope_table(const uint32_t* turns_hi_lo, int32_t n_positions, void* table, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint32_t polls, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_residual_fill(const forkkv_pool_desc& pools, int32_t layer, const void* x, int32_t n_tok,
                                  int32_t hidden, const void* A, int32_t n_ag, const int32_t* slot_res,
                                  uint32_t* status, cudaStream_t stream);

@@ -110,9 +110,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Bounded wait: gives up after `limit` polls (each poll may suspend the thread
 // for a hardware-chosen time), records kDevTimeout and returns false.
 constexpr uint32_t kWaitLimit = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint32_t limit = kWaitLimit) {
 #pragma unroll 1
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   flag_status(status, kDevTimeout);
   return false;

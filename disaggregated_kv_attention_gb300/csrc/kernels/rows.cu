@@ -162,6 +162,18 @@ __global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__
   *reinterpret_cast<uint2*>(a.table + (int64_t)p * kRopeRow + rope_off(p, m)) = v;
 }
 
+// Self-test of the bounded waits: one thread waits on a shared-memory mbarrier that nothing
+// arrives on, through the same helper every pipeline wait uses, with a poll limit of `polls`.
+// The helper gives up, records kDevTimeout and the kernel returns normally.
+__global__ void wait_selftest_kernel(uint32_t polls, uint32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    mbar_wait(&bar, 0, status, polls);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_write_rows(const forkkv_pool_desc& pools, int32_t layer, int32_t n_rows, const int32_t* slot_base,
@@ -215,6 +227,11 @@ cudaError_t launch_rope_table(const uint32_t* turns_hi_lo, int32_t n_positions, 
   a.table = static_cast<uint8_t*>(table);
   const int64_t work = (int64_t)n_positions * 32;
   rope_table_kernel<<<(unsigned)((work + 255) / 256), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(uint32_t polls, uint32_t* status, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(polls, status);
   return cudaGetLastError();
 }
 

@@ -116,6 +116,7 @@ _SIGNATURES = {
     "forkkv_prefill_workspace_size": ([_P(forkkv_attn_params), _P(ctypes.c_size_t)], _i32),
     "forkkv_residual_attn_prefill_chunk": ([_P(forkkv_attn_params), _vp], _i32),
     "forkkv_get_device_status": ([_P(_u32), _vp], _i32),
+    "forkkv_wait_selftest": ([_u32, _vp], _i32),
     "forkkv_residual_attn_decode_static": ([_P(forkkv_attn_params), _vp], _i32),
 }
 
@@ -447,6 +448,10 @@ def forkkv_residual_attn_decode_static(p: forkkv_attn_params, stream=None) -> No
     memory (the workspace fields of ``p`` are ignored; see include/forkkv.h)."""
     _check(lib().forkkv_residual_attn_decode_static(ctypes.byref(p), _stream(stream)),
            "residual_attn_decode_static")
+
+
+def forkkv_wait_selftest(polls: int, stream=None) -> None:
+    _check(lib().forkkv_wait_selftest(int(polls), _stream(stream)), "wait_selftest")
 
 
 def forkkv_get_device_status(stream=None) -> int:

@@ -453,6 +453,20 @@ int32_t forkkv_step_graph_create(const forkkv_attn_params* params, const forkkv_
 int32_t forkkv_step_graph_launch(forkkv_step_graph* graph, void* stream);
 int32_t forkkv_step_graph_destroy(forkkv_step_graph* graph);
 
+/* Self-test of the bounded device waits.  The pages have no counterpart: this
+ * serves the failure handling of the library itself.  Every wait inside the
+ * kernels (on an mbarrier that a copy, a tensor-core commit or another warp
+ * completes) polls a bounded number of times; if the event never comes it gives
+ * up, sets FORKKV_DEV_TIMEOUT in the device status word and the kernel winds
+ * down instead of hanging the GPU.  This call launches one tiny kernel whose
+ * thread waits, through the same wait routine, on an mbarrier that nothing ever
+ * completes, giving up after `polls` polls (1 .. 1048576; each poll may suspend
+ * the thread for a hardware-chosen time of the order of a microsecond).  The
+ * kernel returns normally, so the context stays usable; a following
+ * forkkv_get_device_status() reports FORKKV_DEV_TIMEOUT.  `polls` out of range:
+ * FORKKV_ERR_INVALID_ARG, nothing launched.  Allocates nothing. */
+int32_t forkkv_wait_selftest(uint32_t polls, void* stream);
+
 /* Read and clear the device status word of the current device (OR of
  * FORKKV_DEV_* bits set by kernels since the last read).  Synchronises
  * `stream`. */

@@ -239,6 +239,10 @@ def test_invalid_arguments_rejected():
         fk.forkkv_alloc_create(8, 8, 32)
     assert e.value.code == -5
     fk.forkkv_alloc_destroy(a)
+    for polls in (0, (1 << 20) + 1):  # rejected before any CUDA call: nothing is launched
+        with pytest.raises(fk.ForkKVError) as e:
+            fk.forkkv_wait_selftest(polls, stream=0)
+        assert e.value.code == -1
 
 
 def _tree_tables(rnd, n_agents_per, depth_tokens):
