@@ -6,11 +6,13 @@
 // accumulators rescaled together), laid out for a dense contraction:
 //   grid   (tile of 128 (token, query-head) rows, agent, KV head)
 //   warps  0      producer: 128-key blocks (8 pages) of K and k_res tiles into a
-//                 2-stage ring, V and v_res tiles into a 3-stage ring, with 1-D bulk
-//                 async copies of at most one page tile each (several small copies
-//                 land sooner than one large one); each K tile goes in as its two
+//                 2-stage ring, V and v_res tiles into a 3-stage ring.  V and v_res
+//                 go in as 1-D bulk async copies of one page tile each (several small
+//                 copies land sooner than one large one).  K goes in as its two
 //                 64-column halves, so that a stage holds the block's 128 keys as one
-//                 K-major operand
+//                 K-major operand: when the block's 8 base pages are consecutive, one
+//                 4-D tensor copy per half (8 pages of 16 rows), else one bulk copy per
+//                 page half
 //          1      allocates 512 TMEM columns; one lane issues every MMA
 //          2..9   RoPE group, two warps per key (half of the rotation pairs each):
 //                 U = Kr . B_k^T arrives in TMEM; K = bf16(Kb + RoPE_j(U)) replaces
@@ -30,7 +32,11 @@
 //   epilogue: out = (O + O_r . B_v[:, hD:(h+1)D]) / l, B_v applied once per row.
 // Every wait is on an mbarrier with a bounded spin; a timeout sets the device
 // status word instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "../internal.h"
 #include "common.cuh"
@@ -109,7 +115,21 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+// Box {128 B, 16 rows, 1 half, 8 pages} of the base K pool at (half, page) into shared memory.
+__device__ __forceinline__ void tma_load_kb(void* dst, const CUtensorMap* map, int32_t half, int32_t page,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(half), "r"(page), "r"(smem_u32(bar))
+      : "memory");
+}
+
 struct PrefillArgs {
+  // This layer's base K pool as [Hkv * pages][2 halves][16 rows][128 B]: a box of 8 pages of one
+  // half lands in shared memory as the rows of 128 keys of one 64-column block.
+  CUtensorMap kb_map;
+  int32_t kb_map_ok;
   const uint8_t* k_base;
   const uint8_t* v_base;
   const uint8_t* k_res;
@@ -275,7 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const int32_t pid = __shfl_sync(0xffffffffu, id, (lane >> 1) & 7);
       if (lane == 0) mbar_arrive_expect_tx(&bars[kKFull0 + stage], nvp * (kBaseTile + kResTile));
       __syncwarp();
-      if (lane < 2 * nvp) {
+      // eight consecutive base pages: one tensor copy per 64-column half instead of 16 page halves
+      const int32_t pid0 = __shfl_sync(0xffffffffu, id, 0);
+      const bool run = a.kb_map_ok && nvp == kBlockPages &&
+                       __all_sync(0xffffffffu, lane >= 16 || pid == pid0 + ((lane >> 1) & 7));
+      if (run) {
+        if (lane < 2) tma_load_kb(st + lane * 16384, &a.kb_map, lane, (int32_t)(head_base + pid0), &bars[kKFull0 + stage]);
+      } else if (lane < 2 * nvp) {
         const int hh = lane & 1;
         bulk_g2s(st + hh * 16384 + (lane >> 1) * 2048, a.k_base + (head_base + pid) * kBaseTile + hh * 2048,
                  kBaseTile / 2, &bars[kKFull0 + stage]);
@@ -726,6 +752,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
 }  // namespace
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (nullptr if unavailable).
+static PFN_cuTensorMapEncodeTiled_v12000 kb_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
 cudaError_t launch_prefill(const forkkv_attn_params& p, const void* rope_table, uint32_t* status,
                            cudaStream_t stream) {
   static thread_local int configured_device = -1;
@@ -769,6 +809,18 @@ cudaError_t launch_prefill(const forkkv_attn_params& p, const void* rope_table, 
   const float scale = p.sm_scale > 0.f ? p.sm_scale : 1.0f / sqrtf((float)kHeadDim);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
+  a.kb_map_ok = 0;
+  const int64_t kb_pages = (int64_t)p.pools.num_kv_heads * p.pools.num_base_pages;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = kb_map_encoder();
+  if (enc && kb_pages < (1ll << 31)) {
+    const cuuint64_t dims[4] = {128, 16, 2, (cuuint64_t)kb_pages};
+    const cuuint64_t strides[3] = {128, 2048, kBaseTile};
+    const cuuint32_t box[4] = {128, 16, 1, kBlockPages};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    a.kb_map_ok = enc(&a.kb_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(a.k_base), dims, strides, box,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const int64_t rows = (int64_t)p.q_len * G;
   dim3 grid((unsigned)((rows + kRows - 1) / kRows), p.n_agents, p.num_kv_heads);
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(a);
