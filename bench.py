@@ -52,6 +52,25 @@ def _peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x over all ranks of the initialised process group (x itself on one
+    rank): the job's time is that of its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, agents: int, layers: int, seconds_per_step: float) -> float:
+    """Whole-job throughput of `world` independent replicas (weak scaling): every replica
+    attends `agents` x `layers` (agent, layer) tokens per step, and a step of the job lasts as
+    long as its slowest replica's (seconds_per_step, already the maximum over ranks)."""
+    return world * agents * layers / seconds_per_step
+
+
 def _traffic(kernel: str):
     """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
     try:
@@ -424,15 +443,11 @@ def main() -> int:
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = e_start.elapsed_time(e_end)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
     dec_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     call_us = 1000 * statistics.mean(dec_ms) / layers
     ms_step = total_ms / args.steps
-    value = world * A * layers / (ms_step / 1000)
+    value = job_tokens_per_s(world, A, layers, ms_step / 1000)
 
     # the same step through the public one-graph API (forkkv_step_graph_*: every layer's row
     # write and decode in one CUDA graph), device-timed over the same number of steps
@@ -476,12 +491,8 @@ def main() -> int:
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e_value = world * A * layers / e2e_s
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev)
+    e2e_value = job_tokens_per_s(world, A, layers, e2e_s)
 
     torch.cuda.synchronize()
     fk.forkkv_step_graph_destroy(sg)
