@@ -52,6 +52,16 @@ def _peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+def percentiles(xs, qs=(10, 50, 90)):
+    """Nearest-rank percentiles of a list of timings ({"p10": ..., "p50": ..., "p90": ...})."""
+    v = sorted(xs)
+    out = {}
+    for q in qs:
+        k = max(0, min(len(v) - 1, math.ceil(q / 100 * len(v)) - 1))
+        out[f"p{q}"] = v[k]
+    return out
+
+
 def max_over_ranks(x: float, device=None) -> float:
     """The largest value of x over all ranks of the initialised process group (x itself on one
     rank): the job's time is that of its slowest replica."""
@@ -446,6 +456,7 @@ def main() -> int:
     total_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
     dec_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     call_us = 1000 * statistics.mean(dec_ms) / layers
+    call_pct = {k: 1000 * v / layers for k, v in percentiles(dec_ms).items()}
     ms_step = total_ms / args.steps
     value = job_tokens_per_s(world, A, layers, ms_step / 1000)
 
@@ -512,6 +523,7 @@ def main() -> int:
                      "kernel": "forkkv_residual_attn_decode (split-KV kernel + combine kernel), per layer call",
                      "alg_bytes_per_launch": fig["bytes"], "launch_us": call_us},
         "decode_call_us": call_us,
+        "decode_call_us_percentiles": call_pct,
         "model_step_tokens_per_s": world * A / (ms_step / 1000),
         "step_graph": {"ms_per_step": sg_ms, "tokens_per_s": world * A * layers / (sg_ms / 1000),
                        "model_step_tokens_per_s": world * A / (sg_ms / 1000),

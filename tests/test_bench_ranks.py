@@ -88,3 +88,9 @@ def test_reference_arm_prints_from_rank_zero_only():
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_percentiles_are_nearest_rank():
+    xs = [5.0, 1.0, 4.0, 2.0, 3.0, 9.0, 8.0, 7.0, 6.0, 10.0]
+    assert bench.percentiles(xs) == {"p10": 1.0, "p50": 5.0, "p90": 9.0}
+    assert bench.percentiles([2.5]) == {"p10": 2.5, "p50": 2.5, "p90": 2.5}
