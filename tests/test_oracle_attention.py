@@ -87,6 +87,37 @@ def test_rotate_half_pairing_d4():
     assert np.allclose(out, [[1.0, 3.0, 0.0, 0.0]], atol=1e-14, rtol=0)
 
 
+@pytest.mark.parametrize("i", [0, 1, 2, 3])
+def test_rope_frequency_of_every_pair_index_d8(i):
+    # D=8, theta=1e4: the angular frequency of pair index i is 1e4^(-2i/8) = 10^-i exactly, so a
+    # key at position 10^i is turned by exactly 1 rad on pair (i, i+4) and by 10^(i-k) rad on the
+    # others.  A unit vector on component i+4 must come out as -sin 1 on i and cos 1 on i+4
+    # (written out by hand: (a, b) -> (a cos - b sin, b cos + a sin) with a=0, b=1).  A wrong
+    # exponent (theta^(-i/D), a D-2 denominator, 0-based vs 1-based pair index) moves the angle.
+    x = np.zeros((1, 8))
+    x[0, i + 4] = 1.0
+    got = ra.rope_rotate_half(x, np.array([10 ** i]), 1e4)[0]
+    want = np.zeros(8)
+    want[i], want[i + 4] = -math.sin(1.0), math.cos(1.0)
+    assert np.allclose(got, want, atol=1e-12, rtol=0)
+
+
+def test_rope_second_frequency_through_attention_d4():
+    # D=4, theta=1e4: pair index 1 has frequency 1e4^(-2/4) = 0.01 exactly.  Keys sit at
+    # positions 0 and 100 (key_positions), the query at 100.  Key 1: U = 1*[0,0,0,1]; pair (1,3)
+    # turned by 100*0.01 = 1 rad -> K_lora = [0, -sin1, 0, cos1].  With q = [0,-2,0,0], scale 1/2
+    # and Kb1 = [0, sin1 - ln3, 0, 0]: s1 = -(sin1 - ln3 - sin1) = ln 3; key 0 scores 0.
+    # Weights (1/4, 3/4), V0 = [4,0,0,0], V1 = [0,4,0,0] -> O = [1, 3, 0, 0].
+    ln3, s1 = math.log(3.0), math.sin(1.0)
+    q = np.array([[[0.0, -2.0, 0.0, 0.0]]])
+    kb = np.array([[[0.0, 0, 0, 0]], [[0.0, s1 - ln3, 0, 0]]])
+    vb = np.array([[[4.0, 0, 0, 0]], [[0.0, 4, 0, 0]]])
+    out = ra.residual_attention(q, np.array([100]), kb, vb, np.array([[0.0], [1.0]]), np.zeros((2, 1)),
+                                np.array([[0.0, 0, 0, 1]]), np.zeros((1, 4)), 1e4,
+                                key_positions=np.array([0, 100]))
+    assert np.allclose(out[:, 0, :], [[1.0, 3.0, 0.0, 0.0]], atol=1e-14, rtol=0)
+
+
 def test_hand_cases_through_online_restatement():
     kb, vb, kr, vr, Bk, Bv = _case_b()
     for block in (1, 2):
