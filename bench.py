@@ -1,22 +1,28 @@
 #!/usr/bin/env python3
 """ResidualAttention decode throughput on GB300 (tokens/s and achieved HBM GB/s).
 
-Workload: the Llama-3-8B-shaped decode fan-out (32 q / 8 kv heads, head_dim
-128, rank 16; 8 agents forked from an 8192-token prefix whose base pages are
-aliased with refcount 8, each with U[256,1024] private tokens; 1 query per
-agent), seeded and synthetic, with one set of paged pools per model layer (32
-layers, 1.9 GB) so that consecutive calls never find their inputs in L2.
+Headline workload: the Llama-3-70B-shaped two-level fork tree (64 q / 8 kv
+heads, head_dim 128, rank 16; 64 agents under a 131072-token root, 4 trunks of
+8192 tokens, 16 agents per trunk with U[1,4096] private tokens; 1 query per
+agent), the largest decode workload, seeded and synthetic.  Each pool set
+(layer) holds 1.8 GB, so two sets already keep every call's inputs out of the
+129 MB L2.
 
-One step = one decode step of all 32 layers: per layer, the new token's rows
-are scattered into the pools (forkkv_write_rows) and ResidualAttention decode
-runs (forkkv_residual_attn_decode: split-KV kernel + combine kernel).  The
-writes of a step and the decodes of a step are each captured in a CUDA graph;
-the timed region replays them K times, with CUDA events around each step's
-decodes (the roofline's launch time).  tokens/s counts one (agent, layer)
-attention as one token, i.e. A * layers / step time.  The same step through
-the library's one-graph call (forkkv_step_graph_launch, every layer's write
-and decode in one CUDA graph) is timed too ("step_graph"), and the e2e figure
-runs through it with host copies in and out.
+One step = one decode step over every timed layer: per layer, the new token's
+rows are scattered into the pools (forkkv_write_rows) and ResidualAttention
+decode runs (forkkv_residual_attn_decode: split-KV kernel + combine kernel).
+The writes of a step and the decodes of a step are each captured in a CUDA
+graph; the timed region replays them K times, with CUDA events around each
+step's decodes (the roofline's launch time).  tokens/s counts one (agent,
+layer) attention as one token, i.e. A * layers / step time.  The same step
+through the library's one-graph call (forkkv_step_graph_launch, every layer's
+write and decode in one CUDA graph) is timed too ("step_graph"), and the e2e
+figure runs through it with host copies in and out.
+
+The same line carries "per_config" (the Llama-3-8B-shaped and Qwen2.5-7B-shaped
+decode fan-outs, each with its own roofline) and "prefill" (the Qwen2.5-14B-
+shaped chunked prefill against the dense bf16 tensor peak), timed in the same
+run.  --config picks another headline workload; --fill times the residual fill.
 
 --impl reference times the fp64 CPU oracle instead (the only reference this
 method has), on bounded samples of the same workload.
@@ -40,6 +46,8 @@ sys.path.insert(0, ROOT)
 METRIC = "ResidualAttention decode tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# kernels launched per layer and step: the row write, the split-KV kernel, the combine kernel
+GPU_LAUNCHES_PER_LAYER = 3
 
 
 def _peaks():
@@ -81,11 +89,12 @@ def job_tokens_per_s(world: int, agents: int, layers: int, seconds_per_step: flo
     return world * agents * layers / seconds_per_step
 
 
-def _traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+def _traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from a committed ncu capture (scaled to a full
+    launch where the capture was of a smaller case), if the kernel source is unchanged since."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            d = json.load(f)[kernel]
+            d = json.load(f)[kernel][workload]
         src = os.path.join(ROOT, d["source"])
         with open(src, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()
@@ -195,8 +204,9 @@ def prefill_flops(w) -> int:
     return total
 
 
-def bench_prefill(args, cfg) -> int:
-    """Prefill-chunk throughput (TFLOP/s against the dense bf16 tensor peak), one layer per call."""
+def bench_prefill(args, cfg) -> dict:
+    """Prefill-chunk throughput (TFLOP/s against the dense bf16 tensor peak), one layer per call;
+    returns the JSON line as a dict."""
     import torch
     from disaggregated_kv_attention_gb300 import build as _build
     from disaggregated_kv_attention_gb300 import forkkv as fk
@@ -215,32 +225,36 @@ def bench_prefill(args, cfg) -> int:
         raise RuntimeError("device status set by the prefill kernel")
     for _ in range(args.warmup):
         fk.forkkv_residual_attn_prefill_chunk(p)
+    stream = torch.cuda.current_stream()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
     torch.cuda.synchronize()
     clocks = ClockSampler(0)
     time.sleep(0.3)
     for k in range(args.steps):
-        ev[2 * k].record()
+        ev[2 * k].record(stream)
         fk.forkkv_residual_attn_prefill_chunk(p)
-        ev[2 * k + 1].record()
+        ev[2 * k + 1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    if fk.forkkv_get_device_status():
+        raise RuntimeError("device status set by the prefill kernel")
     ms = [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(args.steps)]
     t = statistics.median(ms) / 1000
     flops = prefill_flops(w)
     hbm, tf, tf_sus, src = _peaks()
     achieved = flops / t / 1e12
     tokens = cfg.n_agents * cfg.q_len
-    print(json.dumps({
+    return {
         "metric": "ResidualAttention prefill-chunk TFLOP/s (% of dense bf16 tensor peak), 1 GPU",
         "value": achieved, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000 * t, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": {"workload": f"{cfg.name}: {cfg.description}", "layers": 1},
+        "data": "synthetic", "config": {"workload": f"{cfg.name}: {cfg.description}", "layers": 1,
+                                        "l2": "inputs larger than L2 (q and out alone are 336 MB)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf, "unit": "TFLOP/s", "frac": achieved / tf,
-                     "traffic": _traffic("prefill_kernel"), "peak_source": f"{src} bf16_tflops burst (of {src})",
-                     "alg_flops_per_launch": flops},
-        "tokens_per_s": tokens / t, "gpu_launches": args.steps, "clocks": clk}))
-    return 0
+                     "traffic": _traffic("prefill_kernel", cfg.name),
+                     "peak_source": f"{src} bf16_tflops burst (of {src})",
+                     "alg_flops_per_launch": flops, "launch_ms_median": 1000 * t},
+        "tokens_per_s": tokens / t, "gpu_launches": args.steps, "clocks": clk}
 
 
 def bench_fill(args, cfg) -> int:
@@ -296,7 +310,7 @@ def bench_fill(args, cfg) -> int:
                                f"rank 16 (k and v), x cycled over {reps} copies (inputs > L2)"},
         "roofline": {"bound": "hbm" if hbm_bound else "tensor", "achieved": gbs if hbm_bound else tfs,
                      "peak": hbm if hbm_bound else tf, "unit": "GB/s" if hbm_bound else "TFLOP/s",
-                     "frac": (gbs / hbm) if hbm_bound else (tfs / tf), "traffic": _traffic("residual_fill_kernel"),
+                     "frac": (gbs / hbm) if hbm_bound else (tfs / tf), "traffic": _traffic("residual_fill_kernel", cfg.name),
                      "peak_source": f"{src} ({'hbm_gbs' if hbm_bound else 'bf16_tflops burst'})",
                      "alg_bytes_per_launch": alg_bytes, "alg_flops_per_launch": flops},
         "achieved_tflops": tfs, "tensor_frac": tfs / tf, "hbm_frac": gbs / hbm,
@@ -304,76 +318,30 @@ def bench_fill(args, cfg) -> int:
     return 0
 
 
-def main() -> int:
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", default="forkkv", choices=["forkkv", "reference"])
-    ap.add_argument("--config", default="llama3_8b_decode")
-    ap.add_argument("--layers", type=int, default=0, help="pool sets (0 = the model's layer count)")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fill", action="store_true", help="time the residual fill of the configuration's fan-out")
-    args = ap.parse_args()
-    args.warmup = max(3, args.warmup)
+# decode workloads reported beside the headline, and the prefill-chunk workload
+PER_CONFIG = ("llama3_8b_decode", "qwen25_7b_mapreduce_decode")
+PREFILL_CONFIG = "qwen25_14b_prefill"
+L2_BYTES = 129e6
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
 
-    from disaggregated_kv_attention_gb300 import workload as wl
-    cfg = wl.CONFIGS[args.config]
-    if args.fill:
-        return bench_fill(args, cfg)
-    if cfg.q_len != 1:
-        return bench_prefill(args, cfg)
-    layers = args.layers or cfg.model_layers
-    w = wl.generate(cfg)
-    fig = workload_figures(w, layers)
-    config = {"workload": f"{cfg.name}: {cfg.description}", "layers": layers, "agents": cfg.n_agents,
-              "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim, "rank": cfg.rank,
-              "page": cfg.page_size, "seq_lens": [int(x) for x in w.seq_lens], "seed": cfg.seed,
-              "l2": "inputs larger than L2: one pool set per layer, %.2f GB in total" % (
-                  layers * fig["bytes"] / 1e9)}
+def pool_sets(cfg, fig, requested: int) -> int:
+    """Pool sets (layers) timed: `requested`, else enough that the sets together hold at least four
+    times the L2 (so a call never finds its inputs there), at least two, at most the model's layers."""
+    if requested:
+        return requested
+    return int(min(cfg.model_layers, max(2, math.ceil(4 * L2_BYTES / fig["bytes"]))))
 
-    if args.impl == "reference":
-        if rank != 0:
-            return 0
-        samples = []
-        for k in range(args.warmup + args.steps):
-            t0 = time.perf_counter()
-            frac = run_oracle_sample(w, k % cfg.n_agents, (k // cfg.n_agents) % cfg.n_kv_heads)
-            dt = time.perf_counter() - t0
-            if k >= args.warmup:
-                samples.append((frac, dt))
-        tok = sum(f for f, _ in samples)
-        sec = sum(d for _, d in samples)
-        value = tok / sec
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sec / len(samples),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": config,
-                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
-                                 "kind": "oracle",
-                                 "sample": f"each step: one (agent, KV head) unit of one layer call "
-                                           f"({cfg.group} query heads, fp64 NumPy), rotating over agents and heads"},
-                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
-        return 0
 
+def decode_run(cfg, w, layers, steps, warmup, dev, world, full):
+    """Time `steps` decode steps over `layers` pool sets of workload w (one step = every layer's row write
+    and decode, each captured in a CUDA graph); with `full`, also the one-graph step API and the e2e leg."""
     import torch
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    from disaggregated_kv_attention_gb300 import build as _build
-    _build.build()
     from disaggregated_kv_attention_gb300 import forkkv as fk
     from disaggregated_kv_attention_gb300 import paged
 
-    dev = torch.device("cuda", local)
+    fig = workload_figures(w, layers)
     P = paged.place(w, device=dev, n_layers=layers)
-    A, Hq, Hkv = cfg.n_agents, cfg.n_q_heads, cfg.n_kv_heads
+    A, Hkv = cfg.n_agents, cfg.n_kv_heads
     lens = [int(x) for x in w.seq_lens]
     rope = fk.rope_table(cfg.rope_theta, P.max_seq_len, device=dev)
     plan, info = fk.forkkv_plan_build(P.bpt_np, w.seq_lens.numpy(), Hkv)
@@ -431,19 +399,19 @@ def main() -> int:
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         g_w.replay()
         g_d.replay()
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(dev.index)
     time.sleep(0.3)
     e_start.record(stream)
-    for k in range(args.steps):
+    for k in range(steps):
         g_w.replay()
         ev0[k].record(stream)
         g_d.replay()
@@ -457,22 +425,39 @@ def main() -> int:
     dec_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     call_us = 1000 * statistics.mean(dec_ms) / layers
     call_pct = {k: 1000 * v / layers for k, v in percentiles(dec_ms).items()}
-    ms_step = total_ms / args.steps
-    value = job_tokens_per_s(world, A, layers, ms_step / 1000)
+    ms_step = total_ms / steps
+    hbm, tf, tf_sus, src = _peaks()
+    achieved = fig["bytes"] / (call_us * 1e-6) / 1e9
+    res = {
+        "fig": fig, "layers": layers, "ms_per_step": ms_step, "call_us": call_us, "call_pct": call_pct,
+        "value": job_tokens_per_s(world, A, layers, ms_step / 1000), "clocks": clk,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": _traffic("decode_split_kernel", cfg.name),
+                     "peak_source": f"{src} hbm_gbs (of {src})",
+                     "kernel": "forkkv_residual_attn_decode (split-KV kernel + combine kernel), per layer call",
+                     "alg_bytes_per_launch": fig["bytes"], "launch_us": call_us},
+        "achieved_tflops": fig["flops"] / (call_us * 1e-6) / 1e12,
+        "tensor_frac": fig["flops"] / (call_us * 1e-6) / 1e12 / tf,
+    }
+    if not full:
+        st = fk.forkkv_get_device_status()
+        if st:
+            raise RuntimeError(f"device status {st} after the timed region")
+        return res
 
     # the same step through the public one-graph API (forkkv_step_graph_*: every layer's row
     # write and decode in one CUDA graph), device-timed over the same number of steps
     rows = [(slot_b, slot_r, kb_new[l], vb_new[l], kr_new[l], vr_new[l]) for l in range(layers)]
     sg = fk.forkkv_step_graph_create(params, rows)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         fk.forkkv_step_graph_launch(sg, stream)
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     g0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         fk.forkkv_step_graph_launch(sg, stream)
     g1.record(stream)
     torch.cuda.synchronize()
-    sg_ms = g0.elapsed_time(g1) / args.steps
+    sg_ms = g0.elapsed_time(g1) / steps
 
     # end to end through the public API: pinned host inputs in, the one-graph step, result out,
     # every step
@@ -486,7 +471,7 @@ def main() -> int:
            (P.rpt, rpt_h), (P.seq_lens, lens_h), (P.positions, pos_h)]
     h2d_bytes = sum(h.numel() * h.element_size() for _, h in h2d)
     d2h_bytes = out_h.numel() * out_h.element_size()
-    e2e_steps = max(10, args.steps // 4)
+    e2e_steps = max(10, steps // 4)
 
     def e2e_step():
         for d, h in h2d:
@@ -503,38 +488,142 @@ def main() -> int:
     for _ in range(e2e_steps):
         e2e_step()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev)
-    e2e_value = job_tokens_per_s(world, A, layers, e2e_s)
-
     torch.cuda.synchronize()
     fk.forkkv_step_graph_destroy(sg)
     st = fk.forkkv_get_device_status()
     if st:
         raise RuntimeError(f"device status {st} after the timed region")
+    res["step_graph"] = {"ms_per_step": sg_ms, "tokens_per_s": world * A * layers / (sg_ms / 1000),
+                         "api": "forkkv_step_graph_launch: one CUDA graph per step (every timed layer)"}
+    res["e2e"] = {"value": job_tokens_per_s(world, A, layers, e2e_s), "unit": "tokens/s",
+                  "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps,
+                  "api": "forkkv_step_graph_launch"}
+    return res
 
-    hbm, tf, tf_sus, src = _peaks()
-    achieved = fig["bytes"] / (call_us * 1e-6) / 1e9
-    traffic = _traffic("decode_split_kernel")
+
+def decode_config(cfg, w, layers):
+    return {"workload": f"{cfg.name}: {cfg.description}", "layers": layers, "model_layers": cfg.model_layers,
+            "agents": cfg.n_agents, "q_heads": cfg.n_q_heads, "kv_heads": cfg.n_kv_heads,
+            "head_dim": cfg.head_dim, "rank": cfg.rank, "page": cfg.page_size,
+            "seq_lens": [int(x) for x in w.seq_lens], "seed": cfg.seed}
+
+
+def _free_device():
+    import gc
+    import torch
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="forkkv", choices=["forkkv", "reference"])
+    ap.add_argument("--config", default="llama3_70b_stress_decode")
+    ap.add_argument("--layers", type=int, default=0, help="pool sets timed (0: enough to hold 4x the L2)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="headline only: no per_config / prefill lines")
+    ap.add_argument("--fill", action="store_true", help="time the residual fill of the configuration's fan-out")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from disaggregated_kv_attention_gb300 import workload as wl
+    cfg = wl.CONFIGS[args.config]
+    if args.fill:
+        return bench_fill(args, cfg)
+    if cfg.q_len != 1:
+        print(json.dumps(bench_prefill(args, cfg)))
+        return 0
+    w = wl.generate(cfg)
+    layers = pool_sets(cfg, workload_figures(w, 1), args.layers)
+    fig = workload_figures(w, layers)
+    config = decode_config(cfg, w, layers)
+    config["l2"] = "inputs larger than L2: %d pool sets (layers), %.2f GB in total" % (
+        layers, layers * fig["bytes"] / 1e9)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        samples = []
+        for k in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            frac = run_oracle_sample(w, k % cfg.n_agents, (k // cfg.n_agents) % cfg.n_kv_heads)
+            dt = time.perf_counter() - t0
+            if k >= args.warmup:
+                samples.append((frac, dt))
+            if k >= args.warmup and sum(d for _, d in samples) > 120:
+                break  # bounded: the whole run stays within a few minutes
+        tok = sum(f for f, _ in samples)
+        sec = sum(d for _, d in samples)
+        value = tok / sec
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+                "steps": len(samples), "warmup": args.warmup, "ms_per_step": 1000 * sec / len(samples),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                                 "kind": "oracle",
+                                 "sample": f"each step: one (agent, KV head) unit of one layer call "
+                                           f"({cfg.group} query heads, fp64 NumPy), rotating over agents and "
+                                           f"heads; {len(samples)} steps timed (capped at 120 s of CPU work)"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from disaggregated_kv_attention_gb300 import build as _build
+    _build.build()
+    dev = torch.device("cuda", local)
+
+    r = decode_run(cfg, w, layers, args.steps, args.warmup, dev, world, full=True)
+    A = cfg.n_agents
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": traffic, "peak_source": f"{src} hbm_gbs (of {src})",
-                     "kernel": "forkkv_residual_attn_decode (split-KV kernel + combine kernel), per layer call",
-                     "alg_bytes_per_launch": fig["bytes"], "launch_us": call_us},
-        "decode_call_us": call_us,
-        "decode_call_us_percentiles": call_pct,
-        "model_step_tokens_per_s": world * A / (ms_step / 1000),
-        "step_graph": {"ms_per_step": sg_ms, "tokens_per_s": world * A * layers / (sg_ms / 1000),
-                       "model_step_tokens_per_s": world * A / (sg_ms / 1000),
-                       "api": "forkkv_step_graph_launch: one CUDA graph per model step (all layers)"},
-        "achieved_tflops": fig["flops"] / (call_us * 1e-6) / 1e12,
+        "roofline": r["roofline"],
+        "decode_call_us": r["call_us"],
+        "decode_call_us_percentiles": r["call_pct"],
+        "model_step_tokens_per_s": world * A / (cfg.model_layers * r["call_us"] * 1e-6),
+        "model_step_note": f"agents / ({cfg.model_layers} layers x the mean layer-call time)",
+        "step_graph": r["step_graph"],
+        "achieved_tflops": r["achieved_tflops"], "tensor_frac": r["tensor_frac"],
         "alg_flops_per_call": fig["flops"],
-        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d_bytes,
-                "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps, "api": "forkkv_step_graph_launch"},
-        "gpu_launches": args.steps * layers * 3,
-        "clocks": clk,
+        "e2e": r["e2e"],
+        "gpu_launches": args.steps * layers * GPU_LAUNCHES_PER_LAYER,
+        "clocks": r["clocks"],
     }
+    del r
+    _free_device()
+    if world == 1 and not args.no_extra:
+        # the other decode workloads and the prefill chunk, timed in the same run
+        per = {}
+        for name in PER_CONFIG:
+            c = wl.CONFIGS[name]
+            wc = wl.generate(c)
+            lc = pool_sets(c, workload_figures(wc, 1), 0)
+            rc = decode_run(c, wc, lc, min(args.steps, 200), args.warmup, dev, world, full=False)
+            per[name] = {"config": decode_config(c, wc, lc), "decode_call_us": rc["call_us"],
+                         "decode_call_us_percentiles": rc["call_pct"], "tokens_per_s": rc["value"],
+                         "roofline": rc["roofline"], "achieved_tflops": rc["achieved_tflops"],
+                         "tensor_frac": rc["tensor_frac"], "clocks": rc["clocks"]}
+            del wc, rc
+            _free_device()
+        line["per_config"] = per
+        pf = bench_prefill(argparse.Namespace(steps=min(args.steps, 20), warmup=args.warmup),
+                           wl.CONFIGS[PREFILL_CONFIG])
+        line["prefill"] = {k: pf[k] for k in ("value", "unit", "ms_per_step", "config", "roofline",
+                                              "tokens_per_s", "clocks", "steps")}
+        _free_device()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     if rank == 0:

@@ -14,6 +14,9 @@ namespace fkv {
 // Device status word: kernels OR FORKKV_DEV_* bits into it; forkkv_get_device_status reads and clears it.
 __device__ uint32_t g_device_status;
 
+// Its device address on the current device, looked up once per device ordinal (with that device
+// current) and cached.  The address belongs to the device's primary context: it goes stale if the
+// process resets the device (cudaDeviceReset), after which the library must not be called again.
 uint32_t* device_status_ptr() {
   static std::mutex mu;
   static uint32_t* ptrs[64] = {nullptr};

@@ -22,7 +22,11 @@ static __device__ __align__(256) unsigned char g_decode_scratch[FORKKV_STATIC_SC
 
 // Device address of g_decode_scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached, keyed by the device ordinal:
+// the address belongs to the device's primary context (the one the CUDA runtime
+// uses), so it goes stale if the process resets the device (cudaDeviceReset) or
+// calls from another context of the same device; such a process must not call
+// this entry point after the reset.
 int32_t scratch_address(void** out) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};

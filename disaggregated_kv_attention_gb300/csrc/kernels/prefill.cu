@@ -208,7 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int t_first = (int)(row0 / G);
     const int t_last = (int)((min(row0 + kRows, n_rows) - 1) / G);
     int32_t pmax = -1;
-    for (int t = t_first; t <= t_last; ++t) pmax = max(pmax, a.positions[(int64_t)agent * a.q_len + t]);
+    bool bad_pos = false;  // a query position must name a slot of the sequence: 0 <= p, slot_of(p) < seq_len
+    for (int t = t_first; t <= t_last; ++t) {
+      const int32_t pt = a.positions[(int64_t)agent * a.q_len + t];
+      bad_pos |= pt < 0 || slot_of(pt) >= a.seq_lens[agent];
+      pmax = max(pmax, pt);
+    }
+    if (bad_pos) flag_status(a.status, kDevBadArg);
     if (a.seq_lens[agent] < 1 || a.seq_lens[agent] > a.max_seq_len) flag_status(a.status, kDevBadArg);
     if ((uint32_t)(a.adapter_ids ? a.adapter_ids[agent] : agent) >= (uint32_t)a.n_adapters)
       flag_status(a.status, kDevBadArg);

@@ -18,9 +18,23 @@
 #include <queue>
 #include <vector>
 
+#include <cuda_runtime.h>
+
 #include "../../include/forkkv.h"
 
 namespace {
+
+// SMs of the current device (one persistent decode CTA each); 152 (a GB300) when no device
+// answers, e.g. when a plan is built on a host without a GPU.
+int32_t device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n < 1) {
+    cudaGetLastError();  // leave no sticky error behind for the caller
+    return 152;
+  }
+  return n;
+}
 
 struct Segment {
   std::vector<int32_t> agents;
@@ -38,7 +52,7 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
                    forkkv_plan_info* info) {
   if (!bpt || !seq_lens || !info || n_agents < 1 || pt_stride < 1 || num_kv_heads < 1 || target_ctas < 0)
     return FORKKV_ERR_INVALID_ARG;
-  if (target_ctas == 0) target_ctas = 152;  // one persistent CTA per SM
+  if (target_ctas == 0) target_ctas = device_sms();  // one persistent CTA per SM
   std::vector<int32_t> npages(n_agents);
   for (int32_t a = 0; a < n_agents; ++a) {
     if (seq_lens[a] < 1) return FORKKV_ERR_INVALID_ARG;

@@ -83,9 +83,11 @@ extern "C" {
 #define FORKKV_PLAN_ITEM_INTS 16       /* int32 per decode work item         */
 #define FORKKV_PLAN_UNIT_INTS 16       /* int32 per decode unit record       */
 
-/* Message for a status code (static string). */
+/* Message for a status code (static string, owned by the library; never
+ * NULL, "unknown status" for a code it does not define).  No counterpart in
+ * the pages: error reporting of this library. */
 const char* forkkv_strerror(int32_t code);
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor).  No counterpart in the pages. */
 int32_t forkkv_version(void);
 
 /* ==== host allocator ======================================================
@@ -125,15 +127,24 @@ typedef struct {
   int64_t base_refsum, res_refsum; /* sum of refcounts */
 } forkkv_stats;
 
-/* Create an allocator over num_base_pages base and num_res_pages residual
- * pages of page_size tokens (page_size must be 16).  *out owns host memory
- * only; release it with forkkv_alloc_destroy. */
+/* Create an allocator over the two page pools of ForkKV L2 section 2 (Q2: a
+ * shared base cache and per-agent residual caches) and section 3 (Figure 6),
+ * paged as in the ForkServe README ("Design vs APC": location-addressed page
+ * frames, P = 16 tokens a page): num_base_pages base and num_res_pages
+ * residual pages (each >= 1) of page_size tokens (page_size must be 16:
+ * UNSUPPORTED otherwise; INVALID_ARG for a count < 1 or out == NULL).  *out
+ * owns host memory only (page ids, refcounts, per-sequence tables); the device
+ * pools it indexes are the caller's.  Release it with forkkv_alloc_destroy. */
 int32_t forkkv_alloc_create(int32_t num_base_pages, int32_t num_res_pages, int32_t page_size,
                             forkkv_alloc** out);
+/* Free the host memory of an allocator (every sequence with it); NULL is
+ * INVALID_ARG.  Device pools are not touched. */
 int32_t forkkv_alloc_destroy(forkkv_alloc* alloc);
 
-/* A root sequence of n_tokens >= 0 tokens with ceil(n/16) private base and
- * residual pages (base pages popped in logical order, then residual ones). */
+/* A root sequence (ForkKV L2 section 3, Figure 6: the parent agent whose
+ * prefix later agents fork from) of n_tokens >= 0 tokens with ceil(n/16)
+ * private base and residual pages (base pages popped in logical order, then
+ * residual ones).  OUT_OF_PAGES (nothing taken) when a pool is short. */
 int32_t forkkv_seq_create(forkkv_alloc* alloc, int32_t n_tokens, int32_t* seq_out);
 
 /* Fork (ForkKV L2 section 3, Figure 6; ForkServe "Methods", CoW tree):
@@ -177,8 +188,13 @@ int32_t forkkv_fork(forkkv_alloc* alloc, int32_t parent, int32_t prefix_len, uin
 int32_t forkkv_append(forkkv_alloc* alloc, int32_t seq, int32_t n_tokens, forkkv_cow_job* jobs,
                       int32_t jobs_cap, int32_t* n_jobs);
 
-/* Drop a sequence: every page's refcount - 1; pages reaching 0 are freed.
- * A child's references keep an aliased trunk alive after its parent is freed. */
+/* Drop a sequence (ForkServe README, "Design vs APC": the extra pin on owned
+ * frames, so that freeing a parent does not drop a trunk its children still
+ * map): every page's refcount - 1; pages reaching 0 are pushed back on their
+ * free stack in logical order (base pages, then residual pages).  A child's
+ * references keep an aliased trunk alive after its parent is freed.  An
+ * unknown or already freed sequence is INVALID_ARG; a refcount that would go
+ * below 0 is REFCOUNT (nothing changes in either case). */
 int32_t forkkv_free(forkkv_alloc* alloc, int32_t seq);
 
 /* Abort a speculative branch (ForkServe README, "Design vs APC" and "Methods":
@@ -211,21 +227,36 @@ int32_t forkkv_commit(forkkv_alloc* alloc, int32_t seq, int32_t lcp_len, const i
 int32_t forkkv_lcp_len(const int32_t* spec, int32_t n_spec, const int32_t* observed, int32_t n_observed,
                        int32_t* out);
 
+/* Length in tokens of a live sequence (INVALID_ARG for an unknown one). */
 int32_t forkkv_seq_len(const forkkv_alloc* alloc, int32_t seq, int32_t* len_out);
 
-/* Page tables of n sequences, row-major [n][stride] (host memory), unused
- * entries set to -1, and their lengths in slots (tokens + hole length, the
- * seq_lens the attention calls take).  INVALID_ARG if a sequence has more than
- * stride pages. */
+/* Per-agent page tables (ForkKV L2 section 3, Figure 6: an agent's bCache
+ * pages, aliased from its ancestors, and its own rCache pages; the ForkServe
+ * README's context tree maps a branch to the parent's frames plus its own):
+ * for seqs[0 .. n), row-major [n][stride] base page ids in bpt and residual
+ * page ids in rpt (host memory, caller-owned, n * stride int32 each), entries
+ * past a sequence's pages set to -1, and seq_lens[i] = its length in slots
+ * (tokens + hole length: the seq_lens the attention calls take).  INVALID_ARG
+ * for an unknown sequence or one with more than stride pages. */
 int32_t forkkv_page_tables(const forkkv_alloc* alloc, const int32_t* seqs, int32_t n, int32_t stride,
                            int32_t* bpt, int32_t* rpt, int32_t* seq_lens);
 
-/* Slot maps of n sequences (host memory): holes[2 i] = first slot of sequence
- * i's hole, holes[2 i + 1] = its length (0, 0 without a hole); the holes array
- * of the attention calls. */
+/* Slot maps of n sequences (ForkServe README, adaptive unaligned tail: the
+ * freeze variant "needs a fork-aware slot map"; host memory, caller-owned,
+ * 2 n int32): holes[2 i] = first slot of sequence i's hole, holes[2 i + 1] =
+ * its length (0, 0 without a hole); the holes array of the attention calls.
+ * INVALID_ARG for an unknown sequence. */
 int32_t forkkv_slot_maps(const forkkv_alloc* alloc, const int32_t* seqs, int32_t n, int32_t* holes);
 
+/* Refcount of one page (ForkServe README, "Design vs APC": fork aliases frames
+ * with refcounts; ForkKV L2 section 3: a bCache page is shared by every agent
+ * that maps it).  kind = FORKKV_JOB_BASE or FORKKV_JOB_RES picks the pool;
+ * BAD_PAGE for a page id outside it. */
 int32_t forkkv_refcount(const forkkv_alloc* alloc, int32_t kind, int32_t page, int32_t* out);
+/* Live, free and shared page counts and refcount sums of both pools (the
+ * accounting behind ForkKV L2 section 4's memory ratio M_R = 1/N + r/n and the
+ * ForkServe README's "Results" page counts).  The struct type holds the name
+ * forkkv_stats, so the call is forkkv_stats_get. */
 int32_t forkkv_stats_get(const forkkv_alloc* alloc, forkkv_stats* out);
 
 /* ==== pools ================================================================ */
@@ -301,7 +332,12 @@ int32_t forkkv_cow_copy_rows(const forkkv_pool_desc* pools, const forkkv_cow_job
  * frequencies (2m, 2m+1) form 8-byte group m = [cos 2m, cos 2m+1, sin 2m, sin 2m+1],
  * stored at 32-byte unit (m / 4) ^ (p % 8), slot m % 4, of the position's row.
  * Angles are reduced exactly in 64-bit fixed point before sin/cos. */
+/* Bytes of a table for n_positions >= 1 positions (INVALID_ARG otherwise). */
 int32_t forkkv_rope_table_bytes(int32_t n_positions, size_t* bytes);
+/* Fill a caller-owned device table (16-byte aligned, forkkv_rope_table_bytes
+ * long) with the rotations of ForkKV L2 section 7's deferred RoPE (Algorithm 1
+ * line 8, RoPE(K_res B_k) at each key's position), for theta > 0.  One launch
+ * on `stream`. */
 int32_t forkkv_rope_table_build(double rope_theta, int32_t n_positions, void* table, void* stream);
 
 /* ==== decode work plan =====================================================
@@ -329,8 +365,14 @@ typedef struct {
   int32_t plan_ints;   /* int32 words written to plan */
 } forkkv_plan_info;
 
-/* target_ctas: CTAs to spread the units over (0 = one per SM of a GB300); the
- * plan uses at most that many. */
+/* Build a plan (ForkKV L2 section 3, Figure 6 and the ForkServe README's
+ * context tree: the trunk of a fork tree is read once for the agents that map
+ * it).  bpt_host [n_agents][pt_stride] and seq_lens_host [n_agents] are host
+ * copies of the attention call's tables; plan is caller-owned host memory of
+ * plan_cap_ints int32 (INVALID_ARG, with info->plan_ints = the size needed,
+ * when it is too small).  target_ctas: CTAs to spread the units over (0 = one
+ * per SM of the current device); the plan uses at most that many.  Copy the
+ * plan to the device and pass it with info's counts in forkkv_attn_params. */
 int32_t forkkv_plan_build(const int32_t* bpt_host, const int32_t* seq_lens_host, int32_t n_agents,
                           int32_t pt_stride, int32_t num_kv_heads, int32_t target_ctas,
                           int32_t* plan, int32_t plan_cap_ints, forkkv_plan_info* info);
@@ -375,20 +417,39 @@ typedef struct {
                               forkkv_slot_maps), or NULL when no agent has a hole */
 } forkkv_attn_params;
 
-/* Scratch bytes forkkv_residual_attn_decode needs for these params. */
+/* Scratch bytes forkkv_residual_attn_decode needs for these params (the
+ * split-KV partials of ForkKV L2 section 4's attention fusion, one (m, l, acc,
+ * acc_r) per work segment, plus the rotation table when p->rope_table is NULL).
+ * Validates p as the decode call does (same status codes); *bytes is a
+ * multiple of 256. */
 int32_t forkkv_decode_workspace_size(const forkkv_attn_params* p, size_t* bytes);
 
-/* ResidualAttention decode (q_len = 1): split-KV over pages (or over a plan's
- * items), dual-accumulator online softmax, then one merge per (agent, query
- * head) that applies B_v once and writes bf16 out.  Launches 2 kernels (3 if
- * the rotation table is built in the workspace). */
+/* ResidualAttention decode (ForkKV L2 section 7, the decode version of the
+ * kernel; section 4: deferred RoPE of K_res B_k at each key's position, the
+ * attention fusion sum p Vb + (sum p Vr) B_v, and check 6, acc and acc_r
+ * rescaled together): q_len = 1, one query token per agent at positions[a]
+ * (= seq_lens[a] - 1 for a decode step whose row is already written).
+ * Split-KV over pages (or over a plan's items), dual-accumulator online
+ * softmax, then one merge per (agent, query head) that applies B_v once and
+ * writes bf16 out [A][Hq][128].  Every pointer is the caller's device memory
+ * (see forkkv_attn_params); workspace >= forkkv_decode_workspace_size bytes.
+ * Host checks (INVALID_ARG / UNSUPPORTED, nothing launched): geometry, null
+ * pointers, alignment, workspace size, plan sizes.  Device checks (status
+ * word): page ids, lengths, positions, adapter ids.  Asynchronous on `stream`;
+ * launches 2 kernels (3 if the rotation table is built in the workspace). */
 int32_t forkkv_residual_attn_decode(const forkkv_attn_params* p, void* stream);
 
+/* Scratch bytes the prefill chunk needs (the rotation table when
+ * p->rope_table is NULL, else 0); validates p as the prefill call does. */
 int32_t forkkv_prefill_workspace_size(const forkkv_attn_params* p, size_t* bytes);
 
-/* ResidualAttention over a prefill chunk: q_len query tokens per agent at
- * `positions`, causal (key j visible iff j <= position and j < seq_len).  The
- * chunk's own rows must already be in the pools (forkkv_write_rows). */
+/* ResidualAttention over a prefill chunk (ForkKV L2 section 7, the prefill
+ * version of the kernel; the same deferred RoPE and fusion as decode): q_len
+ * query tokens per agent at `positions` [A][q_len], causal (key j visible iff
+ * its position <= the query position and j < seq_len), out [A][q_len][Hq][128].
+ * The chunk's own rows must already be in the pools (forkkv_write_rows).  A
+ * query position outside [0, seq_len) sets FORKKV_DEV_BAD_ARG.  Same
+ * ownership, host checks and device checks as the decode call. */
 int32_t forkkv_residual_attn_prefill_chunk(const forkkv_attn_params* p, void* stream);
 
 /* ==== decode without caller scratch =======================================
@@ -407,8 +468,11 @@ int32_t forkkv_residual_attn_prefill_chunk(const forkkv_attn_params* p, void* st
  *     rotation table when `p->rope_table` is NULL) exceeds the array are
  *     rejected with FORKKV_ERR_SCRATCH before anything is launched.
  *   - The first call on each device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it per device ordinal; make that first
+ *     call before any stream capture.  The cached address belongs to the
+ *     device's primary context: after cudaDeviceReset the process must not
+ *     call this entry point again (the same holds for the status word that
+ *     forkkv_get_device_status reads).
  *   - Every call shares the one array and leaves its contents behind; nothing
  *     in it needs to start at zero (every partial is written before it is read).
  *     Calls whose kernels overlap on the GPU (different streams without
@@ -469,7 +533,9 @@ int32_t forkkv_wait_selftest(uint32_t polls, void* stream);
 
 /* Read and clear the device status word of the current device (OR of
  * FORKKV_DEV_* bits set by kernels since the last read).  Synchronises
- * `stream`. */
+ * `stream`.  No counterpart in the pages: the library's failure reporting
+ * (bad page ids, lengths or positions met on the device, and bounded waits
+ * that gave up, are recorded here instead of faulting or hanging). */
 int32_t forkkv_get_device_status(uint32_t* status, void* stream);
 
 #ifdef __cplusplus

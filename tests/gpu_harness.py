@@ -6,7 +6,8 @@ logical tensors directly, so a paging mistake shows up as a parity failure.
 """
 from __future__ import annotations
 
-from typing import Dict, Optional, Sequence
+import os
+from typing import Dict, List, Optional, Sequence
 
 import numpy as np
 import torch
@@ -35,6 +36,16 @@ def oracle(w: wl.Workload, agents: Sequence[int], q_heads: Optional[Sequence[int
     return res
 
 
+# (test id, max_abs, rel_l2) of every comparison made in this process; the session summary
+# (tests/conftest.py) prints them so that a drift towards the tolerance shows in the log.
+PARITY_LOG: List[tuple] = []
+
+
+def record(m: dict) -> None:
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    PARITY_LOG.append((test, m["max_abs"], m["rel_l2"]))
+
+
 def compare(out: torch.Tensor, ref: Dict[int, np.ndarray], q_rows: Optional[Sequence[int]] = None):
     from oracle import residual_attention as ra
     got, want = [], []
@@ -45,7 +56,9 @@ def compare(out: torch.Tensor, ref: Dict[int, np.ndarray], q_rows: Optional[Sequ
         got.append(o)
         want.append(r)
     got, want = np.stack(got), np.stack(want)
-    return ra.metrics(got, want), ra.within_tolerance(got, want)
+    m = ra.metrics(got, want)
+    record(m)
+    return m, ra.within_tolerance(got, want)
 
 
 # base tile / residual tile decoding, from the layout documented in include/forkkv.h

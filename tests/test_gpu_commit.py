@@ -15,6 +15,8 @@ import numpy as np
 import pytest
 import torch
 
+from gpu_harness import record
+
 from disaggregated_kv_attention_gb300 import forkkv as fk
 from disaggregated_kv_attention_gb300.paged import _slots
 from oracle import residual_attention as ra
@@ -129,5 +131,6 @@ def test_commit_split_then_decode_matches_oracle(use_plan):
         ref = ra.residual_attention(f64(q[i]), np.array([lens[i] - 1]), f64(kb), f64(vb), f64(kr), f64(vr),
                                     f64(B_k[i]), f64(B_v[i]), THETA)
         m = ra.metrics(got[i], ref)
+        record(m)
         assert ra.within_tolerance(got[i], ref), (i, m)
     fk.forkkv_alloc_destroy(alloc)

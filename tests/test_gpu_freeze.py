@@ -14,6 +14,8 @@ import numpy as np
 import pytest
 import torch
 
+from gpu_harness import record
+
 from disaggregated_kv_attention_gb300 import forkkv as fk
 from disaggregated_kv_attention_gb300.paged import token_slots
 from oracle import residual_attention as ra
@@ -127,6 +129,7 @@ def test_freeze_decode_matches_oracle(use_plan):
         assert kb.shape[0] == lens[i]
         ref = ra.residual_attention(_f64(q[i]), np.array([lens[i] - 1]), _f64(kb), _f64(vb), _f64(kr), _f64(vr),
                                     _f64(B_k[i]), _f64(B_v[i]), THETA)
+        record(ra.metrics(got[i], ref))
         assert ra.within_tolerance(got[i], ref), (i, ra.metrics(got[i], ref))
     fk.forkkv_alloc_destroy(alloc)
 
@@ -164,5 +167,6 @@ def test_freeze_prefill_chunk_matches_oracle():
     got = out[0].to(torch.float64).cpu().numpy()
     ref = ra.residual_attention(_f64(q[0]), positions[0].numpy(), _f64(kb), _f64(vb), _f64(kr), _f64(vr),
                                 _f64(B_k[0]), _f64(B_v[0]), THETA)
+    record(ra.metrics(got, ref))
     assert ra.within_tolerance(got, ref), ra.metrics(got, ref)
     fk.forkkv_alloc_destroy(alloc)

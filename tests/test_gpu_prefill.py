@@ -73,3 +73,19 @@ def test_prefill_first_token_sees_only_itself():
     ref = oracle(w, [0], q_rows=[0])
     m, ok = compare(out, ref, q_rows=[0])
     assert ok and m["max_abs"] < 1e-2, m
+
+
+@pytest.mark.parametrize("bad", ["negative", "past_end"])
+def test_prefill_position_outside_the_sequence_sets_bad_arg(bad):
+    # A query position must name a slot of its sequence (0 <= p < seq_len).  One out of range is
+    # reported through the device status word (FORKKV_DEV_BAD_ARG); the kernel still finishes.
+    nodes = [wl.Node("root", -1, (40, 40), False), wl.Node("a0", 0, (24, 24), True)]
+    w = _custom("badpos", 16, 4, nodes, q_len=24)
+    P = place(w)
+    P.positions[0, 5] = -1 if bad == "negative" else int(w.seq_lens[0])
+    out = torch.full_like(P.q, float("nan"))
+    p, keep = params(P, out, prefill=True)
+    fk.forkkv_residual_attn_prefill_chunk(p)
+    torch.cuda.synchronize()
+    assert fk.forkkv_get_device_status() == fk.DEV_BAD_ARG
+    assert fk.forkkv_get_device_status() == 0  # read and cleared; the context is still usable

@@ -40,6 +40,8 @@ def _setup(name):
 
 
 def _static_call(P, rope, keep):
+    """One call of the entry point that allocates nothing; rope=None makes it build the rotation
+    table inside its static array too."""
     out = torch.full_like(P.q, float("nan"))
     info = keep["info"]
     p = fk.attn_params(P.pools, 0, P.q, out, P.bpt, P.rpt, P.seq_lens, P.positions, P.max_seq_len, P.B_k, P.B_v,
@@ -61,6 +63,17 @@ def test_static_scratch_decode_matches_regular_decode_on_consecutive_calls():
     small = _setup("tiny_decode")
     for P, rope, ref, keep in (big, small, big):     # calls in a row share the array
         out = _static_call(P, rope, keep)
+        _check(out, ref)
+        assert fk.forkkv_get_device_status() == 0
+
+
+def test_static_scratch_builds_the_rotation_table_in_its_array_on_consecutive_calls():
+    # rope=None: the entry point builds the rotation table inside the static array as well (after
+    # the partials), so consecutive calls of different sizes overwrite each other's table.
+    big = _setup("llama3_8b_decode")
+    small = _setup("tiny_decode")
+    for P, rope, ref, keep in (small, big, small):
+        out = _static_call(P, None, keep)
         _check(out, ref)
         assert fk.forkkv_get_device_status() == 0
 
