@@ -2,6 +2,7 @@
 // async copies, ldmatrix, mma.sync, movmatrix) and the device status word.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -141,6 +142,18 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Box {128 B, 16 rows, 1 half, 8 pages} of a base K pool, seen as [pages][2 halves][16 rows][128 B]
+// through a tensor map, at (half, page) into shared memory: the rows of 128 keys of one 64-column
+// block, in the pool's (pre-swizzled) byte layout.
+__device__ __forceinline__ void tma_load_kb(void* dst, const CUtensorMap* map, int32_t half, int32_t page,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(half), "r"(page), "r"(smem_u32(bar))
       : "memory");
 }
 

@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       return v;
     };
     struct Blk {  // what the copies of one block need
-      int32_t bid, rid, h, na, pbase, nvp, Lmax, Lx;
+      int32_t bid, bx, rid, h, na, pbase, nvp, Lmax, Lx;
     };
     int kbl = 0, knb = 0;  // the cursor: next block within its unit, and the unit's blocks
     bool ended = false;
@@ -455,9 +455,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       x.na = kna;
       x.Lmax = kLmax;
       x.Lx = kLx;
-      x.bid = x.rid = 0;
+      x.bid = x.bx = x.rid = 0;
       if (lane < x.nvp) x.bid = a.bpt[(int64_t)kag0 * a.pt_stride + x.pbase + lane];
-      if (ag < kna && pg < x.nvp) x.rid = a.rpt[(int64_t)kagx * a.pt_stride + x.pbase + pg];
+      if (ag < kna && pg < x.nvp) {
+        x.rid = a.rpt[(int64_t)kagx * a.pt_stride + x.pbase + pg];
+        if (ag > 0) x.bx = a.bpt[(int64_t)kagx * a.pt_stride + x.pbase + pg];  // the other agents' base pages
+      }
       ++kbl;
       return true;
     };
@@ -470,6 +473,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       nx = nx2;
       more = more2;
       if (more2) more2 = next_block(nx2);  // the ids of the block after next go out now
+      // The group shares its base pages: the first agent's ids serve every agent.  A plan built
+      // before a copy-on-write split, a commit or an append that changed an agent's pages no
+      // longer matches the page tables: reported (the first agent's pages are read).
+      const int32_t b0 = __shfl_sync(0xffffffffu, b.bid, pg);  // the first agent's page pg
+      if (ag > 0 && ag < b.na && pg < b.nvp && b.bx != b0) flag_status(a.status, kDevBadArg);
       if ((uint32_t)b.bid >= (uint32_t)a.num_base_pages) {
         flag_status(a.status, kDevBadPage);
         b.bid = 0;
@@ -1038,6 +1046,10 @@ struct CombineArgs {
   const int32_t* adapter_ids;
   int32_t n_adapters;
   __nv_bfloat16* out;        // [A][Hq][128]
+  const int32_t* items;      // plan mode: the plan's work items (FORKKV_PLAN_ITEM_INTS each), else null
+  int32_t n_items;
+  const int32_t* seq_lens;   // [A]
+  int32_t max_seq_len;
 };
 
 constexpr int kCombineChunk = 16;  // slots merged per pass (their partials held in registers)
@@ -1066,6 +1078,25 @@ __global__ void __launch_bounds__(kMaxGroupQ * kHeadDim) decode_combine_kernel(c
   if (s_begin < 0 || s_end < s_begin || s_end > a.n_slots) {
     if (tid == 0) flag_status(a.status, kDevBadArg);
     s_end = s_begin = 0;
+  }
+  if (a.items && h == 0) {
+    // The plan's items of this agent must cover its pages exactly: a sequence that entered a new
+    // page (or was truncated) after the plan was built would otherwise be attended partially.
+    __shared__ int32_t s_pages;
+    if (tid == 0) s_pages = 0;
+    __syncthreads();
+    int32_t pages = 0;
+    for (int32_t i = tid; i < a.n_items; i += blockDim.x) {
+      const int32_t* it = a.items + (int64_t)i * FORKKV_PLAN_ITEM_INTS;
+      const int32_t na = it[2];
+      bool mine = false;
+      for (int x = 0; x < 8; ++x) mine |= x < na && it[4 + x] == agent;
+      if (mine) pages += it[1] - it[0];
+    }
+    if (pages) atomicAdd(&s_pages, pages);
+    __syncthreads();
+    if (tid == 0 && s_pages != (min(a.seq_lens[agent], a.max_seq_len) + kPage - 1) / kPage)
+      flag_status(a.status, kDevBadArg);
   }
   int32_t adapter = a.adapter_ids ? a.adapter_ids[agent] : agent;
   if ((uint32_t)adapter >= (uint32_t)a.n_adapters) adapter = 0;
@@ -1135,6 +1166,27 @@ __global__ void __launch_bounds__(kMaxGroupQ * kHeadDim) decode_combine_kernel(c
 
 }  // namespace
 
+// SMs of the current device (the persistent decode grid is at most one CTA per SM); 152, a GB300,
+// if the device does not answer.
+static int32_t current_sm_count() {
+  static thread_local int cached_dev = -1, cached_sms = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cached_dev = dev;
+    cached_sms = n;
+  }
+  return cached_sms;
+}
+
 DecodeGeometry decode_geometry(const forkkv_attn_params& p) {
   DecodeGeometry g{};
   const int32_t G = p.num_q_heads / p.num_kv_heads;
@@ -1146,7 +1198,7 @@ DecodeGeometry decode_geometry(const forkkv_attn_params& p) {
     // the 8 pages of a block) so that the A * chunks * Hkv units fill the SMs without
     // passing one unit per SM (a second, partial round would double the time).
     const int32_t max_pages = (p.max_seq_len + kPage - 1) / kPage;
-    const int64_t want = 152;  // one CTA per SM
+    const int64_t want = current_sm_count();  // one CTA per SM
     int32_t chunks = (int32_t)(want / ((int64_t)p.n_agents * p.num_kv_heads));
     chunks = max(1, min(chunks, (max_pages + 7) / 8));
     int32_t chunk_pages = (max_pages + chunks - 1) / chunks;
@@ -1167,13 +1219,12 @@ DecodeGeometry decode_geometry(const forkkv_attn_params& p) {
 
 cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, const void* rope_table,
                           uint32_t* status, cudaStream_t stream) {
-  static thread_local int configured_device = -1, sm_count = 0;
+  static thread_local int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  const int sm_count = current_sm_count();
   if (configured_device != dev) {
-    e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(decode_split_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(decode_split_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -1247,6 +1298,10 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   c.adapter_ids = p.adapter_ids;
   c.n_adapters = p.n_adapters;
   c.out = static_cast<__nv_bfloat16*>(p.out);
+  c.items = p.plan;  // the items come first in a plan
+  c.n_items = p.plan ? p.plan_items : 0;
+  c.seq_lens = p.seq_lens;
+  c.max_seq_len = p.max_seq_len;
   decode_combine_kernel<<<dim3(p.n_agents, p.num_kv_heads), G * kHeadDim, 0, stream>>>(c);
   return cudaGetLastError();
 }

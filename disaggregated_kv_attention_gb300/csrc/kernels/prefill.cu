@@ -115,15 +115,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// Box {128 B, 16 rows, 1 half, 8 pages} of the base K pool at (half, page) into shared memory.
-__device__ __forceinline__ void tma_load_kb(void* dst, const CUtensorMap* map, int32_t half, int32_t page,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(half), "r"(page), "r"(smem_u32(bar))
-      : "memory");
-}
 
 struct PrefillArgs {
   // This layer's base K pool as [Hkv * pages][2 halves][16 rows][128 B]: a box of 8 pages of one

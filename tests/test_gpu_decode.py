@@ -268,3 +268,49 @@ def test_step_graph_matches_per_layer_calls():
     torch.cuda.synchronize()
     m, ok = compare(out_ref[0], oracle(w, range(A)))
     assert ok, m
+
+
+def _stale_plan_run(P, bpt, seq_lens, positions, plan_src):
+    """Decode with tables (bpt, seq_lens, positions) but a plan built from plan_src's tables."""
+    out = torch.full_like(P.q, float("nan"))
+    plan, info = fk.forkkv_plan_build(plan_src[0], plan_src[1], P.w.cfg.n_kv_heads)
+    plan_d = torch.from_numpy(plan).to(P.device)
+    p = fk.attn_params(P.pools, 0, P.q, out, bpt, P.rpt, seq_lens, positions, P.max_seq_len, P.B_k, P.B_v,
+                       rope_theta=P.w.cfg.rope_theta, plan=plan_d, plan_info=info)
+    ws = fk.workspace_for(p)
+    fk.forkkv_residual_attn_decode(p)
+    torch.cuda.synchronize()
+    del ws
+    return fk.forkkv_get_device_status()
+
+
+def test_stale_plan_after_a_split_page_is_flagged():
+    # After a copy-on-write split one agent maps its own copy of a trunk page; a plan built before
+    # the split still groups it with the others.  The producer compares every agent's base page
+    # ids of a block with the first agent's and reports the mismatch (FORKKV_DEV_BAD_ARG); the
+    # kernel still runs to the end.  A plan built from the new tables raises nothing.
+    w = wl.generate(wl.CONFIGS["llama3_8b_decode"])
+    P = place(w)
+    old = (P.bpt_np.copy(), w.seq_lens.numpy().copy())
+    bpt = P.bpt.clone()
+    bpt[3, 2] = int(P.bpt_np[0, 5])   # agent 3's page 2 now names another (valid) base page
+    assert _stale_plan_run(P, bpt, P.seq_lens, P.positions, old) == fk.DEV_BAD_ARG
+    assert _stale_plan_run(P, bpt, P.seq_lens, P.positions, (bpt.cpu().numpy(), old[1])) == 0
+
+
+def test_stale_plan_after_a_sequence_grew_into_a_new_page_is_flagged():
+    # An agent whose sequence entered a new page after the plan was built: the plan's items cover
+    # fewer pages than its length needs.  The combine kernel checks coverage and reports it.
+    w = wl.generate(wl.CONFIGS["llama3_8b_decode"])
+    P = place(w)
+    old = (P.bpt_np.copy(), w.seq_lens.numpy().copy())
+    a = int(np.argmin(old[1]))                       # the shortest agent stays within max_seq_len
+    seq_lens, positions = P.seq_lens.clone(), P.positions.clone()
+    grow = 16 - (int(old[1][a]) % 16) + 1            # one slot into the page after its last
+    seq_lens[a] += grow
+    positions[a, 0] += grow
+    assert int(seq_lens[a]) <= P.max_seq_len
+    bpt = P.bpt.clone()
+    new_page = (int(seq_lens[a]) - 1) // 16
+    bpt[a, new_page] = int(P.bpt_np[a, 0])
+    assert _stale_plan_run(P, bpt, seq_lens, positions, old) & fk.DEV_BAD_ARG

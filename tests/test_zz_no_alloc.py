@@ -45,7 +45,7 @@ def _static_call(P, rope, keep):
     out = torch.full_like(P.q, float("nan"))
     info = keep["info"]
     p = fk.attn_params(P.pools, 0, P.q, out, P.bpt, P.rpt, P.seq_lens, P.positions, P.max_seq_len, P.B_k, P.B_v,
-                       rope=rope, plan=keep["plan"], plan_info=info)
+                       rope=rope, rope_theta=P.w.cfg.rope_theta, plan=keep["plan"], plan_info=info)
     fk.forkkv_residual_attn_decode_static(p)          # no workspace passed
     torch.cuda.synchronize()
     return out
