@@ -95,10 +95,12 @@ def _traffic(kernel: str, workload: str):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)[kernel][workload]
-        src = os.path.join(ROOT, d["source"])
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        return d["dram_bytes_per_launch"] if sha == d["source_sha256"] else None
+        sources = d.get("sources") or [d["source"]]
+        h = hashlib.sha256()
+        for src in sources:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return d["dram_bytes_per_launch"] if h.hexdigest() == d.get("sources_sha256", d.get("source_sha256")) else None
     except Exception:
         return None
 

@@ -107,29 +107,6 @@ __device__ __forceinline__ void st4(uint32_t taddr, const uint32_t* r) {
 }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 16-lane shapes: a warp reads (writes) 16 TMEM lanes starting at the lane of `taddr` (inside its
-// quadrant), 8 consecutive 32-bit columns per repetition.  Thread i holds, for repetition k,
-//   r[4k + 0] = (lane i/4,     column 8k + 2(i%4)),  r[4k + 1] = (lane i/4,     column 8k + 2(i%4) + 1),
-//   r[4k + 2] = (lane i/4 + 8, column 8k + 2(i%4)),  r[4k + 3] = (lane i/4 + 8, column 8k + 2(i%4) + 1),
-// the accumulator layout of a warp-level m16n8 MMA with the lanes as its rows.
-__device__ __forceinline__ void ld16x256_x1(uint32_t taddr, uint32_t* r) {
-  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(taddr));
-}
-__device__ __forceinline__ void ld16x256_x4(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void st16x256_x1(uint32_t taddr, const uint32_t* r) {
-  asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
-               "r"(r[2]), "r"(r[3])
-               : "memory");
-}
-
 // Byte offset of (row, col) in a K-major, 128-byte-swizzled tile of `rows` rows:
 // [col / 64][row][128 B], 16-byte chunk c of a row stored at chunk c ^ (row % 8).
 __device__ __forceinline__ uint32_t sw128_off(int rows, int row, int col) {

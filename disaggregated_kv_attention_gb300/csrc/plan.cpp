@@ -106,11 +106,13 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
   // 2. groups of at most 4 agents (4, then 2, 1 for the remainder)
   struct Chunk {
     int32_t agents[8];
-    int32_t na, p0, p1, stages;
+    int32_t na, p0, p1, stages, seg, grp;  // grp: the chunk's index among its segment's groups
   };
   std::vector<Chunk> chunks;
-  for (const Segment& s : segs) {
+  for (size_t si = 0; si < segs.size(); ++si) {
+    const Segment& s = segs[si];
     size_t k = 0;
+    int32_t grp = 0;
     while (k < s.agents.size()) {
       const size_t left = s.agents.size() - k;
       const int32_t na = left >= kMaxGroup ? kMaxGroup : left >= 2 ? 2 : 1;
@@ -121,6 +123,8 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
       c.p1 = s.p1;
       const int32_t wpp = pages_per_stage(na);
       c.stages = (s.p1 - s.p0 + wpp - 1) / wpp;
+      c.seg = (int32_t)si;
+      c.grp = grp++;
       chunks.push_back(c);
       k += na;
     }
@@ -148,6 +152,7 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
   struct Unit {
     int64_t cost;
     int32_t code;
+    int32_t seg, first, head, grp;  // siblings: the groups of one segment on the same pages and head
   };
   // items under caps T: (chunk index, first stage, end stage)
   auto make_items = [&](const int32_t* T, std::vector<std::array<int32_t, 3>>& out) {
@@ -171,10 +176,21 @@ int32_t plan_build(const int32_t* bpt, const int32_t* seq_lens, int32_t n_agents
     std::vector<Unit> units;
     units.reserve(its.size() * num_kv_heads);
     for (size_t i = 0; i < its.size(); ++i) {
-      const int64_t cost = unit_cost(its[i][2] - its[i][1], chunks[its[i][0]].na);
-      for (int32_t h = 0; h < num_kv_heads; ++h) units.push_back({cost, (int32_t)(i * num_kv_heads + h)});
+      const Chunk& c = chunks[its[i][0]];
+      const int64_t cost = unit_cost(its[i][2] - its[i][1], c.na);
+      for (int32_t h = 0; h < num_kv_heads; ++h)
+        units.push_back({cost, (int32_t)(i * num_kv_heads + h), c.seg, its[i][1], h, c.grp});
     }
-    std::stable_sort(units.begin(), units.end(), [](const Unit& x, const Unit& y) { return x.cost > y.cost; });
+    // Largest first; among equal costs, the groups that share a segment's pages (a trunk read by
+    // several agent groups) next to each other for the same pages and head, so that they land on
+    // CTAs of equal load and stream those pages at the same time: the repeats then come from L2.
+    std::stable_sort(units.begin(), units.end(), [](const Unit& x, const Unit& y) {
+      if (x.cost != y.cost) return x.cost > y.cost;
+      if (x.seg != y.seg) return x.seg < y.seg;
+      if (x.first != y.first) return x.first < y.first;
+      if (x.head != y.head) return x.head < y.head;
+      return x.grp < y.grp;
+    });
     const int32_t C = (int32_t)std::min<int64_t>(C_max, (int64_t)units.size());
     using Load = std::pair<int64_t, int32_t>;  // (load, CTA): the least loaded, then the lowest index
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
