@@ -193,7 +193,7 @@ int32_t forkkv_cow_copy_rows(const forkkv_pool_desc* pools, const forkkv_cow_job
 
 int32_t forkkv_rope_table_bytes(int32_t n_positions, size_t* bytes) {
   if (n_positions < 0 || !bytes) return FORKKV_ERR_INVALID_ARG;
-  *bytes = (size_t)n_positions * FORKKV_ROPE_ROW_BYTES;
+  *bytes = (size_t)((n_positions + FORKKV_PAGE_SIZE - 1) / FORKKV_PAGE_SIZE) * FORKKV_PAGE_SIZE * FORKKV_ROPE_ROW_BYTES;
   return FORKKV_OK;
 }
 

@@ -30,9 +30,12 @@ __host__ __device__ __forceinline__ uint32_t base_off(int t, int d) {
 __host__ __device__ __forceinline__ uint32_t res_off(int t, int k) {
   return (uint32_t)(t * 32 + (((k >> 3) ^ ((t >> 2) & 1)) << 4) + (k & 7) * 2);
 }
-// Byte offset of frequency group m (frequencies 2m, 2m+1) in the rotation-table row of position p.
-__host__ __device__ __forceinline__ uint32_t rope_off(int p, int m) {
-  return (uint32_t)((((m >> 2) ^ (p & 7)) << 5) + (m & 3) * 8);
+// Byte offset in the rotation table of frequency group m (8 bytes: cos 2m, cos 2m+1, sin 2m,
+// sin 2m+1) of position p.  Page-major: the 16 positions of a page take 4 KB, in which group
+// block m / 4 (512 bytes) holds the page's positions 32 bytes apart, group m % 4 at 8 m % 32.
+// A warp that reads one group block of 8 consecutive positions reads 256 contiguous bytes.
+__host__ __device__ __forceinline__ int64_t rope_off(int64_t p, int m) {
+  return (p >> 4) * 4096 + (m >> 2) * 512 + (p & 15) * 32 + (m & 3) * 8;
 }
 
 __device__ __forceinline__ void flag_status(uint32_t* status, uint32_t bits) {

@@ -712,18 +712,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const int pbase = p0 + b * kBlockPages;
         const int j = pbase * kPage + row;
         if (ai == 0) {
-          // chunk c = 32 hf + 16 cc holds frequency groups m = c/2 .. c/2 + 7: 32-byte units
-          // c/8 and c/8 + 1 of the row of position jr, stored at unit u ^ (jr % 8)
+          // chunk c = 32 hf + 16 cc holds frequency groups m = c/2 .. c/2 + 7: the 32-byte group
+          // blocks c/8 and c/8 + 1 of position jr (rope_off(jr, 4 u) for block u)
           const int kp = (hn0 != 0 && j >= hend) ? j - hn0 : j;
           const int jr = kp < a.rope_positions ? kp : 0;
-          const uint4* rrow = reinterpret_cast<const uint4*>(a.rope + (int64_t)jr * kRopeRow);
+          const uint8_t* rrow = a.rope + rope_off(jr, 0);
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
             for (int uu = 0; uu < 2; ++uu) {
               const int un = 4 * hf + 2 * cc + uu;
-              rp[cc][2 * uu] = __ldg(rrow + (un ^ (jr & 7)) * 2);
-              rp[cc][2 * uu + 1] = __ldg(rrow + (un ^ (jr & 7)) * 2 + 1);
+              rp[cc][2 * uu] = __ldg(reinterpret_cast<const uint4*>(rrow + un * 512));
+              rp[cc][2 * uu + 1] = __ldg(reinterpret_cast<const uint4*>(rrow + un * 512 + 16));
             }
           ok = mbar_wait(&bars[kKFull0 + stage], (g >> 1) & 1, a.status);
           if (!ok) break;
@@ -1256,7 +1256,8 @@ cudaError_t launch_decode(const forkkv_attn_params& p, const DecodeGeometry& g, 
   a.adapter_ids = p.adapter_ids;
   a.n_adapters = p.n_adapters;
   a.rope = static_cast<const uint8_t*>(rope_table);
-  a.rope_positions = p.rope_table ? p.rope_table_positions : (p.max_seq_len + kPage - 1) / kPage * kPage;
+  // whole pages of the table only (a page-major table holds positions in blocks of 16)
+  a.rope_positions = p.rope_table ? p.rope_table_positions / kPage * kPage : (p.max_seq_len + kPage - 1) / kPage * kPage;
   const float scale = p.sm_scale > 0.f ? p.sm_scale : 1.0f / sqrtf((float)kHeadDim);
   a.scale_log2 = scale * 1.4426950408889634f;
   int32_t n_ctas;

@@ -488,14 +488,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const uint32_t ub = tl + kTmBuf + 128 * (b & 1);
       const int j = b * kBlockKeys + row;
       const int jr = kpos(j) < a.rope_positions ? kpos(j) : 0;
-      // this key's rotation row (position jr): frequency groups 4 u .. 4 u + 3 are 32-byte unit u,
-      // stored at unit u ^ (jr % 8); this half needs units 4 hf .. 4 hf + 3
-      const uint4* rrow = reinterpret_cast<const uint4*>(a.rope + (int64_t)jr * kRopeRow);
+      // this key's rotation entries (position jr): frequency groups 4 u .. 4 u + 3 are 32 bytes
+      // at rope_off(jr, 4 u); this half needs u = 4 hf .. 4 hf + 3
+      const uint8_t* rrow = a.rope + rope_off(jr, 0);
       uint4 rp[4][2];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        rp[u][0] = rrow[((4 * hf + u) ^ (jr & 7)) * 2];
-        rp[u][1] = rrow[((4 * hf + u) ^ (jr & 7)) * 2 + 1];
+        rp[u][0] = *reinterpret_cast<const uint4*>(rrow + (4 * hf + u) * 512);
+        rp[u][1] = *reinterpret_cast<const uint4*>(rrow + (4 * hf + u) * 512 + 16);
       }
       ok = mbar_wait(&bars[kKFull0 + stage], (b / kKStages) & 1, a.status) &&
            mbar_wait(&bars[kUFull0 + (b & 1)], (b >> 1) & 1, a.status);
@@ -802,7 +802,8 @@ cudaError_t launch_prefill(const forkkv_attn_params& p, const void* rope_table, 
   a.adapter_ids = p.adapter_ids;
   a.n_adapters = p.n_adapters;
   a.rope = static_cast<const uint8_t*>(rope_table);
-  a.rope_positions = p.rope_table ? p.rope_table_positions : (p.max_seq_len + kPage - 1) / kPage * kPage;
+  // whole pages of the table only (a page-major table holds positions in blocks of 16)
+  a.rope_positions = p.rope_table ? p.rope_table_positions / kPage * kPage : (p.max_seq_len + kPage - 1) / kPage * kPage;
   const float scale = p.sm_scale > 0.f ? p.sm_scale : 1.0f / sqrtf((float)kHeadDim);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__
   uint2 v;
   v.x = pack_bf16(cs[0], cs[1]);
   v.y = pack_bf16(sn[0], sn[1]);
-  *reinterpret_cast<uint2*>(a.table + (int64_t)p * kRopeRow + rope_off(p, m)) = v;
+  *reinterpret_cast<uint2*>(a.table + rope_off(p, m)) = v;
 }
 
 // Self-test of the bounded waits: one thread waits on a shared-memory mbarrier that nothing

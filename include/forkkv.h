@@ -328,11 +328,14 @@ int32_t forkkv_cow_copy_rows(const forkkv_pool_desc* pools, const forkkv_cow_job
 
 /* ==== rotation table ======================================================
  * cos/sin of p * theta^(-2i/128) for positions p < n_positions and the 64
- * rotate-half frequencies i (bf16), FORKKV_ROPE_ROW_BYTES per position:
- * frequencies (2m, 2m+1) form 8-byte group m = [cos 2m, cos 2m+1, sin 2m, sin 2m+1],
- * stored at 32-byte unit (m / 4) ^ (p % 8), slot m % 4, of the position's row.
+ * rotate-half frequencies i (bf16), FORKKV_ROPE_ROW_BYTES per position, laid
+ * out page-major: frequencies (2m, 2m+1) form the 8-byte group m =
+ * [cos 2m, cos 2m+1, sin 2m, sin 2m+1] of position p, at byte
+ * (p / 16) * 4096 + (m / 4) * 512 + (p % 16) * 32 + (m % 4) * 8, so that the
+ * same groups of consecutive positions are contiguous.
  * Angles are reduced exactly in 64-bit fixed point before sin/cos. */
-/* Bytes of a table for n_positions >= 1 positions (INVALID_ARG otherwise). */
+/* Bytes of a table for n_positions >= 0 positions, whole pages of 16
+ * positions (INVALID_ARG for n_positions < 0). */
 int32_t forkkv_rope_table_bytes(int32_t n_positions, size_t* bytes);
 /* Fill a caller-owned device table (16-byte aligned, forkkv_rope_table_bytes
  * long) with the rotations of ForkKV L2 section 7's deferred RoPE (Algorithm 1
@@ -403,7 +406,8 @@ typedef struct {
   const void* B_v;         /* bf16 [n_adapters][16][num_kv_heads * 128] */
   const int32_t* adapter_ids; /* [A] adapter of each agent, or NULL for agent a -> adapter a */
   int32_t n_adapters;
-  const void* rope_table;  /* table for >= max_seq_len positions, or NULL: built in workspace */
+  const void* rope_table;  /* table for >= max_seq_len positions (whole pages of 16 are read),
+                              or NULL: built in workspace */
   int32_t rope_table_positions;
   double rope_theta;       /* used when rope_table is NULL */
   float sm_scale;          /* 0 -> 1/sqrt(128) */

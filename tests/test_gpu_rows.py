@@ -126,14 +126,13 @@ def test_rope_table_matches_float64_trig():
     n = 2 ** 17 + 64
     t = fk.rope_table(theta, n)
     torch.cuda.synchronize()
-    raw = t.cpu().numpy()
+    raw = t.cpu().numpy().reshape(-1)
     pos = np.array([0, 1, 2, 15, 16, 1000, 65535, 2 ** 17, 2 ** 17 + 17, n - 1])
     f = theta ** (-np.arange(0, 128, 2, dtype=np.float64) / 128)
     for p in pos:
-        row = raw[p]
         for m in range(32):
-            off = (((m >> 2) ^ (p & 7)) << 5) + (m & 3) * 8
-            bits = row[off:off + 8].view(np.uint16).astype(np.uint32) << 16
+            off = (p >> 4) * 4096 + (m >> 2) * 512 + (p & 15) * 32 + (m & 3) * 8  # page-major layout
+            bits = raw[off:off + 8].view(np.uint16).astype(np.uint32) << 16
             vals = bits.view(np.float32).astype(np.float64)  # bf16 -> fp32 is exact
             ang = p * f[2 * m:2 * m + 2]
             assert np.allclose(vals[:2], np.cos(ang), atol=4e-3, rtol=0), (p, m)  # bf16: 2^-9 relative
