@@ -300,6 +300,20 @@ __device__ __forceinline__ void copy_tiles(const uint8_t* pool, bool base, int32
   }
 }
 
+// Every wait of this kernel hints the hardware to suspend the waiting thread for up to 1 us
+// per poll (it wakes as soon as the phase completes), so waiting warps leave the issue slots to
+// the working ones (measured: 1-1.5 % faster than polls without the hint).
+constexpr uint32_t kSuspendNs = 1000;
+
+// Bounded wait for a phase (acquire), suspending between polls.
+__device__ __forceinline__ bool mbar_wait_s(uint64_t* bar, uint32_t parity, uint32_t* status) {
+#pragma unroll 1
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait_for(bar, parity, kSuspendNs)) return true;
+  flag_status(status, kDevTimeout);
+  return false;
+}
+
 // Wait for a phase completed by a tensor-core commit (the waiter orders its tensor-memory
 // accesses with tcgen05.fence::after_thread_sync, so no memory acquire is needed).
 __device__ __forceinline__ bool mbar_wait_tc(uint64_t* bar, uint32_t parity, uint32_t* status) {
@@ -308,10 +322,10 @@ __device__ __forceinline__ bool mbar_wait_tc(uint64_t* bar, uint32_t parity, uin
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     if (ok) return true;
   }
@@ -382,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 
   // Unit k of this CTA as published by the producer: wait for its descriptor, and release
   // the ring slot once the caller has copied what it needs (`take`).
-  auto unit_wait = [&](int k) { return mbar_wait(&bars[kUnitReady0 + (k & 1)], (k >> 1) & 1, a.status); };
+  auto unit_wait = [&](int k) { return mbar_wait_s(&bars[kUnitReady0 + (k & 1)], (k >> 1) & 1, a.status); };
   auto unit_at = [&](int k, int f) -> int32_t { return s_units[(k & 1) * kUnitInts + f]; };
   auto unit_release = [&](int k) {
     __syncwarp();
@@ -407,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     bool ok = true;
     // publish `cur` as unit n_pub once its ring slot is free; build the next descriptor
     auto publish = [&]() -> int32_t {
-      if (n_pub >= 2) ok = ok && mbar_wait(&bars[kUnitFree0 + (n_pub & 1)], ((n_pub >> 1) - 1) & 1, a.status);
+      if (n_pub >= 2) ok = ok && mbar_wait_s(&bars[kUnitFree0 + (n_pub & 1)], ((n_pub >> 1) - 1) & 1, a.status);
       const int32_t v = unit_finish(a, cur, lane);
       if (lane < kUnitInts) s_units[(n_pub & 1) * kUnitInts + lane] = v;
       __syncwarp();
@@ -490,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       const bool brun = __ballot_sync(0xffffffffu, lane < 8 && pg > 0 && pg < b.nvp && b.bid != pb + 1) == 0;
       const bool rrun = ((__ballot_sync(0xffffffffu, pg > 0 && pg < b.nvp && b.rid != pr + 1) >> (lane & ~7)) & 0xffu) == 0;
       // K tiles
-      if (g >= 2 && !(ok = mbar_wait(&bars[kKEmpty0 + (g & 1)], ((g >> 1) - 1) & 1, a.status))) break;
+      if (g >= 2 && !(ok = mbar_wait_s(&bars[kKEmpty0 + (g & 1)], ((g >> 1) - 1) & 1, a.status))) break;
       uint64_t* kbar = &bars[kKFull0 + (g & 1)];
       if (lane == 0) mbar_arrive_expect_tx(kbar, tile_bytes(true, b.nvp, kPage));
       if (lane < 8)
@@ -499,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       // each agent's k_res tiles, into the slot of its (block, agent) step
       for (int x = 0; x < b.na && ok; ++x) {
         const int n = kn + x, kslot = n & 3;
-        if (n >= kResSlots && !(ok = mbar_wait(&bars[kKrEmpty0 + kslot], ((n >> 2) - 1) & 1, a.status))) break;
+        if (n >= kResSlots && !(ok = mbar_wait_s(&bars[kKrEmpty0 + kslot], ((n >> 2) - 1) & 1, a.status))) break;
         uint64_t* rbar = &bars[kKrFull0 + kslot];
         if (lane == 8 * x) mbar_arrive_expect_tx(rbar, tile_bytes(false, b.nvp, kPage));
         if (ag == x) copy_tiles(a.k_res, false, b.rid, b.nvp, kPage, smem + kOffKr + kslot * kResSlotBytes, rbar, rrun, pg);
@@ -508,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       kn += b.na;
       // V tiles and every agent's v_res tiles, on one barrier (released by the block's value
       // products); one arrival raises the bytes of every group
-      if (g >= 2 && !(ok = mbar_wait(&bars[kVEmpty0 + (g & 1)], ((g >> 1) - 1) & 1, a.status))) break;
+      if (g >= 2 && !(ok = mbar_wait_s(&bars[kVEmpty0 + (g & 1)], ((g >> 1) - 1) & 1, a.status))) break;
       uint64_t* vbar = &bars[kVFull0 + (g & 1)];
       const int last = (b.pbase + b.nvp - 1) * kPage;  // first key of the block's last page
       const int vrows = min(kPage, max(0, b.Lmax - last));
@@ -533,10 +547,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
     // never leave with copies in flight: the last phase of every barrier written to
     for (int b = max(0, g - 2); b < g; ++b) {
-      mbar_wait(&bars[kKFull0 + (b & 1)], (b >> 1) & 1, a.status);
-      mbar_wait(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status);
+      mbar_wait_s(&bars[kKFull0 + (b & 1)], (b >> 1) & 1, a.status);
+      mbar_wait_s(&bars[kVFull0 + (b & 1)], (b >> 1) & 1, a.status);
     }
-    for (int n = max(0, kn - kResSlots); n < kn; ++n) mbar_wait(&bars[kKrFull0 + (n & 3)], (n >> 2) & 1, a.status);
+    for (int n = max(0, kn - kResSlots); n < kn; ++n) mbar_wait_s(&bars[kKrFull0 + (n & 3)], (n >> 2) & 1, a.status);
   } else if (warp == 1) {
     // ------------------------------ U issuer ------------------------------
     //   U = Kr . B_k   [128 keys x 128]   per (block, agent).  Per unit the warp stages B_k of
@@ -563,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (k > 0) {  // every U of the previous unit is done with B_k
         if (lane == 0) {
           tc::commit(&bars[kUUnit]);
-          ok = mbar_wait(&bars[kUUnit], (k - 1) & 1, a.status);
+          ok = mbar_wait_s(&bars[kUUnit], (k - 1) & 1, a.status);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -589,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (lane == 0) {
         for (int n = 0; n < N && ok; ++n) {
           const int m = gn + n;
-          ok = mbar_wait(&bars[kKrFull0 + (m & 3)], (m >> 2) & 1, a.status) &&
-               (m < 2 || mbar_wait(&bars[kUFree0 + (m & 1)], ((m >> 1) - 1) & 1, a.status));
+          ok = mbar_wait_s(&bars[kKrFull0 + (m & 3)], (m >> 2) & 1, a.status) &&
+               (m < 2 || mbar_wait_s(&bars[kUFree0 + (m & 1)], ((m >> 1) - 1) & 1, a.status));
           if (!ok) break;
           tc::fence_after();
           tc::mma_ss(tm + kTmU + 128 * (m & 1), dKr + (m & 3) * (kResSlotBytes >> 4), dBk + (n % na) * (4096 >> 4),
@@ -604,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
     if (lane == 0) {
       tc::commit(&bars[kMmaDone]);  // never leave with MMAs in flight
-      mbar_wait(&bars[kMmaDone], 0, a.status);
+      mbar_wait_s(&bars[kMmaDone], 0, a.status);
     }
     __syncwarp();
   } else if (warp == kScoreWarp) {
@@ -627,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (k > 0) {  // every S of the previous unit is done with Q^T
         if (lane == 0) {
           tc::commit(&bars[kSUnit]);
-          ok = mbar_wait(&bars[kSUnit], (k - 1) & 1, a.status);
+          ok = mbar_wait_s(&bars[kSUnit], (k - 1) & 1, a.status);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -658,8 +672,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         for (int n = 0; n < N && ok; ++n) {
           const int m = gn + n;
           const int kr = m & 1, sr = m % kSRing, sp = (m / kSRing) & 1;  // ring slots of step m
-          ok = mbar_wait(&bars[kKFFull0 + kr], (m >> 1) & 1, a.status) &&
-               (m < kSRing || mbar_wait(&bars[kSFree0 + sr], sp ^ 1, a.status));
+          ok = mbar_wait_s(&bars[kKFFull0 + kr], (m >> 1) & 1, a.status) &&
+               (m < kSRing || mbar_wait_s(&bars[kSFree0 + sr], sp ^ 1, a.status));
           if (!ok) break;
           tc::fence_after();
           const uint32_t q = kOffQ + (n % na) * 2048;  // the two 64-column halves of Q^T at q, q + 1024
@@ -678,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     }
     if (lane == 0) {
       tc::commit(&bars[kSDone]);
-      mbar_wait(&bars[kSDone], 0, a.status);
+      mbar_wait_s(&bars[kSDone], 0, a.status);
     }
     __syncwarp();
   } else if (warp < kSoftWarp0) {
@@ -725,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
               rp[cc][2 * uu] = __ldg(reinterpret_cast<const uint4*>(rrow + un * 512));
               rp[cc][2 * uu + 1] = __ldg(reinterpret_cast<const uint4*>(rrow + un * 512 + 16));
             }
-          ok = mbar_wait(&bars[kKFull0 + stage], (g >> 1) & 1, a.status);
+          ok = mbar_wait_s(&bars[kKFull0 + stage], (g >> 1) & 1, a.status);
           if (!ok) break;
         }
         // U of this step, read out at once (as bf16 pairs) so that its buffer frees early
@@ -831,11 +845,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const uint32_t idV = tc::idesc_bf16(128, na > 2 ? 32 : 16, 1, 1);
         const uint64_t dR =
             tc::smem_desc(sBase + kOffVr + (4 - na) * kResSlotBytes, kResSlotBytes, 256, tc::kSwizzle32B);
-        if (k > 0) ok = mbar_wait(&bars[kEpiDone], (k - 1) & 1, a.status);
+        if (k > 0) ok = mbar_wait_s(&bars[kEpiDone], (k - 1) & 1, a.status);
         for (int b = 0; b < nb && ok; ++b) {
           const int g = gb + b;
-          ok = mbar_wait(&bars[kVFull0 + (g & 1)], (g >> 1) & 1, a.status) &&
-               mbar_wait(&bars[kPFull0 + (g & 1)], (g >> 1) & 1, a.status);
+          ok = mbar_wait_s(&bars[kVFull0 + (g & 1)], (g >> 1) & 1, a.status) &&
+               mbar_wait_s(&bars[kPFull0 + (g & 1)], (g >> 1) & 1, a.status);
           if (!ok) break;
           tc::fence_after();
           const int nvp = min(kBlockPages, p1 - (p0 + b * kBlockPages));
@@ -855,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         gb += nb;
       }
       tc::commit(&bars[kValDone]);
-      mbar_wait(&bars[kValDone], 0, a.status);
+      mbar_wait_s(&bars[kValDone], 0, a.status);
     }
     __syncwarp();
   } else {
@@ -926,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           mr[q] = mref[ai * 8 + q];
           ps[q] = (vis && q < G) ? ex2(sc[q] - (mr[q] == -INFINITY ? 0.f : mr[q])) : 0.f;
         }
-        ok = mbar_wait(&bars[kRed0 + (m & 1)], (m >> 1) & 1, a.status);
+        ok = mbar_wait_s(&bars[kRed0 + (m & 1)], (m >> 1) & 1, a.status);
         if (!ok) break;
         // lazy rescale: keep the reference maximum unless the block maximum passes it by 2^8
         float alpha[kG];
@@ -951,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           if (b > 0) {
             // O^T and R are stable once the value products of block g - 1 are done (one barrier
             // per block parity, so a wait is never more than one phase ahead of the barrier)
-            ok = mbar_wait(&bars[kODone0 + ((g - 1) & 1)], ((g - 1) >> 1) & 1, a.status);
+            ok = mbar_wait_s(&bars[kODone0 + ((g - 1) & 1)], ((g - 1) >> 1) & 1, a.status);
             if (!ok) break;
             tc::fence_after();
             uint32_t ov[kG], rv[kG];
@@ -982,7 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         uint32_t pw[4] = {0u, 0u, 0u, 0u};  // P^T[key][g] in bf16, zero past G or for masked keys
 #pragma unroll
         for (int q2 = 0; q2 < kG / 2; ++q2) pw[q2] = pack_bf16(ps[2 * q2], ps[2 * q2 + 1]);
-        if (ai == 0 && g >= 2) ok = mbar_wait(&bars[kPFree0 + (g & 1)], ((g >> 1) - 1) & 1, a.status);
+        if (ai == 0 && g >= 2) ok = mbar_wait_s(&bars[kPFree0 + (g & 1)], ((g >> 1) - 1) & 1, a.status);
         if (!ok) break;
         // P^T of agent ai: columns 8 ai .. 8 ai + 7 = atom ai / 2, 16-byte chunk ai % 2 of each row
         uint8_t* pbuf = smem + kOffP + (g & 1) * 8192 + (ai >> 1) * 4096;
@@ -996,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (!ok) break;
       // epilogue: one partial (m, l, acc, acc_r) per (agent, head) of the unit
       const int glast = gb + nb - 1;
-      if (nb > 0) ok = mbar_wait(&bars[kODone0 + (glast & 1)], (glast >> 1) & 1, a.status);
+      if (nb > 0) ok = mbar_wait_s(&bars[kODone0 + (glast & 1)], (glast >> 1) & 1, a.status);
       tc::fence_after();
       if (slot_base >= 0) {
         for (int ai = 0; ai < na; ++ai) {
