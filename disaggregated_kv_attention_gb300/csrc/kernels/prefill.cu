@@ -18,17 +18,19 @@
 //                 U = Kr . B_k^T arrives in TMEM; K = bf16(Kb + RoPE_j(U)) replaces
 //                 Kb in place in the stage, which the score MMA then reads
 //          10..17 softmax group, two warps per query row (half of the keys each):
-//                 S from TMEM, causal mask, online softmax; P (bf16) to shared
-//                 memory as the A operand of the value products
+//                 S from TMEM, causal mask, online softmax; P (bf16) back into the
+//                 block's TMEM buffer, over the S it came from, as the A operand of
+//                 the value products
 //   MMAs per block:  U[128x128]   = Kr[128x16] . B_k^T           (smem x smem)
 //                    S[128x128]   = Q[128x128] . K^T             (smem x smem)
-//                    O[128x128]  += P[128x128] . Vb[128x128]      (smem x smem)
-//                    O_r[128x16] += P . Vr[128x16]                (smem x smem)
-//   U and S of a block share one of two TMEM buffers (by block parity), freed
-//   as soon as the softmax has read S, so the next blocks' U, rotation and S
-//   run while this block's softmax does; a K stage is released by the commit of
-//   its score MMA, so the rotation of block b + 1 overlaps the score product of
-//   block b.  The MMA warp issues whichever product is ready first.
+//                    O[128x128]  += P[128x128] . Vb[128x128]      (tmem x smem)
+//                    O_r[128x16] += P . Vr[128x16]                (tmem x smem)
+//   U, S and P of a block share one of two TMEM buffers (by block parity); U of
+//   block b + 2 goes into the buffer once the value products of block b (the
+//   last readers of its P) are done.  The next blocks' U, rotation and S run while this
+//   block's softmax does; a K stage (a ring of three) is released by the commit
+//   of its score MMA, so the rotation of block b + 1 overlaps the score product
+//   of block b.  The MMA warp issues whichever product is ready first.
 //   epilogue: out = (O + O_r . B_v[:, hD:(h+1)D]) / l, B_v applied once per row.
 // Every wait is on an mbarrier with a bounded spin; a timeout sets the device
 // status word instead of hanging.
@@ -53,28 +55,29 @@ constexpr int kThreads = (kSoftWarp0 + 8) * 32;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int kOffPmax = 1024;                  // [2 parities][2 halves][128 rows] partial row maxima
-constexpr int kKStages = 2, kVStages = 3;  // ring depths (at most 3 each)
+constexpr int kKStages = 3, kVStages = 3;  // ring depths (at most 3 each)
 // K stages: [the block's keys, K-major 128B-swizzled [2 halves][128 rows][128 B] | 8 k_res tiles];
 // key 16 p + t of the block is row t of its page p, so half hh of page p's tile lands at
 // hh * 16384 + p * 2048 and the swizzle (on row % 8 == t % 8) carries over unchanged
 constexpr int kOffKStage = 3072;
 constexpr int kOffVStage = kOffKStage + kKStages * 36864;  // V stages of [8 V tiles | 8 v_res tiles]
 constexpr int kStageBytes = 36864, kStRes = 32768;  // the residual tiles follow the base tiles
-constexpr int kOffP = kOffVStage + kVStages * kStageBytes;  // P, K-major 128B-swizzled [2][128 rows][128 B]
-constexpr int kOffBk = kOffP + 32768;                // B_k^T, K-major 32B-swizzled [128 d][16 r]
-constexpr int kOffBv = kOffBk + 4096;                // B_v slice [16][128] bf16
-constexpr int kSmemBytes = kOffBv + 4096 + 1024;     // + slack for aligning the base
+constexpr int kOffBk = kOffVStage + kVStages * kStageBytes;  // B_k^T, K-major 32B-swizzled [128 d][16 r]
+constexpr int kOffBv = kOffBk + 4096;                         // B_v slice [16][128] bf16
+constexpr int kSmemBytes = kOffBv + 4096;  // the dynamic window is 1024-byte aligned (checked)
 static_assert(kSmemBytes <= 227 * 1024, "more shared memory than a CTA may have");
 
-// tensor memory columns: two buffers (U, then S) by block parity, O, O_r
-// and Q (bf16 pairs: the A operand of the score product)
+// tensor memory columns: two buffers (U, then S, then P over S) by block parity, O, O_r
+// and Q (bf16 pairs: the A operand of the score product).  P of the keys 64 sh .. 64 sh + 63
+// (bf16 pairs) sits at columns 64 sh .. 64 sh + 31 of its buffer, under the S columns that the
+// softmax warps of half sh themselves read.
 constexpr uint32_t kTmBuf = 0, kTmO = 256, kTmOr = 384, kTmQ = 400, kTmCols = 512;
 
 // mbarrier indices
 enum { kKFull0, kKFull1, kKFull2, kKEmpty0, kKEmpty1, kKEmpty2, kVFull0, kVFull1, kVFull2, kVEmpty0, kVEmpty1, kVEmpty2,
        kUFull0, kUFull1,
        kKFReady0, kKFReady1, kKFReady2, kSFull0, kSFull1,
-       kSFree0, kSFree1, kPFull, kPVDone, kQReady, kBkReady, kMmaDone, kNumBars };
+       kPFull0, kPFull1, kPVDone0, kPVDone1, kQReady, kBkReady, kMmaDone, kNumBars };
 static_assert(kNumBars * 8 <= 256, "barriers overlap the state that follows them");
 
 // Bytes of nvp page tiles whose last page keeps only `rows` rows.
@@ -146,8 +149,11 @@ struct PrefillArgs {
 
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023) {  // swizzled operand tiles need a 1024-byte aligned window
+    if (threadIdx.x == 0) flag_status(a.status, kDevBadArg);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 256);
   int32_t* s_meta = reinterpret_cast<int32_t*>(smem + 272);
@@ -187,10 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bars[kUFull1], 1);
     mbar_init(&bars[kSFull0], 1);
     mbar_init(&bars[kSFull1], 1);
-    mbar_init(&bars[kSFree0], 8);  // every softmax warp, once its last read of S is done
-    mbar_init(&bars[kSFree1], 8);
-    mbar_init(&bars[kPFull], 8);  // every softmax warp
-    mbar_init(&bars[kPVDone], 1);
+    // P written, by block parity (the softmax may write P of block b + 1 before the value
+    // products of block b are issued, so one barrier could run two phases ahead of its waiter)
+    mbar_init(&bars[kPFull0], 8);  // every softmax warp
+    mbar_init(&bars[kPFull1], 8);
+    mbar_init(&bars[kPVDone0], 1);  // the commit after the value products of an even block
+    mbar_init(&bars[kPVDone1], 1);  // of an odd block
     mbar_init(&bars[kQReady], 8);
     mbar_init(&bars[kBkReady], kRopeWarps);
     mbar_init(&bars[kMmaDone], 1);
@@ -219,7 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int32_t key_limit = s_meta[0];
   const int n_pages = (key_limit + kPage - 1) / kPage;
   const int n_blocks = (n_pages + kBlockPages - 1) / kBlockPages;
-  uint8_t* sP = smem + kOffP;
   uint8_t* sBk = smem + kOffBk;
   uint8_t* sBv = smem + kOffBv;
 
@@ -390,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // Issues, whichever is ready first (scores first: the softmax waits on them and the value
     // products of the previous block need only be done before the next P is written; then the
     // value products, then U):
-    //   U(b)  into buffer b % 2 once block b's K stage is in and the softmax has read S(b - 2);
+    //   U(b)  into buffer b % 2 once block b's K stage is in and P.V(b - 2), the last reader of
+    //         that buffer, is done;
     //   S(b)  over U(b) once the rotation group has built K(b) in its stage (whose commit then
     //         frees the stage for block b + 3);
     //   P.V(b) once the softmax has written P(b) and block b's V stage is in.
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const uint32_t idS = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idPV = tc::idesc_bf16(128, 128, 0, 1);
       const uint32_t idPVr = tc::idesc_bf16(128, 16, 0, 1);
-      const uint32_t aK = smem_u32(smem + kOffKStage), aBk = smem_u32(sBk), aP = smem_u32(sP);
+      const uint32_t aK = smem_u32(smem + kOffKStage), aBk = smem_u32(sBk);
       bool ok = mbar_wait(&bars[kQReady], 0, a.status) && mbar_wait(&bars[kBkReady], 0, a.status);
       int iu = 0, is = 0, ip = 0;  // next U, S and P.V to issue
       uint32_t idle = 0;
@@ -419,23 +427,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           ++is;
           did = true;
         }
-        if (ip < is && mbar_test(&bars[kPFull], ip & 1) && mbar_test(&bars[kVFull0 + ip % kVStages], (ip / kVStages) & 1)) {
+        if (ip < is && mbar_test(&bars[kPFull0 + (ip & 1)], (ip >> 1) & 1) &&
+            mbar_test(&bars[kVFull0 + ip % kVStages], (ip / kVStages) & 1)) {
           tc::fence_after();
           const uint32_t aV = smem_u32(smem + kOffVStage + (ip % kVStages) * kStageBytes);
           const int nvp = min(kBlockPages, n_pages - ip * kBlockPages);
-          for (int ks = 0; ks < nvp; ++ks)  // 16 keys per step: 32 bytes of P's rows, one V tile
-            tc::mma_ss(tm + kTmO, tc::smem_desc(aP + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
+          // P of keys 16 ks .. 16 ks + 15: 8 columns of the block's buffer (keys 64 .. at column 64)
+          const uint32_t pb = tm + kTmBuf + 128 * (ip & 1);
+          for (int ks = 0; ks < nvp; ++ks)  // 16 keys per step: one V tile
+            tc::mma_ts(tm + kTmO, pb + (ks >> 2) * 64 + (ks & 3) * 8,
                        tc::smem_desc(aV + ks * kBaseTile, 2048, 1024, tc::kSwizzle128B), idPV, (ip > 0 || ks > 0));
           for (int ks = 0; ks < nvp; ++ks)
-            tc::mma_ss(tm + kTmOr, tc::smem_desc(aP + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, tc::kSwizzle128B),
+            tc::mma_ts(tm + kTmOr, pb + (ks >> 2) * 64 + (ks & 3) * 8,
                        tc::smem_desc(aV + kStRes + ks * kResTile, 4096, 256, tc::kSwizzle32B), idPVr, (ip > 0 || ks > 0));
-          tc::commit(&bars[kPVDone]);
+          tc::commit(&bars[kPVDone0 + (ip & 1)]);
           tc::commit(&bars[kVEmpty0 + ip % kVStages]);
           ++ip;
           did = true;
         }
         if (iu < n_blocks && iu - is < 2 && mbar_test(&bars[kKFull0 + iu % kKStages], (iu / kKStages) & 1) &&
-            (iu < 2 || mbar_test(&bars[kSFree0 + (iu & 1)], ((iu >> 1) - 1) & 1))) {
+            (iu < 2 || (ip + 2 > iu && mbar_test(&bars[kPVDone0 + (iu & 1)], ((iu >> 1) - 1) & 1)))) {
           tc::fence_after();
           const uint32_t st = aK + (iu % kKStages) * kStageBytes;
           tc::mma_ss(tm + kTmBuf + 128 * (iu & 1), tc::smem_desc(st + kStRes, 16, 256, tc::kSwizzle32B),
@@ -453,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           }
           // sleep on the event due first
           if (ip < is)
-            mbar_try_wait_for(&bars[kPFull], ip & 1, 200);
+            mbar_try_wait_for(&bars[kPFull0 + (ip & 1)], (ip >> 1) & 1, 200);
           else if (is < iu)
             mbar_try_wait_for(&bars[kKFReady0 + is % kKStages], (is / kKStages) & 1, 200);
           else
@@ -625,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const float alpha = (need && m != -INFINITY) ? exp2f(m - mn) : 1.f;
         if (b > 0) {
           // O (this half's columns; the first half also O_r) is stable once P.V of block b - 1 is done
-          ok = ok && mbar_wait(&bars[kPVDone], (b - 1) & 1, a.status);
+          ok = ok && mbar_wait(&bars[kPVDone0 + ((b - 1) & 1)], ((b - 1) >> 1) & 1, a.status);
           tc::fence_after();
 #pragma unroll
           for (int c = 0; c < 64 + 16; c += 16) {
@@ -685,22 +696,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         f2_split(ls2[1], l2, l3);
         l += (l0 + l1) + (l2 + l3);
       }
-      // S of this block is read: its buffer may take U of block b + 2
+      // P of this half's keys (bf16 pairs) into the block's buffer over the S columns this half
+      // has read (the buffer's previous P, of block b - 2, was done with before U(b) went in)
+      tc::st16(tl + buf + 64 * sh, pw);
+      tc::st16(tl + buf + 64 * sh + 16, pw + 16);
+      tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kSFree0 + (b & 1)]);
-      // P to shared memory once the value products of block b - 1 are done with the previous P
-      if (b > 0) ok = ok && mbar_wait(&bars[kPVDone], (b - 1) & 1, a.status);
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        *reinterpret_cast<uint4*>(sP + tc::sw128_off(128, qr, 64 * sh + 8 * c8)) =
-            make_uint4(pw[4 * c8], pw[4 * c8 + 1], pw[4 * c8 + 2], pw[4 * c8 + 3]);
-      tc::fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kPFull]);
+      if (lane == 0) mbar_arrive(&bars[kPFull0 + (b & 1)]);
     }
     // epilogue: the row sum of both halves, then this half's output columns
-    if (ok && n_blocks > 0) ok = mbar_wait(&bars[kPVDone], (n_blocks - 1) & 1, a.status);
+    if (ok && n_blocks > 0) ok = mbar_wait(&bars[kPVDone0 + ((n_blocks - 1) & 1)], ((n_blocks - 1) >> 1) & 1, a.status);
     if (ok) ok = mbar_wait(&bars[kQReady], 0, a.status);  // every thread's part of the B_v slice is in place
     named_sync(pair_bar, pair_threads);  // both halves are past their last use of s_pmax
     s_pmax[sh * 128 + qr] = l;
