@@ -193,8 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bars[kUFull1], 1);
     mbar_init(&bars[kSFull0], 1);
     mbar_init(&bars[kSFull1], 1);
-    // P written, by block parity (the softmax may write P of block b + 1 before the value
-    // products of block b are issued, so one barrier could run two phases ahead of its waiter)
+    // P written, by block parity: a softmax warp may write P of block b + 1 before a slower one
+    // has written P of block b, and on a single barrier its arrival would complete block b's
+    // phase early; it cannot reach block b + 2 before block b's value products are done
     mbar_init(&bars[kPFull0], 8);  // every softmax warp
     mbar_init(&bars[kPFull1], 8);
     mbar_init(&bars[kPVDone0], 1);  // the commit after the value products of an even block
