@@ -600,20 +600,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       }
       tc::fence_proxy_async();
       __syncwarp();
-      if (lane == 0) {
-        for (int n = 0; n < N && ok; ++n) {
-          const int m = gn + n;
-          ok = mbar_wait_s(&bars[kKrFull0 + (m & 3)], (m >> 2) & 1, a.status) &&
-               (m < 2 || mbar_wait_s(&bars[kUFree0 + (m & 1)], ((m >> 1) - 1) & 1, a.status));
-          if (!ok) break;
-          tc::fence_after();
-          tc::mma_ss(tm + kTmU + 128 * (m & 1), dKr + (m & 3) * (kResSlotBytes >> 4), dBk + (n % na) * (4096 >> 4),
-                     idU, 0);
+      for (int n = 0, ai = 0; n < N && ok; ++n) {
+        const int m = gn + n;
+        ok = mbar_wait_s(&bars[kKrFull0 + (m & 3)], (m >> 2) & 1, a.status) &&
+             (m < 2 || mbar_wait_s(&bars[kUFree0 + (m & 1)], ((m >> 1) - 1) & 1, a.status));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc::fence_after();
+        const uint64_t dk = dKr + (m & 3) * (kResSlotBytes >> 4), db = dBk + ai * (4096 >> 4);
+        const uint32_t du = tm + kTmU + 128 * (m & 1);
+        if (tc::elect_one()) {
+          tc::mma_ss(du, dk, db, idU, 0);
           tc::commit(&bars[kUFull0 + (m & 1)]);
           tc::commit(&bars[kKrEmpty0 + (m & 3)]);
         }
+        __syncwarp();
+        if (++ai == na) ai = 0;
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       gn += N;
     }
     if (lane == 0) {
@@ -668,26 +671,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         }
       tc::fence_proxy_async();
       __syncwarp();
-      if (lane == 0) {
-        for (int n = 0; n < N && ok; ++n) {
-          const int m = gn + n;
-          const int kr = m & 1, sr = m % kSRing, sp = (m / kSRing) & 1;  // ring slots of step m
-          ok = mbar_wait_s(&bars[kKFFull0 + kr], (m >> 1) & 1, a.status) &&
-               (m < kSRing || mbar_wait_s(&bars[kSFree0 + sr], sp ^ 1, a.status));
-          if (!ok) break;
-          tc::fence_after();
-          const uint32_t q = kOffQ + (n % na) * 2048;  // the two 64-column halves of Q^T at q, q + 1024
-          const uint64_t dq0 = tc::smem_desc(sBase + q, 16, kOffQZero - q, tc::kSwizzle128B);
-          const uint64_t dq1 = tc::smem_desc(sBase + q + 1024, 16, kOffQZero - q - 1024, tc::kSwizzle128B);
-          const uint32_t dS = tm + kTmS + 16 * sr, aK = tm + kTmKF + 64 * kr;
+      int sr = gn % kSRing, sp = (gn / kSRing) & 1;  // S ring slot and its phase of step gn
+      for (int n = 0, ai = 0; n < N && ok; ++n) {
+        const int m = gn + n;
+        const int kr = m & 1;
+        ok = mbar_wait_s(&bars[kKFFull0 + kr], (m >> 1) & 1, a.status) &&
+             (m < kSRing || mbar_wait_s(&bars[kSFree0 + sr], sp ^ 1, a.status));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc::fence_after();
+        const uint32_t q = kOffQ + ai * 2048;  // the two 64-column halves of Q^T at q, q + 1024
+        const uint64_t dq0 = tc::smem_desc(sBase + q, 16, kOffQZero - q, tc::kSwizzle128B);
+        const uint64_t dq1 = tc::smem_desc(sBase + q + 1024, 16, kOffQZero - q - 1024, tc::kSwizzle128B);
+        const uint32_t dS = tm + kTmS + 16 * sr, aK = tm + kTmKF + 64 * kr;
+        if (tc::elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // K = 16 per step: 8 TMEM columns of A, 32 bytes of B
             tc::mma_ts(dS, aK + 8 * ks, (ks < 4 ? dq0 : dq1) + 2 * (ks & 3), idS, ks > 0);
           tc::commit(&bars[kSFull0 + sr]);
           tc::commit(&bars[kKFFree0 + kr]);
         }
+        __syncwarp();
+        if (++ai == na) ai = 0;
+        if (++sr == kSRing) {
+          sr = 0;
+          sp ^= 1;
+        }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       gn += N;
     }
     if (lane == 0) {
@@ -719,8 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       if (end) break;
       const int32_t hend = (hc0 >> 4) + (hc0 & 15), hn0 = hc0 & 15;
       const int N = blocks_of(p0, p1) * na;
-      for (int n = 0; n < N && ok; ++n) {
-        const int b = n / na, ai = n - b * na;
+      for (int n = 0, b = 0, ai = 0; n < N && ok; ++n, ai = ai + 1 == na ? 0 : ai + 1, b += ai == 0) {
         const int g = gb + b, m = gn + n;  // global block and step
         const int stage = g & 1;
         const int pbase = p0 + b * kBlockPages;
@@ -829,33 +838,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     // hold l[g] = sum over keys of P for every agent; the other cells are cross terms,
     // never read.  A unit's first block overwrites O and R once the epilogue of the
     // previous unit has read them.
-    if (lane == 0) {
-      const uint32_t sBase = smem_u32(smem);
-      const uint64_t dV = tc::smem_desc(sBase + kOffV, 2048, 1024, tc::kSwizzle128B);
-      const uint64_t dP = tc::smem_desc(sBase + kOffP, 4096, 256, tc::kSwizzle32B);
-      int gb = 0;
-      bool ok = true;
-      for (int k = 0; ok; ++k) {
-        if (!unit_wait(k)) break;
-        const int32_t p0 = unit_at(k, kUfP0), p1 = unit_at(k, kUfP1), na = unit_at(k, kUfNa);
-        const bool end = unit_at(k, kUfEnd) != 0;
-        mbar_arrive(&bars[kUnitFree0 + (k & 1)]);
-        if (end) break;
-        const int nb = blocks_of(p0, p1);
-        const uint32_t idV = tc::idesc_bf16(128, na > 2 ? 32 : 16, 1, 1);
-        const uint64_t dR =
-            tc::smem_desc(sBase + kOffVr + (4 - na) * kResSlotBytes, kResSlotBytes, 256, tc::kSwizzle32B);
-        if (k > 0) ok = mbar_wait_s(&bars[kEpiDone], (k - 1) & 1, a.status);
-        for (int b = 0; b < nb && ok; ++b) {
-          const int g = gb + b;
-          ok = mbar_wait_s(&bars[kVFull0 + (g & 1)], (g >> 1) & 1, a.status) &&
-               mbar_wait_s(&bars[kPFull0 + (g & 1)], (g >> 1) & 1, a.status);
-          if (!ok) break;
-          tc::fence_after();
-          const int nvp = min(kBlockPages, p1 - (p0 + b * kBlockPages));
-          const uint64_t dv = dV + (g & 1) * (kBlockTiles >> 4), dp = dP + (g & 1) * (8192 >> 4);
-          const uint64_t dr = dR + (g & 1) * (kVrGroupBytes >> 4);  // 8 atoms of 16 rows, 4 KB apart
-          const uint32_t acc0 = b > 0;
+    const uint32_t sBase = smem_u32(smem);
+    const uint64_t dV = tc::smem_desc(sBase + kOffV, 2048, 1024, tc::kSwizzle128B);
+    const uint64_t dP = tc::smem_desc(sBase + kOffP, 4096, 256, tc::kSwizzle32B);
+    int gb = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      if (!unit_wait(k)) break;
+      const int32_t p0 = unit_at(k, kUfP0), p1 = unit_at(k, kUfP1), na = unit_at(k, kUfNa);
+      const bool end = unit_at(k, kUfEnd) != 0;
+      unit_release(k);
+      if (end) break;
+      const int nb = blocks_of(p0, p1);
+      const uint32_t idV = tc::idesc_bf16(128, na > 2 ? 32 : 16, 1, 1);
+      const uint64_t dR =
+          tc::smem_desc(sBase + kOffVr + (4 - na) * kResSlotBytes, kResSlotBytes, 256, tc::kSwizzle32B);
+      if (k > 0) ok = __all_sync(0xffffffffu, mbar_wait_s(&bars[kEpiDone], (k - 1) & 1, a.status));
+      for (int b = 0; b < nb && ok; ++b) {
+        const int g = gb + b;
+        ok = mbar_wait_s(&bars[kVFull0 + (g & 1)], (g >> 1) & 1, a.status) &&
+             mbar_wait_s(&bars[kPFull0 + (g & 1)], (g >> 1) & 1, a.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc::fence_after();
+        const int nvp = min(kBlockPages, p1 - (p0 + b * kBlockPages));
+        const uint64_t dv = dV + (g & 1) * (kBlockTiles >> 4), dp = dP + (g & 1) * (8192 >> 4);
+        const uint64_t dr = dR + (g & 1) * (kVrGroupBytes >> 4);  // 8 atoms of 16 rows, 4 KB apart
+        const uint32_t acc0 = b > 0;
+        if (tc::elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < kBlockPages; ++ks)  // one page (16 keys) per step
             if (ks < nvp) tc::mma_ss(tm + kTmO, dv + ks * (kBaseTile >> 4), dp + ks * (512 >> 4), idV, acc0 | (ks > 0));
@@ -866,8 +876,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           tc::commit(&bars[kODone0 + (g & 1)]);
           tc::commit(&bars[kVEmpty0 + (g & 1)]);
         }
-        gb += nb;
+        __syncwarp();
       }
+      gb += nb;
+    }
+    if (tc::elect_one()) {
       tc::commit(&bars[kValDone]);
       mbar_wait_s(&bars[kValDone], 0, a.status);
     }
@@ -900,8 +913,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       unit_release(k);
       if (end) break;
       const int nb = blocks_of(p0, p1), N = nb * na;
-      for (int n = 0; n < N && ok; ++n) {
-        const int b = n / na, ai = n - b * na;
+      int sr = gn % kSRing, sp = (gn / kSRing) & 1;  // S ring slot and its phase of step gn
+      for (int n = 0, b = 0, ai = 0; n < N && ok;
+           ++n, ai = ai + 1 == na ? 0 : ai + 1, b += ai == 0, sp ^= sr + 1 == kSRing, sr = sr + 1 == kSRing ? 0 : sr + 1) {
         const int g = gb + b, m = gn + n;  // global block and step
         const int pbase = p0 + b * kBlockPages;
         const int j = pbase * kPage + row;
@@ -911,8 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const bool in_hole = hn != 0 && j >= hs && j < hs + hn;
         const int32_t kp = (hn != 0 && j >= hs + hn) ? j - hn : j;
         const bool vis = j < L && !in_hole && kp <= pos && j < p1 * kPage;
-        const int sr = m % kSRing;
-        ok = mbar_wait_tc(&bars[kSFull0 + sr], (m / kSRing) & 1, a.status);
+        ok = mbar_wait_tc(&bars[kSFull0 + sr], sp, a.status);
         if (!ok) break;
         tc::fence_after();
         uint32_t sv[kG];

@@ -88,9 +88,8 @@ __global__ void __launch_bounds__(kFillThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
-      for (int kc = 0; kc < a.n_kchunks && ok; ++kc) {
-        const int s = kc % S;
-        if (kc >= S) ok = mbar_wait(&bars[S + s], (kc / S - 1) & 1, a.status);
+      for (int kc = 0, s = 0, ph = 0; kc < a.n_kchunks && ok; ++kc, ph ^= s + 1 == S, s = s + 1 == S ? 0 : s + 1) {
+        if (kc >= S) ok = mbar_wait(&bars[S + s], ph ^ 1, a.status);
         if (!ok) break;
         uint8_t* st = smem + s * stage_bytes;
         mbar_arrive_expect_tx(&bars[s], stage_bytes);
@@ -106,24 +105,29 @@ __global__ void __launch_bounds__(kFillThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16(kFillM, a.nc, 0, 0);
-      bool ok = true;
-      for (int kc = 0; kc < a.n_kchunks && ok; ++kc) {
-        const int s = kc % S;
-        ok = mbar_wait(&bars[s], (kc / S) & 1, a.status);
-        if (!ok) break;
-        tc::fence_after();
-        const uint32_t ax = smem_u32(smem + s * stage_bytes), aw = ax + xbytes;
+    // the whole warp runs the loop; one elected lane issues the MMAs and commits
+    const uint32_t idesc = tc::idesc_bf16(kFillM, a.nc, 0, 0);
+    bool ok = true;
+    for (int kc = 0, s = 0, ph = 0; kc < a.n_kchunks && ok; ++kc) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars[s], ph, a.status));
+      if (!ok) break;
+      tc::fence_after();
+      const uint32_t ax = smem_u32(smem + s * stage_bytes), aw = ax + xbytes;
+      const uint64_t dx = tc::smem_desc(ax, 16, 1024, tc::kSwizzle128B), dw = tc::smem_desc(aw, 16, 1024, tc::kSwizzle128B);
+      if (tc::elect_one()) {
 #pragma unroll
         for (int ks = 0; ks < kKB * kFillK / 16; ++ks)  // 16 hidden elements per MMA, 4 per box
-          tc::mma_ss(tm, tc::smem_desc(ax + (ks >> 2) * xbox + 32 * (ks & 3), 16, 1024, tc::kSwizzle128B),
-                     tc::smem_desc(aw + (ks >> 2) * wbox + 32 * (ks & 3), 16, 1024, tc::kSwizzle128B), idesc,
-                     (kc > 0 || ks > 0));
+          tc::mma_ss(tm, dx + (((ks >> 2) * xbox + 32 * (ks & 3)) >> 4), dw + (((ks >> 2) * wbox + 32 * (ks & 3)) >> 4),
+                     idesc, (kc > 0 || ks > 0));
         tc::commit(&bars[S + s]);
       }
-      tc::commit(&bars[2 * S]);  // the accumulator is final (or the loop gave up: nothing pending)
+      __syncwarp();
+      if (++s == S) {
+        s = 0;
+        ph ^= 1;
+      }
     }
+    if (tc::elect_one()) tc::commit(&bars[2 * S]);  // the accumulator is final (or the loop gave up: nothing pending)
     __syncwarp();
   } else if (warp >= 4) {
     const int q4 = warp & 3;
