@@ -938,11 +938,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         float sc[kG];
 #pragma unroll
         for (int q = 0; q < kG; ++q) sc[q] = (vis && q < G) ? __uint_as_float(sv[q]) * a.scale_log2 : -INFINITY;
+        // max over the warp's keys of each query head, stored by one lane as float4s
         float* red = s_red + (m & 1) * 32;
+        {
+          float wq[kG];
 #pragma unroll
-        for (int q = 0; q < kG; ++q) {  // max over the warp's keys of each query head
-          const float wq = warp_max(sc[q]);
-          if (lane == q) red[sw_ * kG + q] = wq;
+          for (int q = 0; q < kG; ++q) wq[q] = warp_max(sc[q]);
+          if (lane == 0) {
+            float4* r4 = reinterpret_cast<float4*>(red + sw_ * kG);
+            r4[0] = make_float4(wq[0], wq[1], wq[2], wq[3]);
+            if constexpr (kG == 8) r4[1] = make_float4(wq[4 % kG], wq[5 % kG], wq[6 % kG], wq[7 % kG]);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kRed0 + (m & 1)]);
@@ -956,17 +962,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         ok = mbar_wait_s(&bars[kRed0 + (m & 1)], (m >> 1) & 1, a.status);
         if (!ok) break;
         // lazy rescale: keep the reference maximum unless the block maximum passes it by 2^8
-        float alpha[kG];
+        float bm[kG];
         bool need_any = false;
+        {
+          float4 x[4][2];  // the four warps' maxima, read as float4s
 #pragma unroll
-        for (int q = 0; q < kG; ++q) {
-          const float bm = fmaxf(fmaxf(red[q], red[kG + q]), fmaxf(red[2 * kG + q], red[3 * kG + q]));
-          const bool need = q < G && bm > mr[q] + 8.f;
-          need_any |= need;
-          alpha[q] = (need && mr[q] != -INFINITY) ? ex2(mr[q] - bm) : 1.f;
-          if (need) mr[q] = bm;
+          for (int w = 0; w < 4; ++w) {
+            x[w][0] = reinterpret_cast<const float4*>(red + w * kG)[0];
+            if constexpr (kG == 8) x[w][1] = reinterpret_cast<const float4*>(red + w * kG)[1];
+          }
+#pragma unroll
+          for (int q = 0; q < kG; ++q) {
+            float v[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const float4 y = x[w][q >> 2];
+              v[w] = (q & 3) == 0 ? y.x : (q & 3) == 1 ? y.y : (q & 3) == 2 ? y.z : y.w;
+            }
+            bm[q] = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
+            need_any |= q < G && bm[q] > mr[q] + 8.f;
+          }
         }
         if (need_any) {  // uniform across the group: every warp saw the same maxima
+          float alpha[kG];
+#pragma unroll
+          for (int q = 0; q < kG; ++q) {
+            const bool need = q < G && bm[q] > mr[q] + 8.f;
+            alpha[q] = (need && mr[q] != -INFINITY) ? ex2(mr[q] - bm[q]) : 1.f;
+            if (need) mr[q] = bm[q];
+          }
           float ml = mr[0];
 #pragma unroll
           for (int q = 1; q < kG; ++q)
