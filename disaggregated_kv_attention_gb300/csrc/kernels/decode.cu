@@ -15,8 +15,8 @@
 //                 separately, each agent's residual k/v tiles into a 4-slot ring;
 //                 1-D bulk async copies, one per run of consecutive page ids,
 //                 completing on mbarriers
-//     warp 1      allocates tensor memory; stages B_k of the unit's head and one
-//                 lane issues, per (block, agent):
+//     warp 1      allocates tensor memory; stages B_k of the unit's head and
+//                 issues, per (block, agent):
 //                   U    = Kr . B_k                 [128 keys x 128]  smem x smem
 //     warp 15     stages Q of the unit's agents and issues, per (block, agent):
 //                   S    = K . Q^T                  [128 keys x 16]   K from TMEM
@@ -29,14 +29,16 @@
 //                 maxima across the group, lazy rescale of O (only when the
 //                 running maximum grows by 2^8), P^T to shared memory; at the end
 //                 of a unit one partial (m, l, acc, acc_r) per (agent, KV head)
-//     warp 14     one lane issues, per block and for all its agents at once,
+//     warp 14     issues, per block and for all its agents at once,
 //                   O^T += Vb^T . P^T  and  R += Vr^T . P^T (rank-16 value path)
 //                 and l as the product of a tile of ones with P^T.
 //   combine       one CTA per (agent, KV head, query head): log-sum-exp merge of
 //                 the partials, then out = (acc + acc_r . B_v[:, hD:(h+1)D]) / l,
 //                 B_v applied once per query head.
-// Every wait is on an mbarrier with a bounded spin; a timeout sets the device
-// status word instead of hanging.
+// The three issuer warps run their loops with all 32 lanes (descriptors and ring
+// indices computed warp-uniformly) and issue each MMA and commit from one lane
+// chosen by elect.sync.  Every wait is on an mbarrier with a bounded spin; a
+// timeout sets the device status word instead of hanging.
 #include <math.h>
 
 #include <algorithm>
