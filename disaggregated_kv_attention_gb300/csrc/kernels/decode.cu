@@ -22,8 +22,8 @@
 //                   S    = K . Q^T                  [128 keys x 16]   K from TMEM
 //                 (K and S in rings of three in tensor memory)
 //     warps 2..9  RoPE group, one key per thread and half of the columns per
-//                 warp: K = Kb + RoPE_j(U), the rotation of the (small) residual
-//                 term in bf16x2 and one rounding of K, written to tensor memory
+//                 warp: K = Kb + RoPE_j(U) in bf16x2 fused multiply-adds onto Kb
+//                 (K rounded twice at its own scale), written to tensor memory
 //                 as the A operand of the score product
 //     warps 10..13 softmax group, one key per thread: scores, length mask, block
 //                 maxima across the group, lazy rescale of O (only when the
@@ -801,16 +801,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           for (int i2 = 0; i2 < 8; ++i2) {  // frequency group c/2 + i2: frequencies of d = c + 2 i2, + 1
             const uint4 w = rp[cc][(i2 >> 2) * 2 + ((i2 & 3) >> 1)];
             const uint32_t cw = (i2 & 1) ? w.z : w.x, sw = (i2 & 1) ? w.w : w.y;
-            // the rotated residual term in bf16x2 (its roundings are at the residual's scale), then
-            // one bf16 rounding of K = Kb + RoPE_j(U)
+            // K = Kb + RoPE_j(U) in two fused multiply-adds per bf16x2 pair: Kb - U_hi sin,
+            // then + U_lo cos (and Kb + U_lo sin, then + U_hi cos), each rounded to bf16 at K's
+            // scale (two roundings of K instead of one: measured rel_l2 3.4e-3 against 2.9e-3, for
+            // a third fewer rotation instructions)
             const __nv_bfloat162 C = *reinterpret_cast<const __nv_bfloat162*>(&cw);
             const __nv_bfloat162 S = *reinterpret_cast<const __nv_bfloat162*>(&sw);
             const __nv_bfloat162 UL = *reinterpret_cast<const __nv_bfloat162*>(&ul[cc][i2]);
             const __nv_bfloat162 UH = *reinterpret_cast<const __nv_bfloat162*>(&uh[cc][i2]);
-            const __nv_bfloat162 rl = __hfma2(__hneg2(UH), S, __hmul2(UL, C));
-            const __nv_bfloat162 rh = __hfma2(UH, C, __hmul2(UL, S));
-            const __nv_bfloat162 kl2 = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&klw[i2]), rl);
-            const __nv_bfloat162 kh2 = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&khw[i2]), rh);
+            const __nv_bfloat162 kl2 =
+                __hfma2(UL, C, __hfma2(__hneg2(UH), S, *reinterpret_cast<const __nv_bfloat162*>(&klw[i2])));
+            const __nv_bfloat162 kh2 = __hfma2(UH, C, __hfma2(UL, S, *reinterpret_cast<const __nv_bfloat162*>(&khw[i2])));
             olo[i2] = *reinterpret_cast<const uint32_t*>(&kl2);
             ohi[i2] = *reinterpret_cast<const uint32_t*>(&kh2);
           }
