@@ -956,12 +956,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kRed0 + (m & 1)]);
         // while the other warps' maxima come in: probabilities against the current reference
+        // (a masked score is -inf, and 2^-inf = 0: no mask is needed on the probabilities)
         float mr[kG], ps[kG];
-#pragma unroll
-        for (int q = 0; q < kG; ++q) {
-          mr[q] = mref[ai * 8 + q];
-          ps[q] = (vis && q < G) ? ex2(sc[q] - (mr[q] == -INFINITY ? 0.f : mr[q])) : 0.f;
+        {
+          const float4* m4 = reinterpret_cast<const float4*>(mref + ai * 8);
+          const float4 x0 = m4[0];
+          mr[0] = x0.x;
+          mr[1] = x0.y;
+          mr[2] = x0.z;
+          mr[3] = x0.w;
+          if constexpr (kG == 8) {
+            const float4 x1 = m4[1];
+            mr[4 % kG] = x1.x;
+            mr[5 % kG] = x1.y;
+            mr[6 % kG] = x1.z;
+            mr[7 % kG] = x1.w;
+          }
         }
+#pragma unroll
+        for (int q = 0; q < kG; ++q) ps[q] = ex2(sc[q] - (mr[q] == -INFINITY ? 0.f : mr[q]));
         ok = mbar_wait_s(&bars[kRed0 + (m & 1)], (m >> 1) & 1, a.status);
         if (!ok) break;
         // lazy rescale: keep the reference maximum unless the block maximum passes it by 2^8
@@ -1001,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           __syncwarp();
           if (publisher) mref[ai * 8 + gl] = ml;
 #pragma unroll
-          for (int q = 0; q < kG; ++q) ps[q] = (vis && q < G) ? ex2(sc[q] - mr[q]) : 0.f;
+          for (int q = 0; q < kG; ++q) ps[q] = mr[q] == -INFINITY ? 0.f : ex2(sc[q] - mr[q]);
           if (b > 0) {
             // O^T and R are stable once the value products of block g - 1 are done (one barrier
             // per block parity, so a wait is never more than one phase ahead of the barrier)
