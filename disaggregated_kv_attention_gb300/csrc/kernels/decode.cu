@@ -342,6 +342,11 @@ __device__ __forceinline__ float warp_max(float v) {
   return r;
 }
 
+// The reference maximum of a (unit, agent, query head) before any visible key: a finite floor
+// rather than -inf, so that s - m is never -inf - (-inf) and needs no guard.  The first visible
+// key always passes it by 2^8 and sets the reference; the epilogue reports the floor as -inf.
+constexpr float kNoMax = -3.4028234663852886e38f;
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -907,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       const int32_t slot_base = unit_at(k, kUfSlot);
       const bool end = unit_at(k, kUfEnd) != 0;
       __syncwarp();
-      mref[lane] = -INFINITY;  // 4 agents x 8 query heads
+      mref[lane] = kNoMax;  // 4 agents x 8 query heads
       if (lane < kMaxGroup) {
         lp[2 * lane] = unit_at(k, kUfL + lane);  // 0 past the unit's agents
         lp[2 * lane + 1] = unit_at(k, kUfPos + lane);
@@ -956,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kRed0 + (m & 1)]);
         // while the other warps' maxima come in: probabilities against the current reference
-        // (a masked score is -inf, and 2^-inf = 0: no mask is needed on the probabilities)
+        // (a masked score is -inf and the reference is finite, so 2^(s - m) = 0 needs no mask)
         float mr[kG], ps[kG];
         {
           const float4* m4 = reinterpret_cast<const float4*>(mref + ai * 8);
@@ -974,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           }
         }
 #pragma unroll
-        for (int q = 0; q < kG; ++q) ps[q] = ex2(sc[q] - (mr[q] == -INFINITY ? 0.f : mr[q]));
+        for (int q = 0; q < kG; ++q) ps[q] = ex2(sc[q] - mr[q]);
         ok = mbar_wait_s(&bars[kRed0 + (m & 1)], (m >> 1) & 1, a.status);
         if (!ok) break;
         // lazy rescale: keep the reference maximum unless the block maximum passes it by 2^8
@@ -1004,7 +1009,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
 #pragma unroll
           for (int q = 0; q < kG; ++q) {
             const bool need = q < G && bm[q] > mr[q] + 8.f;
-            alpha[q] = (need && mr[q] != -INFINITY) ? ex2(mr[q] - bm[q]) : 1.f;
+            // from the floor kNoMax, alpha = 0: O and R hold only zero probabilities until then
+            alpha[q] = need ? ex2(mr[q] - bm[q]) : 1.f;
             if (need) mr[q] = bm[q];
           }
           float ml = mr[0];
@@ -1014,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
           __syncwarp();
           if (publisher) mref[ai * 8 + gl] = ml;
 #pragma unroll
-          for (int q = 0; q < kG; ++q) ps[q] = mr[q] == -INFINITY ? 0.f : ex2(sc[q] - mr[q]);
+          for (int q = 0; q < kG; ++q) ps[q] = ex2(sc[q] - mr[q]);
           if (b > 0) {
             // O^T and R are stable once the value products of block g - 1 are done (one barrier
             // per block parity, so a wait is never more than one phase ahead of the barrier)
@@ -1079,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
               a.part[(rec0 + q) * kPartCols + row] = nb > 0 ? __uint_as_float(ov[q]) : 0.f;
               if (r >= 0 && r < kRank) a.part[(rec0 + q) * kPartCols + kHeadDim + r] = nb > 0 ? __uint_as_float(rv[q]) : 0.f;
               if (row == kRank * na) {  // first row of the ones product: l
-                a.ml[(rec0 + q) * 2] = nb > 0 ? mref[ai * 8 + q] : -INFINITY;
+                a.ml[(rec0 + q) * 2] = nb > 0 && mref[ai * 8 + q] != kNoMax ? mref[ai * 8 + q] : -INFINITY;
                 a.ml[(rec0 + q) * 2 + 1] = nb > 0 ? __uint_as_float(rv[q]) : 0.f;
               }
             }
