@@ -140,7 +140,7 @@ enum {
   kUfHole = 22                                           // hole (16 * first slot + length, 0: none)
 };
 constexpr int kOffUnits = 1408;  // 2 x kUnitInts int32 in the header of shared memory
-constexpr int kOffHoles = 1664;  // the softmax warps' copies of the unit's hole codes
+constexpr int kOffHoles = 1664;  // the softmax warps' copies of each agent's hole end
 static_assert(kOffUnits + 2 * kUnitInts * 4 <= kOffHoles && kOffHoles + 4 * kMaxGroup * 4 <= 2048,
               "unit ring and hole codes overlap each other or the operand tiles");
 
@@ -368,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 384);
   float* s_red = reinterpret_cast<float*>(smem + 512);      // [2][4 warps][8] block maxima
   float* s_mref = reinterpret_cast<float*>(smem + 768);     // [4 warps][4 agents][8] reference maxima
-  int32_t* s_lp = reinterpret_cast<int32_t*>(smem + 1280);  // [4 warps][4 agents][2] length, position
+  int32_t* s_lp = reinterpret_cast<int32_t*>(smem + 1280);  // [4 warps][4 agents][2] visible limit, hole start
   int32_t* s_units = reinterpret_cast<int32_t*>(smem + kOffUnits);  // [2][kUnitInts] unit descriptors
-  int32_t* s_lh = reinterpret_cast<int32_t*>(smem + kOffHoles);      // [4 warps][4 agents] hole codes
+  int32_t* s_lh = reinterpret_cast<int32_t*>(smem + kOffHoles);      // [4 warps][4 agents] hole end
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.G;
@@ -899,8 +899,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
     const int row = 32 * sw_ + lane;  // key row of the block == TMEM lane (and d row of O^T)
     const uint32_t tl = tm + ((uint32_t)(32 * sw_) << 16);
     float* mref = s_mref + sw_ * (kMaxGroup * 8);  // this warp's copy (all four evolve identically)
-    int32_t* lp = s_lp + sw_ * (kMaxGroup * 2);    // this warp's copy of each agent's (length, position)
-    int32_t* lh = s_lh + sw_ * kMaxGroup;          // and of each agent's hole code
+    int32_t* lp = s_lp + sw_ * (kMaxGroup * 2);    // this warp's copy of each agent's (visible limit, hole start)
+    int32_t* lh = s_lh + sw_ * kMaxGroup;          // and of each agent's hole end
     // query head whose reference maximum this lane publishes after a rescale, and the publishing lanes
     const int gl = kG == 8 ? lane >> 2 : lane >> 3;
     const bool publisher = kG == 8 ? (lane & 3) == 0 : (lane & 7) == 0;
@@ -914,9 +914,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
       __syncwarp();
       mref[lane] = kNoMax;  // 4 agents x 8 query heads
       if (lane < kMaxGroup) {
-        lp[2 * lane] = unit_at(k, kUfL + lane);  // 0 past the unit's agents
-        lp[2 * lane + 1] = unit_at(k, kUfPos + lane);
-        lh[lane] = unit_at(k, kUfHole + lane);
+        // Agent `lane`'s visible slots: j < lim, outside its hole [hlo, hhi).  The key in slot j
+        // sits at position j, or j - hole length past the hole, so a query at position pos sees
+        // slot j up to pos (pos before the hole) or pos + hole length (pos past it); slots past
+        // the agent's length or the unit's pages are never visible.
+        const int32_t L = unit_at(k, kUfL + lane), pos = unit_at(k, kUfPos + lane);  // L: 0 past the unit's agents
+        const int32_t hc = unit_at(k, kUfHole + lane), hs = hc >> 4, hn = hc & 15;
+        const int32_t last = (hn != 0 && pos >= hs) ? pos + hn : pos;  // the query's own slot
+        lp[2 * lane] = min(min(L, p1 * kPage), last + 1);
+        lp[2 * lane + 1] = hs;
+        lh[lane] = hs + hn;
       }
       unit_release(k);
       if (end) break;
@@ -927,12 +934,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
         const int g = gb + b, m = gn + n;  // global block and step
         const int pbase = p0 + b * kBlockPages;
         const int j = pbase * kPage + row;
-        const int32_t L = lp[2 * ai], pos = lp[2 * ai + 1], hc = lh[ai];
-        // slot j: hidden in the agent's hole; past it, its key position is j - hole length
-        const int32_t hs = hc >> 4, hn = hc & 15;
-        const bool in_hole = hn != 0 && j >= hs && j < hs + hn;
-        const int32_t kp = (hn != 0 && j >= hs + hn) ? j - hn : j;
-        const bool vis = j < L && !in_hole && kp <= pos && j < p1 * kPage;
+        const int2 lim_lo = reinterpret_cast<const int2*>(lp)[ai];  // (visible limit, hole start)
+        const bool vis = j < lim_lo.x && (j < lim_lo.y || j >= lh[ai]);
         ok = mbar_wait_tc(&bars[kSFull0 + sr], sp, a.status);
         if (!ok) break;
         tc::fence_after();
@@ -1001,14 +1004,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_split_kernel(const __grid_
               v[w] = (q & 3) == 0 ? y.x : (q & 3) == 1 ? y.y : (q & 3) == 2 ? y.z : y.w;
             }
             bm[q] = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-            need_any |= q < G && bm[q] > mr[q] + 8.f;
+            need_any |= bm[q] > mr[q] + 8.f;  // heads past G: -inf scores, never a rescale
           }
         }
         if (need_any) {  // uniform across the group: every warp saw the same maxima
           float alpha[kG];
 #pragma unroll
           for (int q = 0; q < kG; ++q) {
-            const bool need = q < G && bm[q] > mr[q] + 8.f;
+            const bool need = bm[q] > mr[q] + 8.f;
             // from the floor kNoMax, alpha = 0: O and R hold only zero probabilities until then
             alpha[q] = need ? ex2(mr[q] - bm[q]) : 1.f;
             if (need) mr[q] = bm[q];
