@@ -348,3 +348,33 @@ def test_cpp_freeze_fanout_matches_model():
         pr.op("free", root)
         pr.check_state()
         pr.close()
+
+
+def test_plan_deals_sibling_groups_side_by_side():
+    """Agent groups that read the same trunk pages (one segment, split into groups of 4) are dealt,
+    for the same pages and KV head, to consecutive CTAs of the first round, so that they stream
+    those pages at the same time (the planner's order: cost, segment, first block, head, group;
+    each unit to the least loaded CTA, so CTA c's first unit is the c-th)."""
+    rnd = random.Random(11)
+    bpt, lens = _tree_tables(rnd, [16, 16], (4096, 256))  # 32 agents on one root, 2 trunks of 16
+    hkv = 8
+    plan, info = fk.forkkv_plan_build(bpt, lens, hkv, 0)
+    items = plan[:info.n_items * fk.PLAN_ITEM_INTS].reshape(info.n_items, fk.PLAN_ITEM_INTS)
+    rest = plan[info.n_items * fk.PLAN_ITEM_INTS + len(lens) + 1:]
+    units = rest[info.n_slots:].reshape(info.n_units, fk.PLAN_UNIT_INTS)
+    by_slot = {it[12]: i for i, it in enumerate(items)}
+    cost = lambda it: ((it[1] - it[0] + 7) // 8) * max(930 * it[2], 2400) + 3000
+    siblings = {}
+    for c in range(info.n_ctas):  # record c is CTA c's first unit
+        u = units[c]
+        it = items[by_slot[u[4]]]
+        p0, p1 = int(it[0]), int(it[1])
+        key = (cost(it), p0, p1, int(bpt[it[4], p0]), int(u[3]))  # same pages (physical), same head
+        siblings.setdefault(key, []).append((c, tuple(int(a) for a in it[4:4 + it[2]])))
+    groups = [v for v in siblings.values() if len(v) > 1]
+    assert groups, "the scenario must put sibling groups in the first round"
+    for v in groups:
+        cs = [c for c, _ in v]
+        assert cs == list(range(cs[0], cs[0] + len(cs))), v  # consecutive CTAs
+        agent_sets = [set(ags) for _, ags in v]
+        assert all(not (x & y) for i, x in enumerate(agent_sets) for y in agent_sets[i + 1:])  # distinct groups
